@@ -1,0 +1,162 @@
+/*
+ * i8ql -- int8 quantized linear layers on GB300 (sm_103a).
+ *
+ * C ABI of libi8ql.so.  Five operations make up the quantized linear layer
+ * of LLM serving: per-output-channel weight quantization, per-token
+ * activation quantization, the W8A8 GEMM with its scale/bias epilogue, the
+ * weight-only W8A16 GEMM/GEMV, and the grouped W8A16 GEMM over MoE experts.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer is a DEVICE pointer to a buffer the caller owns, allocates
+ *    and frees.  The library keeps no copy of any weight or activation.
+ *  - Matrices are dense row-major with no padding: an [R, K] matrix stores
+ *    element (r, k) at r * K + k.  bf16 values are passed as their raw
+ *    16-bit patterns (i8ql_bf16).  Matrix base pointers must be 16-byte
+ *    aligned; scale and offset arrays 4-byte aligned; bias 2-byte aligned.
+ *  - K must be a positive multiple of 16 and at most I8QL_MAX_K.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Calls only enqueue work: they return before the GPU finishes
+ *    and never synchronise the host.
+ *  - Errors are returned, never thrown or trapped.  Argument errors are
+ *    found on the host before anything is launched.  Faults seen by a
+ *    running kernel (a bounded wait that gave up, bad group offsets) are
+ *    recorded in a per-device sticky word, read by i8ql_get_device_error.
+ *  - A call with an empty problem (M = 0 or T_total = 0) returns I8QL_OK and
+ *    launches nothing.
+ *  - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ */
+#ifndef I8QL_H
+#define I8QL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t i8ql_bf16; /* raw bfloat16 bits */
+typedef int32_t i8ql_status;
+
+enum {
+    I8QL_OK = 0,
+    I8QL_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer  */
+    I8QL_ERR_UNSUPPORTED = 2,  /* K not a multiple of 16, K > I8QL_MAX_K, size too large */
+    I8QL_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed          */
+    I8QL_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (sticky word)        */
+    I8QL_ERR_BAD_OFFSETS = 5,  /* grouped offsets not 0 .. T_total, non-decreasing     */
+    I8QL_ERR_NO_DEVICE = 6     /* no CUDA device, or not an sm_103 device              */
+};
+
+/* Largest K whose worst-case int8 dot product fits int32:
+ * floor((2^31 - 1) / 127^2) = 133,144. */
+#define I8QL_MAX_K 133144
+
+/*
+ * Per-output-channel symmetric int8 weight quantization.
+ *
+ * Source: "Phase 5a: int8 weight-only quantization", Summary (self-computed
+ * per-output-channel int8 weights; float32 scale arithmetic; a zero-channel
+ * guard that touches only all-zero channels) and "Day 6 -- Quantize It
+ * Yourself", The mechanism, blocks 1 and 4 (q = clamp(round(w / s)),
+ * s = absmax / qmax, round-to-nearest).
+ *
+ * For every row n of w (bf16 [N, K], one row per output channel):
+ *   a = max_k |w[n,k]|;  scale[n] = a / 127 (fp32 IEEE division), or 1 if a == 0;
+ *   q[n,k] = clamp(rint(w[n,k] / scale[n]), -127, 127), ties to even,
+ *            one IEEE fp32 division per element, no flush of subnormals.
+ * Outputs: q int8 [N, K], scale fp32 [N].  N >= 0.
+ */
+i8ql_status quantize_weight_per_channel_int8(const i8ql_bf16* w, int64_t N, int64_t K,
+                                             int8_t* q, float* scale, void* stream);
+
+/*
+ * Dynamic symmetric per-token int8 activation quantization.
+ *
+ * Source: "feat(quantization): support compressed-tensors W8A8 and mixed
+ * modules", Design and Supported Execution Scheme (dynamic symmetric INT8
+ * per-token input activations) and "Day 6 -- Quantize It Yourself", The
+ * mechanism, block 5 (per-token dynamic scales computed on the fly).
+ *
+ * The same arithmetic as quantize_weight_per_channel_int8, applied to each
+ * token row m of x (bf16 [M, K]).  Outputs: q int8 [M, K], scale fp32 [M].
+ */
+i8ql_status quantize_act_per_token_int8(const i8ql_bf16* x, int64_t M, int64_t K,
+                                        int8_t* q, float* scale, void* stream);
+
+/*
+ * W8A8 GEMM: int8 x int8 -> exact int32, then the scale/bias epilogue.
+ *
+ * Source: "feat(quantization): support compressed-tensors W8A8 and mixed
+ * modules", Design and Supported Execution Scheme (static per-channel int8
+ * weights, dynamic per-token int8 activations, no output quantization) and
+ * "Day 6 -- Quantize It Yourself", The mechanism, block 5 (W8A8 runs the GEMM
+ * on 8-bit operands).
+ *
+ *   acc[m,n] = sum_k qx[m,k] * qw[n,k]                      (exact int32)
+ *   y[m,n]   = bf16_rne(((float)acc[m,n] * sx[m]) * sw[n] (+ (float)bias[n]))
+ * Inputs: qx int8 [M, K], sx fp32 [M], qw int8 [N, K] (both K-contiguous),
+ * sw fp32 [N], bias bf16 [N] or NULL.  Outputs: y bf16 [M, N]; acc_debug
+ * int32 [M, N] or NULL (when given, receives the exact accumulator).
+ * The epilogue may fuse multiply-adds: y is within one bf16 ulp of the
+ * value above.
+ */
+i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                      const i8ql_bf16* bias, i8ql_bf16* y, int32_t* acc_debug,
+                      int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Weight-only W8A16 GEMM / GEMV (decode).
+ *
+ * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 5 (int8
+ * weights dequantized inside the kernel, the product on bf16 math: a
+ * memory-bandwidth win) and "Phase 5a: int8 weight-only quantization",
+ * Summary (weight-only quantization saves memory bandwidth, not FLOPs).
+ *
+ *   y[m,n] = bf16_rne(sw[n] * sum_k q[n,k] * x[m,k])
+ * with bf16 x [M, K], int8 qw [N, K], fp32 sw [N]; y bf16 [M, N].  The codes
+ * enter the bf16 product exactly and the fp32 scale is applied once per
+ * output, so s * q is never rounded to bf16.  Accumulation is fp32.  Any M
+ * is accepted; the kernels are built for M <= 64.
+ */
+i8ql_status w8a16_gemm(const i8ql_bf16* x, const int8_t* qw, const float* sw, i8ql_bf16* y,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Grouped W8A16 over MoE experts.
+ *
+ * Source: "Phase 5a: int8 weight-only quantization", Summary (a grouped
+ * GEMM over MoE experts on stacked [E, N, K] expert weights with
+ * per-output-channel int8 scales).
+ *
+ * Rows offsets[e] .. offsets[e+1]-1 of x (bf16 [T_total, K], grouped by
+ * expert) go through expert e:
+ *   y[r,n] = bf16_rne(sw[e,n] * sum_k qw[e,n,k] * x[r,k]).
+ * offsets: int32 [E + 1] in DEVICE memory, offsets[0] = 0, non-decreasing,
+ * offsets[E] = T_total; the host never reads it.  An expert with no rows
+ * reads none of its weights.  If the offsets break these rules the kernel
+ * skips the bad experts and records I8QL_ERR_BAD_OFFSETS in the sticky word.
+ * qw int8 [E, N, K], sw fp32 [E, N], y bf16 [T_total, N].  E >= 1.
+ */
+i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64_t E,
+                               const int8_t* qw, const float* sw, i8ql_bf16* y,
+                               int64_t T_total, int64_t N, int64_t K, void* stream);
+
+/*
+ * Waits for `stream`, then reads and clears the current device's sticky
+ * kernel-error word.  Returns I8QL_OK, I8QL_ERR_TIMEOUT or
+ * I8QL_ERR_BAD_OFFSETS (the first fault recorded since the last read), or
+ * I8QL_ERR_CUDA if the wait itself failed.
+ */
+i8ql_status i8ql_get_device_error(void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* i8ql_status_string(i8ql_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t i8ql_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* I8QL_H */

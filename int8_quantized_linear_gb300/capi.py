@@ -1,0 +1,190 @@
+"""Python binding of ``libi8ql.so`` (argument marshalling only).
+
+Each function keeps the name of its C entry point, takes torch CUDA tensors,
+checks dtypes, shapes and contiguity, allocates any output the caller did not
+pass (torch is only the device-memory and stream provider), and calls the C
+ABI with raw device pointers and the current CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.  If the
+library is missing, loading fails with an error that says how to build it.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libi8ql.so")
+
+I8QL_OK = 0
+I8QL_ERR_INVALID_ARG = 1
+I8QL_ERR_UNSUPPORTED = 2
+I8QL_ERR_CUDA = 3
+I8QL_ERR_TIMEOUT = 4
+I8QL_ERR_BAD_OFFSETS = 5
+I8QL_ERR_NO_DEVICE = 6
+I8QL_MAX_K = 133144
+
+# Every symbol the C header declares, with its ctypes signature.
+_P, _I64, _S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+SIGNATURES = {
+    "quantize_weight_per_channel_int8": (_S, [_P, _I64, _I64, _P, _P, _P]),
+    "quantize_act_per_token_int8": (_S, [_P, _I64, _I64, _P, _P, _P]),
+    "w8a8_gemm": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w8a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "grouped_w8a16_gemm": (_S, [_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "i8ql_get_device_error": (_S, [_P]),
+    "i8ql_status_string": (ctypes.c_char_p, [_S]),
+    "i8ql_version": (_S, []),
+}
+
+_LIB = None
+
+
+class I8qlError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIBRARY):
+            raise ImportError(
+                f"{LIBRARY} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        handle = ctypes.CDLL(LIBRARY)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def status_string(status: int) -> str:
+    return lib().i8ql_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != I8QL_OK:
+        raise I8qlError(status, where)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, shape: tuple, name: str) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.numel() and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _quant(fn_name: str, src: torch.Tensor, q, scale, stream):
+    if src.dim() != 2:
+        raise ValueError("input must be 2-D [rows, K]")
+    rows, k = src.shape
+    _need(src, torch.bfloat16, (rows, k), "input")
+    if q is None:
+        q = torch.empty((rows, k), dtype=torch.int8, device=src.device)
+    if scale is None:
+        scale = torch.empty((rows,), dtype=torch.float32, device=src.device)
+    _need(q, torch.int8, (rows, k), "q")
+    _need(scale, torch.float32, (rows,), "scale")
+    st = getattr(lib(), fn_name)(_ptr(src), rows, k, _ptr(q), _ptr(scale), _stream(stream))
+    _check(st, fn_name)
+    return q, scale
+
+
+def quantize_weight_per_channel_int8(w: torch.Tensor, q=None, scale=None, stream=None):
+    """int8 codes [N, K] and fp32 per-output-channel scales [N] of bf16 w."""
+    return _quant("quantize_weight_per_channel_int8", w, q, scale, stream)
+
+
+def quantize_act_per_token_int8(x: torch.Tensor, q=None, scale=None, stream=None):
+    """int8 codes [M, K] and fp32 per-token scales [M] of bf16 x."""
+    return _quant("quantize_act_per_token_int8", x, q, scale, stream)
+
+
+def w8a8_gemm(qx, sx, qw, sw, bias=None, y=None, acc_debug=None, stream=None):
+    """bf16 y [M, N] = ((float)(qx @ qw^T) * sx[:, None]) * sw[None, :] (+ bias)."""
+    m, k = qx.shape
+    n = qw.shape[0]
+    _need(qx, torch.int8, (m, k), "qx")
+    _need(sx, torch.float32, (m,), "sx")
+    _need(qw, torch.int8, (n, k), "qw")
+    _need(sw, torch.float32, (n,), "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (n,), "bias")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=qw.device)
+    _need(y, torch.bfloat16, (m, n), "y")
+    if acc_debug is not None:
+        _need(acc_debug, torch.int32, (m, n), "acc_debug")
+    st = lib().w8a8_gemm(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y),
+                         _ptr(acc_debug), m, n, k, _stream(stream))
+    _check(st, "w8a8_gemm")
+    return y
+
+
+def w8a16_gemm(x, qw, sw, y=None, stream=None):
+    """bf16 y [M, N] = bf16(sw[n] * sum_k qw[n, k] * x[m, k])."""
+    m, k = x.shape
+    n = qw.shape[0]
+    _need(x, torch.bfloat16, (m, k), "x")
+    _need(qw, torch.int8, (n, k), "qw")
+    _need(sw, torch.float32, (n,), "sw")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=qw.device)
+    _need(y, torch.bfloat16, (m, n), "y")
+    st = lib().w8a16_gemm(_ptr(x), _ptr(qw), _ptr(sw), _ptr(y), m, n, k, _stream(stream))
+    _check(st, "w8a16_gemm")
+    return y
+
+
+def grouped_w8a16_gemm(x, offsets, qw, sw, y=None, stream=None):
+    """Grouped W8A16: rows offsets[e] .. offsets[e+1] of x use expert e."""
+    t, k = x.shape
+    e, n, k2 = qw.shape
+    if k2 != k:
+        raise ValueError("qw and x disagree on K")
+    _need(x, torch.bfloat16, (t, k), "x")
+    _need(offsets, torch.int32, (e + 1,), "offsets")
+    _need(qw, torch.int8, (e, n, k), "qw")
+    _need(sw, torch.float32, (e, n), "sw")
+    if y is None:
+        y = torch.empty((t, n), dtype=torch.bfloat16, device=qw.device)
+    _need(y, torch.bfloat16, (t, n), "y")
+    st = lib().grouped_w8a16_gemm(_ptr(x), _ptr(offsets), e, _ptr(qw), _ptr(sw), _ptr(y), t, n, k,
+                                  _stream(stream))
+    _check(st, "grouped_w8a16_gemm")
+    return y
+
+
+def i8ql_get_device_error(stream=None) -> int:
+    """Wait for the stream, then read and clear the sticky kernel-fault word."""
+    return int(lib().i8ql_get_device_error(_stream(stream)))
+
+
+def i8ql_version() -> int:
+    return int(lib().i8ql_version())

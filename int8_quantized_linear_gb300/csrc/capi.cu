@@ -1,0 +1,234 @@
+// C ABI of libi8ql.so: argument validation, per-device state and dispatch.
+//
+// Every entry point validates its arguments on the host before touching the
+// CUDA runtime, so argument errors never launch anything and can be tested
+// without a GPU.
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace i8ql {
+
+// The sticky kernel-fault word; one instance per device context.
+__device__ unsigned g_kernel_faults;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::atomic<bool> ready{false};
+    unsigned* err = nullptr;
+    int sm_count = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+i8ql_status check_k(int64_t K) {
+    if (K <= 0) return I8QL_ERR_INVALID_ARG;
+    if (K % 16 != 0 || K > I8QL_MAX_K) return I8QL_ERR_UNSUPPORTED;
+    return I8QL_OK;
+}
+
+i8ql_status check_rows(int64_t R) {
+    if (R < 0) return I8QL_ERR_INVALID_ARG;
+    if (R >= kMaxRows) return I8QL_ERR_UNSUPPORTED;
+    return I8QL_OK;
+}
+
+i8ql_status check_matrix(const void* p, int64_t rows) {
+    if (rows == 0) return I8QL_OK;
+    if (p == nullptr || !aligned(p, 16)) return I8QL_ERR_INVALID_ARG;
+    return I8QL_OK;
+}
+
+i8ql_status check_vec(const void* p, int64_t n, uintptr_t align) {
+    if (n == 0) return I8QL_OK;
+    if (p == nullptr || !aligned(p, align)) return I8QL_ERR_INVALID_ARG;
+    return I8QL_OK;
+}
+
+#define I8QL_TRY(expr)                       \
+    do {                                     \
+        i8ql_status _s = (expr);             \
+        if (_s != I8QL_OK) return _s;        \
+    } while (0)
+
+i8ql_status from_cuda(cudaError_t e) { return e == cudaSuccess ? I8QL_OK : I8QL_ERR_CUDA; }
+
+}  // namespace
+
+bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        *status = I8QL_ERR_NO_DEVICE;
+        return false;
+    }
+    DeviceState& st = g_devices[dev];
+    if (!st.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!st.ready.load(std::memory_order_relaxed)) {
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+                cudaGetLastError();
+                *status = I8QL_ERR_CUDA;
+                return false;
+            }
+            if (major != 10 || minor != 3) {
+                *status = I8QL_ERR_NO_DEVICE;
+                return false;
+            }
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_kernel_faults) != cudaSuccess) {
+                cudaGetLastError();
+                *status = I8QL_ERR_CUDA;
+                return false;
+            }
+            st.err = static_cast<unsigned*>(addr);
+            st.sm_count = sms;
+            st.ready.store(true, std::memory_order_release);
+        }
+    }
+    env->stream = static_cast<cudaStream_t>(stream);
+    env->err = st.err;
+    env->sm_count = st.sm_count;
+    return true;
+}
+
+}  // namespace i8ql
+
+using namespace i8ql;
+
+extern "C" {
+
+i8ql_status quantize_weight_per_channel_int8(const i8ql_bf16* w, int64_t N, int64_t K, int8_t* q,
+                                             float* scale, void* stream) {
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_k(K));
+    I8QL_TRY(check_matrix(w, N));
+    I8QL_TRY(check_matrix(q, N));
+    I8QL_TRY(check_vec(scale, N, 4));
+    if (N == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_quant_rows(w, N, K, q, scale, env));
+}
+
+i8ql_status quantize_act_per_token_int8(const i8ql_bf16* x, int64_t M, int64_t K, int8_t* q,
+                                        float* scale, void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    I8QL_TRY(check_matrix(x, M));
+    I8QL_TRY(check_matrix(q, M));
+    I8QL_TRY(check_vec(scale, M, 4));
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_quant_rows(x, M, K, q, scale, env));
+}
+
+i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                      const i8ql_bf16* bias, i8ql_bf16* y, int32_t* acc_debug, int64_t M, int64_t N,
+                      int64_t K, void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_matrix(qx, M));
+    I8QL_TRY(check_vec(sx, M, 4));
+    I8QL_TRY(check_matrix(qw, N));
+    I8QL_TRY(check_vec(sw, N, 4));
+    if (bias != nullptr && !aligned(bias, 2)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_matrix(y, M));
+    if (acc_debug != nullptr && !aligned(acc_debug, 16)) return I8QL_ERR_INVALID_ARG;
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_w8a8(qx, sx, qw, sw, bias, y, acc_debug, M, N, K, env));
+}
+
+i8ql_status w8a16_gemm(const i8ql_bf16* x, const int8_t* qw, const float* sw, i8ql_bf16* y,
+                       int64_t M, int64_t N, int64_t K, void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_matrix(x, M));
+    I8QL_TRY(check_matrix(qw, N));
+    I8QL_TRY(check_vec(sw, N, 4));
+    I8QL_TRY(check_matrix(y, M));
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_w8a16(x, nullptr, 1, qw, sw, y, M, N, K, env));
+}
+
+i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64_t E,
+                               const int8_t* qw, const float* sw, i8ql_bf16* y, int64_t T_total,
+                               int64_t N, int64_t K, void* stream) {
+    I8QL_TRY(check_rows(T_total));
+    I8QL_TRY(check_k(K));
+    if (N <= 0 || E <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    if (E > 65535) return I8QL_ERR_UNSUPPORTED;
+    if ((double)E * (double)N * (double)K > 9.0e18) return I8QL_ERR_UNSUPPORTED;
+    if (offsets == nullptr || !aligned(offsets, 4)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_matrix(x, T_total));
+    if (qw == nullptr || !aligned(qw, 16)) return I8QL_ERR_INVALID_ARG;
+    if (sw == nullptr || !aligned(sw, 4)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_matrix(y, T_total));
+    if (T_total == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_w8a16(x, offsets, E, qw, sw, y, T_total, N, K, env));
+}
+
+i8ql_status i8ql_get_device_error(void* stream) {
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    if (cudaStreamSynchronize(env.stream) != cudaSuccess) return I8QL_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, env.err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return I8QL_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(env.err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return I8QL_ERR_CUDA;
+    }
+    if (word & kErrBitTimeout) return I8QL_ERR_TIMEOUT;
+    if (word & kErrBitBadOffsets) return I8QL_ERR_BAD_OFFSETS;
+    return I8QL_OK;
+}
+
+const char* i8ql_status_string(i8ql_status status) {
+    switch (status) {
+        case I8QL_OK: return "ok";
+        case I8QL_ERR_INVALID_ARG: return "invalid argument (null, negative size or misaligned pointer)";
+        case I8QL_ERR_UNSUPPORTED: return "unsupported size (K must be a positive multiple of 16, at most 133144)";
+        case I8QL_ERR_CUDA: return "CUDA runtime or launch failure";
+        case I8QL_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+        case I8QL_ERR_BAD_OFFSETS: return "grouped offsets are not 0..T_total and non-decreasing";
+        case I8QL_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
+        default: return "unknown status";
+    }
+}
+
+int32_t i8ql_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Internal helpers shared by the i8ql CUDA sources (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/i8ql.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030)
+#error "i8ql kernels are written for sm_103a (GB300) only"
+#endif
+
+namespace i8ql {
+
+// Sticky per-device kernel fault word.  Kernels OR a status bit into it:
+constexpr unsigned kErrBitTimeout = 1u;
+constexpr unsigned kErrBitBadOffsets = 2u;
+
+// Largest supported sizes (indices stay well inside 64-bit arithmetic and
+// grid limits).
+constexpr int64_t kMaxRows = (int64_t)1 << 31;
+
+// Wall-clock limit of every bounded wait inside a kernel (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void record_fault(unsigned* err, unsigned bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// Launch parameters every entry point passes down.
+struct LaunchEnv {
+    cudaStream_t stream;
+    unsigned* err;   // device address of the sticky word of the current device
+    int sm_count;
+};
+
+// Returns the environment of the current device, creating per-device state
+// on first use.  Returns false (and sets *status) on failure.
+bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status);
+
+// Kernel launchers (one per operation).  They assume validated arguments.
+cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
+                              const LaunchEnv& env);
+cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw,
+                         const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                         const LaunchEnv& env);
+cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                        const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
+                        int64_t K, const LaunchEnv& env);
+
+}  // namespace i8ql

@@ -1,0 +1,149 @@
+// Per-row symmetric int8 quantization: per-output-channel weights and
+// per-token activations share this kernel.
+//
+// Sources: "Phase 5a: int8 weight-only quantization", Summary (per-output-
+// channel int8, float32 scale arithmetic, zero-channel guard only for
+// all-zero channels); "Day 6 -- Quantize It Yourself", The mechanism,
+// blocks 1, 4 and 5 (q = clamp(round(w / s)), s = absmax / 127, round to
+// nearest, per-token dynamic activation scales).
+//
+// One fused pass: each row is read once from HBM into registers (16-byte
+// vector loads), its absmax is reduced across the threads that own it, and
+// the codes are written from the same registers.  Rows longer than the
+// register budget are read a second time (an L2 hit).  The arithmetic is
+// IEEE fp32: __fdiv_rn for both a / 127 and v / s, __float2int_rn (ties to
+// even) for the rounding, no flush of subnormals (built without fast math).
+// HBM traffic: 2 bytes read + 1 byte written per element, plus 4 bytes per row.
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace i8ql {
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float absmax8(const uint4& v, float a) {
+    a = fmaxf(a, fabsf(lo_bf16(v.x)));
+    a = fmaxf(a, fabsf(hi_bf16(v.x)));
+    a = fmaxf(a, fabsf(lo_bf16(v.y)));
+    a = fmaxf(a, fabsf(hi_bf16(v.y)));
+    a = fmaxf(a, fabsf(lo_bf16(v.z)));
+    a = fmaxf(a, fabsf(hi_bf16(v.z)));
+    a = fmaxf(a, fabsf(lo_bf16(v.w)));
+    a = fmaxf(a, fabsf(hi_bf16(v.w)));
+    return a;
+}
+
+__device__ __forceinline__ uint32_t code(float v, float s) {
+    int c = __float2int_rn(__fdiv_rn(v, s));
+    c = max(-127, min(127, c));
+    return static_cast<uint32_t>(c) & 0xffu;
+}
+
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float s) {
+    return code(lo_bf16(w0), s) | (code(hi_bf16(w0), s) << 8) | (code(lo_bf16(w1), s) << 16) |
+           (code(hi_bf16(w1), s) << 24);
+}
+
+__device__ __forceinline__ uint4 load_nc(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// TPR threads own one row; VPT > 0 keeps up to VPT 8-element vectors per
+// thread in registers, VPT == 0 streams the row twice.
+template <int TPR, int VPT>
+__global__ void __launch_bounds__(kQuantThreads)
+quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
+                  int8_t* __restrict__ q, float* __restrict__ scale) {
+    constexpr int kRowsPerCta = kQuantThreads / TPR;
+    constexpr int kWarpsPerRow = TPR / 32;
+    __shared__ float warp_max[kQuantThreads / 32];
+
+    const int tid = threadIdx.x;
+    const int rloc = tid / TPR;
+    const int lt = tid % TPR;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + rloc;
+    const bool valid = row < rows;
+    const int64_t nvec = K / 8;
+    const uint4* rp = reinterpret_cast<const uint4*>(src) + (valid ? row : 0) * nvec;
+
+    constexpr int kRegs = VPT > 0 ? VPT : 1;
+    uint4 v[kRegs];
+    float a = 0.0f;
+    if constexpr (VPT > 0) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t idx = lt + (int64_t)i * TPR;
+            if (valid && idx < nvec) {
+                v[i] = load_nc(rp + idx);
+            } else {
+                v[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) a = absmax8(v[i], a);
+    } else {
+        if (valid)
+            for (int64_t idx = lt; idx < nvec; idx += TPR) a = absmax8(rp[idx], a);
+    }
+
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    if constexpr (kWarpsPerRow > 1) {
+        if ((tid & 31) == 0) warp_max[tid >> 5] = a;
+        __syncthreads();
+        const int w0 = rloc * kWarpsPerRow;
+#pragma unroll
+        for (int w = 0; w < kWarpsPerRow; ++w) a = fmaxf(a, warp_max[w0 + w]);
+    }
+
+    // Zero-channel guard: only an all-zero row is special.
+    const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 127.0f);
+    if (!valid) return;
+    if (lt == 0) scale[row] = s;
+
+    uint2* qp = reinterpret_cast<uint2*>(q + row * K);
+    if constexpr (VPT > 0) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t idx = lt + (int64_t)i * TPR;
+            if (idx < nvec) qp[idx] = make_uint2(codes4(v[i].x, v[i].y, s), codes4(v[i].z, v[i].w, s));
+        }
+    } else {
+        for (int64_t idx = lt; idx < nvec; idx += TPR) {
+            const uint4 u = rp[idx];
+            qp[idx] = make_uint2(codes4(u.x, u.y, s), codes4(u.z, u.w, s));
+        }
+    }
+}
+
+template <int TPR, int VPT>
+cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
+                       cudaStream_t stream) {
+    constexpr int kRowsPerCta = kQuantThreads / TPR;
+    const int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    quant_rows_kernel<TPR, VPT><<<dim3((unsigned)blocks), kQuantThreads, 0, stream>>>(src, rows, K, q, s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
+                              const LaunchEnv& env) {
+    const int64_t nvec = K / 8;
+    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, s, env.stream);
+    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, s, env.stream);
+    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, s, env.stream);
+    return launch_cfg<256, 0>(src, rows, K, q, s, env.stream);
+}
+
+}  // namespace i8ql

@@ -1,0 +1,508 @@
+// W8A8 GEMM: int8 x int8 -> exact int32 -> scale/bias epilogue -> bf16.
+//
+// Sources: "feat(quantization): support compressed-tensors W8A8 and mixed
+// modules", Design and Supported Execution Scheme (static symmetric int8
+// per-channel weights, dynamic symmetric int8 per-token activations, no
+// output quantization) and "Day 6 -- Quantize It Yourself", The mechanism,
+// block 5 (W8A8: both operands 8-bit, the GEMM on the tensor cores).
+//
+//   acc[m,n] = sum_k qx[m,k] * qw[n,k]          (exact int32)
+//   y[m,n]   = bf16_rne(((float)acc * sx[m]) * sw[n] (+ bias[n]))
+//
+// sm_103a has no integer kind of tcgen05.mma, so the product runs on the
+// fifth-generation tensor cores as kind::f16 with exact arithmetic:
+//  * every int8 code is exactly representable in fp16, and every product of
+//    two codes (|p| <= 16129) is exact in the fp32 accumulator;
+//  * the fp32 accumulator in tensor memory (TMEM) stays exact while its
+//    magnitude is below 2^24, which holds for any 1024-deep chunk of k
+//    (1024 * 127^2 = 16,516,096 < 16,777,216);
+//  * after each chunk the epilogue warps drain the fp32 chunk sum from TMEM,
+//    convert it to int32 (exact) and add it to an int32 running sum kept in
+//    a second TMEM region; the next chunk restarts the fp32 accumulator.
+//
+// Warp roles (416 threads, one CTA per output tile, 1 CTA per SM):
+//  * warps 0-3: epilogue (warp w owns TMEM lanes 32w .. 32w+31);
+//  * warp 4: TMEM allocation and the single-thread MMA issuer;
+//  * warps 5-12: converters.  They stream 16-byte int8 vectors from global
+//    memory, turn them into fp16 in registers (bias-and-subtract trick, exact),
+//    and store them in the 128-byte-swizzled K-major layout the MMA reads,
+//    through a 4-stage shared-memory ring guarded by mbarriers.
+// Tile: 128 rows of operand A x BN rows of operand B x 64 k per stage.
+// Large M: A = activations, B = weights, BN = 256.  M <= 128 ("swap AB"):
+// A = weights, B = tokens, BN = M rounded up to 16, so the tensor core does
+// no work on padding rows.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
+// records I8QL_ERR_TIMEOUT in the sticky fault word, all roles leave their
+// loops, the MMA issuer waits (bounded) for its outstanding MMAs, and the
+// TMEM is freed before the CTA exits.
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace i8ql {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kMaxBN = 256;
+constexpr int kChunkKB = 16;  // k-blocks per exact fp32 chunk (1024 k)
+constexpr int kEpiWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kThreads = (kEpiWarps + 1 + kConvWarps) * 32;
+constexpr int kAStageBytes = kBM * kBK * 2;
+constexpr int kBStageBytes = kMaxBN * kBK * 2;
+constexpr int kMaxConvItems = (kBM + kMaxBN) * 4 / kConvThreads;  // 16-byte vectors per thread per stage
+constexpr int kSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256 /*barriers*/;
+
+struct W8A8Params {
+    const int8_t* a;  // operand A rows (K contiguous)
+    const int8_t* b;  // operand B rows (K contiguous)
+    int64_t rows_a, rows_b, K;
+    const float* sx;
+    const float* sw;
+    const uint16_t* bias;
+    uint16_t* y;
+    int32_t* acc;
+    int64_t M, N;
+    int64_t tiles_b;
+    int bn;
+    int swap;
+    uint32_t tmem_cols;
+    unsigned* err;
+};
+
+struct SmemCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t drained;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity.  Returns false
+// if the CTA is aborting or the wall-clock limit expired (which starts the
+// abort and records the fault).
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, SmemCtl* ctl, unsigned* err) {
+    const uint32_t addr = smem_u32(bar);
+    uint64_t t0 = 0;
+    bool started = false;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try(addr, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+            const uint64_t now = global_ns();
+            if (!started) {
+                t0 = now;
+                started = true;
+            } else if (now - t0 > kWaitLimitNs) {
+                record_fault(err, kErrBitTimeout);
+                *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Every lane of a warp waits (each gets the barrier's acquire), then the
+// warp agrees: if any lane gave up, all of them take the abort path, so the
+// warp stays converged for the .sync.aligned tcgen05 instructions.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, SmemCtl* ctl, unsigned* err) {
+    const bool ok = mbar_wait(bar, parity, ctl, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3ffffu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset
+    d |= (uint64_t)1 << 46;            // version
+    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp16 A and B, fp32 D, both K-major.
+__device__ __forceinline__ uint32_t f16_idesc(int bn) {
+    return (1u << 4) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Four int8 codes -> two fp16x2 words (exact): the biased byte u = q + 128
+// becomes the low mantissa byte of fp16 1024 (value 1024 + u); subtracting
+// 1152 leaves q.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    lo = __byte_perm(u, 0x64646464u, 0x5150);
+    hi = __byte_perm(u, 0x64646464u, 0x5352);
+    asm("sub.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+    asm("sub.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* a_stages = smem;
+    uint8_t* b_stages = smem + kStages * kAStageBytes;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(b_stages + kStages * kBStageBytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t tile = blockIdx.x;
+    const int64_t tile_b = tile % p.tiles_b;
+    const int64_t tile_a = tile / p.tiles_b;
+    const int bn = p.bn;
+    const int64_t K = p.K;
+    const int nkb = (int)((K + kBK - 1) / kBK);
+    const int nchunks = (nkb + kChunkKB - 1) / kChunkKB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->full[s], kConvWarps);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->acc_full, 1);
+        mbar_init(&ctl->acc_empty, kEpiWarps);
+        mbar_init(&ctl->drained, 1);
+        ctl->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&ctl->tmem_base)),
+                     "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const uint32_t run_col = p.tmem_cols / 2;  // int32 running sum region
+
+    if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = f16_idesc(bn);
+            const uint32_t a_base = smem_u32(a_stages);
+            const uint32_t b_base = smem_u32(b_stages);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int st = kb % kStages;
+                if (kb > 0 && kb % kChunkKB == 0) {
+                    // the epilogue must have drained the previous chunk
+                    if (!mbar_wait(&ctl->acc_empty, (uint32_t)((kb / kChunkKB - 1) & 1), ctl, p.err)) break;
+                }
+                if (!mbar_wait(&ctl->full[st], (uint32_t)((kb / kStages) & 1), ctl, p.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t ad = sw128_desc(a_base + st * kAStageBytes + kk * 32);
+                    const uint64_t bd = sw128_desc(b_base + st * kBStageBytes + kk * 32);
+                    mma_f16(tmem, ad, bd, idesc, (kb % kChunkKB != 0 || kk != 0) ? 1u : 0u);
+                }
+                mma_commit(&ctl->empty[st]);
+                if (kb % kChunkKB == kChunkKB - 1 || kb == nkb - 1) mma_commit(&ctl->acc_full);
+            }
+            // Wait (bounded) until every MMA issued above has completed.
+            mma_commit(&ctl->drained);
+            uint64_t t0 = global_ns();
+            while (!mbar_try(smem_u32(&ctl->drained), 0)) {
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    record_fault(p.err, kErrBitTimeout);
+                    ctl->abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp > kMmaWarp) {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - (kMmaWarp + 1) * 32;
+        const int items = (kBM + bn) * 4;
+        const int64_t a_row0 = tile_a * kBM;
+        const int64_t b_row0 = tile_b * bn;
+        uint4 v[kMaxConvItems];
+        auto load_stage = [&](int kb) {
+            const int64_t k0 = (int64_t)kb * kBK;
+#pragma unroll
+            for (int j = 0; j < kMaxConvItems; ++j) {
+                const int item = ct + j * kConvThreads;
+                v[j] = make_uint4(0, 0, 0, 0);
+                if (item < items) {
+                    const bool is_a = item < kBM * 4;
+                    const int it = is_a ? item : item - kBM * 4;
+                    const int row = it >> 2;
+                    const int c = it & 3;
+                    const int64_t grow = (is_a ? a_row0 : b_row0) + row;
+                    const int64_t k = k0 + 16 * c;
+                    if (grow < (is_a ? p.rows_a : p.rows_b) && k < K)
+                        v[j] = ldg_stream((is_a ? p.a : p.b) + grow * K + k);
+                }
+            }
+        };
+        load_stage(0);
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb % kStages;
+            if (!warp_wait(&ctl->empty[st], (uint32_t)(((kb / kStages) & 1) ^ 1), ctl, p.err)) break;
+            const uint32_t a_buf = smem_u32(a_stages + st * kAStageBytes);
+            const uint32_t b_buf = smem_u32(b_stages + st * kBStageBytes);
+#pragma unroll
+            for (int j = 0; j < kMaxConvItems; ++j) {
+                const int item = ct + j * kConvThreads;
+                if (item < items) {
+                    const bool is_a = item < kBM * 4;
+                    const int it = is_a ? item : item - kBM * 4;
+                    const int row = it >> 2;
+                    const int c = it & 3;
+                    uint32_t h[8];
+                    i8x4_to_f16(v[j].x, h[0], h[1]);
+                    i8x4_to_f16(v[j].y, h[2], h[3]);
+                    i8x4_to_f16(v[j].z, h[4], h[5]);
+                    i8x4_to_f16(v[j].w, h[6], h[7]);
+                    const uint32_t row_base = (is_a ? a_buf : b_buf) + (row >> 3) * 1024 + (row & 7) * 128;
+                    const uint32_t c0 = (uint32_t)((2 * c) ^ (row & 7));
+                    const uint32_t c1 = (uint32_t)((2 * c + 1) ^ (row & 7));
+                    st_shared_v4(row_base + c0 * 16, h[0], h[1], h[2], h[3]);
+                    st_shared_v4(row_base + c1 * 16, h[4], h[5], h[6], h[7]);
+                }
+            }
+            // make the generic-proxy stores visible to the tensor core
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->full[st]);
+            if (kb + 1 < nkb) load_stage(kb + 1);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int64_t arow = tile_a * kBM + warp * 32 + lane;
+        const int ngrp = bn / 16;
+        for (int c = 0; c < nchunks; ++c) {
+            if (!warp_wait(&ctl->acc_full, (uint32_t)(c & 1), ctl, p.err)) break;
+            tc_fence_after();
+            const bool last = c == nchunks - 1;
+            for (int grp = 0; grp < ngrp; ++grp) {
+                __syncwarp();
+                uint32_t r[16];
+                tmem_ld16(lane_base + grp * 16, r);
+                tmem_wait_ld();
+                int32_t v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = __float2int_rn(__uint_as_float(r[j]));
+                if (c > 0) {
+                    uint32_t s[16];
+                    tmem_ld16(lane_base + run_col + grp * 16, s);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += (int32_t)s[j];
+                }
+                if (!last) {
+                    uint32_t s[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) s[j] = (uint32_t)v[j];
+                    tmem_st16(lane_base + run_col + grp * 16, s);
+                    continue;
+                }
+                // Final chunk: scale/bias epilogue and stores.
+                const int64_t bcol0 = tile_b * bn + grp * 16;
+                if (!p.swap) {
+                    const int64_t m = arow;
+                    if (m < p.M) {
+                        const float sxm = p.sx[m];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int64_t n = bcol0 + j;
+                            if (n < p.N) {
+                                float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), sxm), __ldg(p.sw + n));
+                                if (p.bias) f = __fadd_rn(f, bf16_to_f32(__ldg(p.bias + n)));
+                                p.y[m * p.N + n] = f32_to_bf16_rn(f);
+                                if (p.acc) p.acc[m * p.N + n] = v[j];
+                            }
+                        }
+                    }
+                } else {
+                    const int64_t n = arow;
+                    if (n < p.N) {
+                        const float swn = p.sw[n];
+                        const float bn_f = p.bias ? bf16_to_f32(p.bias[n]) : 0.0f;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int64_t m = bcol0 + j;
+                            if (m < p.M) {
+                                float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), __ldg(p.sx + m)), swn);
+                                if (p.bias) f = __fadd_rn(f, bn_f);
+                                p.y[m * p.N + n] = f32_to_bf16_rn(f);
+                                if (p.acc) p.acc[m * p.N + n] = v[j];
+                            }
+                        }
+                    }
+                }
+            }
+            if (!last) {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->acc_empty);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols)
+                     : "memory");
+    }
+}
+
+uint32_t pow2_cols(int need) {
+    uint32_t c = 32;
+    while ((int)c < need) c <<= 1;
+    return c;
+}
+
+}  // namespace
+
+cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                        const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                        const LaunchEnv& env) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(w8a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    W8A8Params p{};
+    p.K = K;
+    p.sx = sx;
+    p.sw = sw;
+    p.bias = bias;
+    p.y = y;
+    p.acc = acc;
+    p.M = M;
+    p.N = N;
+    p.err = env.err;
+    int64_t tiles_a;
+    if (M <= kBM) {
+        // swap AB: weights fill the 128-row MMA operand, tokens the N side
+        p.swap = 1;
+        p.a = qw;
+        p.rows_a = N;
+        p.b = qx;
+        p.rows_b = M;
+        p.bn = (int)((M + 15) / 16 * 16);
+        p.tiles_b = 1;
+        tiles_a = (N + kBM - 1) / kBM;
+    } else {
+        p.swap = 0;
+        p.a = qx;
+        p.rows_a = M;
+        p.b = qw;
+        p.rows_b = N;
+        p.bn = kMaxBN;
+        p.tiles_b = (N + kMaxBN - 1) / kMaxBN;
+        tiles_a = (M + kBM - 1) / kBM;
+    }
+    p.tmem_cols = pow2_cols(2 * p.bn);
+    const int64_t tiles = tiles_a * p.tiles_b;
+    w8a8_kernel<<<dim3((unsigned)tiles), kThreads, kSmemBytes, env.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace i8ql

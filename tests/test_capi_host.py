@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI that launch nothing (run without a GPU).
+
+The library must load, export every function the header declares, and
+reject bad arguments on the host with the documented status codes before any
+CUDA call.
+"""
+
+from __future__ import annotations
+
+import os
+import re
+
+import pytest
+import torch
+
+from int8_quantized_linear_gb300 import build as lib_build
+from int8_quantized_linear_gb300 import capi
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "i8ql.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return capi.lib()
+
+
+def _declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", text)
+    return sorted({n for n in names if n not in {"if", "defined"}})
+
+
+def test_header_declares_the_five_operations():
+    names = _declared_functions()
+    for op in ("quantize_weight_per_channel_int8", "quantize_act_per_token_int8", "w8a8_gemm",
+               "w8a16_gemm", "grouped_w8a16_gemm"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert names, "no declarations parsed"
+    for name in names:
+        assert hasattr(lib, name), f"libi8ql.so does not export {name}"
+        assert name in capi.SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_status_strings_and_version(lib):
+    for s in range(0, 7):
+        assert capi.status_string(s)
+    assert capi.status_string(99) == "unknown status"
+    assert capi.i8ql_version() >= 10000
+
+
+A = 0x10000  # a fake, 16-byte-aligned "device" address: never dereferenced here
+B = 0x20000
+C = 0x30000
+D = 0x40000
+
+
+@pytest.mark.parametrize("fn", ["quantize_weight_per_channel_int8", "quantize_act_per_token_int8"])
+def test_quant_argument_errors(lib, fn):
+    f = getattr(lib, fn)
+    assert f(A, 4, 0, B, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, 4, 24, B, C, None) == capi.I8QL_ERR_UNSUPPORTED
+    assert f(A, 4, capi.I8QL_MAX_K + 16, B, C, None) == capi.I8QL_ERR_UNSUPPORTED
+    assert f(A, -1, 16, B, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(None, 4, 16, B, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A + 8, 4, 16, B, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, 4, 16, B + 4, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, 4, 16, B, C + 2, None) == capi.I8QL_ERR_INVALID_ARG
+    # an empty problem launches nothing and succeeds, whatever the pointers
+    assert f(None, 0, 16, None, None, None) == capi.I8QL_OK
+
+
+def test_w8a8_argument_errors(lib):
+    f = lib.w8a8_gemm
+    ok = (A, B, C, D, None, A, None, 8, 16, 64, None)
+    args = list(ok)
+    args[9] = 40  # K not a multiple of 16
+    assert f(*args) == capi.I8QL_ERR_UNSUPPORTED
+    args = list(ok); args[8] = 0  # N = 0
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG
+    args = list(ok); args[0] = None
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG
+    args = list(ok); args[2] = B + 1
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG
+    args = list(ok); args[4] = A + 1  # bias must be 2-byte aligned
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG
+    args = list(ok); args[6] = A + 4  # acc_debug must be 16-byte aligned
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG
+    args = list(ok); args[7] = 0
+    assert f(*args) == capi.I8QL_OK
+
+
+def test_w8a16_argument_errors(lib):
+    f = lib.w8a16_gemm
+    assert f(A, B, C, D, 4, 16, 8, None) == capi.I8QL_ERR_UNSUPPORTED
+    assert f(A, B, C, D, 4, -2, 64, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, None, C, D, 4, 16, 64, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, B, C + 2, D, 4, 16, 64, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(None, B, C, None, 0, 16, 64, None) == capi.I8QL_OK
+
+
+def test_grouped_argument_errors(lib):
+    f = lib.grouped_w8a16_gemm
+    ok = [A, B, 4, C, D, A, 8, 16, 64, None]
+    a = list(ok); a[1] = None
+    assert f(*a) == capi.I8QL_ERR_INVALID_ARG
+    a = list(ok); a[2] = 0
+    assert f(*a) == capi.I8QL_ERR_INVALID_ARG
+    a = list(ok); a[2] = 70000
+    assert f(*a) == capi.I8QL_ERR_UNSUPPORTED
+    a = list(ok); a[8] = 20
+    assert f(*a) == capi.I8QL_ERR_UNSUPPORTED
+    a = list(ok); a[6] = 0
+    assert f(*a) == capi.I8QL_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_device_reports_no_device(lib):
+    assert lib.w8a16_gemm(A, B, C, D, 4, 16, 64, None) == capi.I8QL_ERR_NO_DEVICE

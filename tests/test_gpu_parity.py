@@ -1,0 +1,370 @@
+"""GPU parity of every kernel against the CPU oracle, through the C ABI.
+
+Inputs come from the seeded generators; the oracle only ever sees those
+inputs (never a GPU result).  Bars:
+ * int8 codes, fp32 scales and int32 accumulators: bit-exact;
+ * W8A8 bf16 outputs: within 1 bf16 ulp of the oracle's fp32 epilogue
+   rounded once;
+ * W8A16 / grouped outputs: relative Frobenius error <= 2e-3 against the fp64
+   dequantize-then-matmul reference, and every element within the worst-case
+   bound of fp32 accumulation plus one bf16 rounding.
+Outputs carry guard bands that must survive every launch.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_quantized_linear_gb300 import capi, synthetic
+from tests import util
+from tests.golden import load as golden
+
+pytestmark = pytest.mark.gpu
+
+W8A16_FROB = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library(cuda_device):
+    from int8_quantized_linear_gb300 import build
+    build.build()
+    capi.lib()
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    yield
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+
+
+def dev(t):
+    return t.to("cuda")
+
+
+# ------------------------------------------------------------------ quantization
+
+def gpu_quant(src_bf16: torch.Tensor, weight: bool = True):
+    rows, k = src_bf16.shape
+    qbuf, q = util.guarded((rows, k), torch.int8, "cuda", 77)
+    sbuf, s = util.guarded((rows,), torch.float32, "cuda", -3.0)
+    fn = capi.quantize_weight_per_channel_int8 if weight else capi.quantize_act_per_token_int8
+    fn(dev(src_bf16), q=q, scale=s)
+    torch.cuda.synchronize()
+    assert util.guard_intact(qbuf, rows * k, 77) and util.guard_intact(sbuf, rows, -3.0)
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+def check_quant(src_bf16: torch.Tensor, weight: bool = True):
+    q, s = gpu_quant(src_bf16, weight)
+    q_ref, s_ref = oracle.quant_rows(util.bits(src_bf16))
+    assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32)), "scales differ"
+    bad = np.argwhere(q != q_ref)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}"
+    return q, s
+
+
+@pytest.mark.parametrize("case", golden.quant_rows(), ids=lambda c: c[0])
+def test_quant_golden_rows_on_gpu(case):
+    name, row, scale, codes = case
+    k = 16
+    vals = np.zeros((1, k), np.float64)
+    vals[0, :len(row)] = row
+    src = torch.tensor(vals, dtype=torch.float64).to(torch.bfloat16)
+    for weight in (True, False):
+        q, s = gpu_quant(src, weight)
+        assert s[0] == np.float32(scale), name
+        assert q[0, :len(codes)].tolist() == codes, name
+
+
+def test_quant_tiny_layer():
+    w, x = synthetic.tiny_layer(0)
+    _, sw = check_quant(w, True)
+    assert sw[7] == 1.0  # the all-zero row
+    check_quant(x, False)
+
+
+def _adversarial_rows(rows, k, seed):
+    w = synthetic.weight(rows, k, seed).float()
+    g = torch.Generator().manual_seed(seed)
+    w[0] = 0.0
+    if rows > 2:
+        w[1] *= 1e-35  # tiny normal / subnormal magnitudes
+    if rows > 3:
+        w[2] = torch.randint(-4, 5, (k,), generator=g).float() * 0.5  # many exact ties
+    return w.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,k", [(1, 16), (3, 48), (33, 1040), (129, 4096), (7, 12288),
+                                    (5, 16384), (4, 16400), (2, 20000), (300, 256), (1000, 2560)])
+def test_quant_shapes(rows, k):
+    check_quant(_adversarial_rows(rows, k, rows * 7 + k), True)
+    check_quant(_adversarial_rows(rows, k, rows * 11 + k), False)
+
+
+@pytest.mark.parametrize("name", list(synthetic.QWEN3_4B_SHAPES) + ["qwen3_8b_gate_up"])
+def test_quant_full_size_weights(name):
+    if name == "qwen3_8b_gate_up":
+        n, k = synthetic.QWEN3_8B_SHAPES["gate_up"]
+    else:
+        n, k = synthetic.QWEN3_4B_SHAPES[name]
+    check_quant(synthetic.weight(n, k, 1), True)
+
+
+def test_quant_full_size_activations():
+    check_quant(synthetic.activations(4096, 2560, 2), False)
+    check_quant(synthetic.activations(8, 9728, 2), False)
+
+
+def test_quant_empty_rows_is_noop():
+    q = torch.empty((0, 64), dtype=torch.int8, device="cuda")
+    s = torch.empty((0,), dtype=torch.float32, device="cuda")
+    capi.quantize_act_per_token_int8(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"), q=q, scale=s)
+
+
+# ------------------------------------------------------------------ W8A8
+
+def _codes(rows, k, seed, extreme=False):
+    g = np.random.default_rng(seed)
+    if extreme:
+        return (g.integers(0, 2, size=(rows, k)) * 254 - 127).astype(np.int8)
+    return g.integers(-127, 128, size=(rows, k)).astype(np.int8)
+
+
+def gpu_w8a8(qx, sx, qw, sw, bias_bits=None):
+    m, k = qx.shape
+    n = qw.shape[0]
+    ybuf, y = util.guarded((m, n), torch.int16, "cuda", 0x7F7F)
+    abuf, acc = util.guarded((m, n), torch.int32, "cuda", -5)
+    bias = None if bias_bits is None else util.from_bits(bias_bits, "cuda")
+    capi.w8a8_gemm(dev(torch.from_numpy(qx)), dev(torch.from_numpy(sx)), dev(torch.from_numpy(qw)),
+                   dev(torch.from_numpy(sw)), bias=bias, y=y.view(torch.bfloat16), acc_debug=acc)
+    torch.cuda.synchronize()
+    assert util.guard_intact(ybuf, m * n, 0x7F7F) and util.guard_intact(abuf, m * n, -5)
+    return acc.cpu().numpy(), y.cpu().numpy().view(np.uint16)
+
+
+def check_w8a8_full(qx, sx, qw, sw, bias_bits=None):
+    acc, y = gpu_w8a8(qx, sx, qw, sw, bias_bits)
+    acc_ref, _, y_ref = oracle.w8a8(qx, sx, qw, sw, bias_bits)
+    assert np.array_equal(acc.astype(np.int64), acc_ref), \
+        f"acc differs at {np.argwhere(acc != acc_ref)[:3].tolist()}"
+    assert util.max_ulp_diff(y, y_ref) <= 1
+    return acc, y
+
+
+def _scales(n, seed, lo=1e-4, hi=2e-2):
+    g = np.random.default_rng(seed)
+    return (lo + (hi - lo) * g.random(n)).astype(np.float32)
+
+
+def test_w8a8_tiny_layer_end_to_end():
+    w, x = synthetic.tiny_layer(0)
+    qw, sw = check_quant(w, True)
+    qx, sx = check_quant(x, False)
+    bias = util.bits(synthetic.bias(512, 5))
+    for b in (None, bias):
+        check_w8a8_full(qx, sx, qw, sw, b)
+
+
+@pytest.mark.parametrize("m", [1, 7, 16, 64, 100, 128, 129, 256, 300])
+@pytest.mark.parametrize("n,k", [(17, 48), (256, 1024), (513, 1040), (255, 2064)])
+def test_w8a8_shapes(m, n, k):
+    qx, qw = _codes(m, k, m * 3 + k), _codes(n, k, n * 5 + k)
+    sx, sw = _scales(m, m + 1, 0.01, 1.0), _scales(n, n + 2)
+    bias = util.bits(synthetic.bias(n, n)) if (m + n) % 2 else None
+    check_w8a8_full(qx, sx, qw, sw, bias)
+
+
+@pytest.mark.parametrize("m,n,k", [(130, 260, 16384), (2, 3, 133120), (64, 40, 32768)])
+def test_w8a8_exact_at_extreme_accumulators(m, n, k):
+    """All codes +-127: every 1024-deep chunk sits near 2^24 and the int32
+    total near 2^31, so any rounding in the chunked accumulation shows."""
+    qx, qw = _codes(m, k, 1, extreme=True), _codes(n, k, 2, extreme=True)
+    qx[0, :] = 127
+    qw[0, :] = 127  # acc[0,0] = 127^2 * k
+    sx, sw = _scales(m, 3, 1e-6, 1e-5), _scales(n, 4, 1e-6, 1e-5)
+    acc, y = gpu_w8a8(qx, sx, qw, sw)
+    assert acc[0, 0] == 127 * 127 * k
+    pm = np.arange(min(m, 64)).repeat(min(n, 8))
+    pn = np.tile(np.arange(min(n, 8)), min(m, 64))
+    ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, None, pm, pn)
+    assert np.array_equal(acc[pm, pn].astype(np.int64), ref_acc)
+    assert util.max_ulp_diff(y[pm, pn], ref_y) <= 1
+
+
+def _points(m, n, count, seed):
+    g = np.random.default_rng(seed)
+    pm = np.concatenate([g.integers(0, m, count), [0, m - 1, m - 1, 0]])
+    pn = np.concatenate([g.integers(0, n, count), [0, n - 1, 0, n - 1]])
+    return pm, pn
+
+
+@pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
+@pytest.mark.parametrize("m", [128, 2048])
+def test_w8a8_qwen3_4b_prefill_sampled(shape, m):
+    n, k = synthetic.QWEN3_4B_SHAPES[shape]
+    w = synthetic.weight(n, k, 1)
+    x = synthetic.activations(m, k, 2)
+    qw, sw = check_quant(w, True)
+    qx, sx = check_quant(x, False)
+    bias = util.bits(synthetic.bias(n, 2))
+    acc, y = gpu_w8a8(qx, sx, qw, sw, bias)
+    pm, pn = _points(m, n, 3000, m + n)
+    ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, bias, pm, pn)
+    assert np.array_equal(acc[pm, pn].astype(np.int64), ref_acc)
+    assert util.max_ulp_diff(y[pm, pn], ref_y) <= 1
+
+
+# ------------------------------------------------------------------ W8A16
+
+def gpu_w8a16(x_bf16, qw, sw):
+    m, k = x_bf16.shape
+    n = qw.shape[0]
+    ybuf, y = util.guarded((m, n), torch.int16, "cuda", 0x7F7F)
+    capi.w8a16_gemm(dev(x_bf16), dev(torch.from_numpy(qw)), dev(torch.from_numpy(sw)), y=y.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert util.guard_intact(ybuf, m * n, 0x7F7F)
+    return util.from_bits(y.cpu().numpy().view(np.uint16)).double().numpy()
+
+
+def w8a16_bound(x_bits, qw, sw, k):
+    """Worst-case |error|: fp32 accumulation (k terms) plus one bf16 rounding."""
+    absx = x_bits & np.uint16(0x7FFF)
+    mag = oracle.w8a16(absx, np.abs(qw.astype(np.int16)).astype(np.int8), sw)
+    return mag * (k * 2.0 ** -23)
+
+
+def check_w8a16(x_bf16, qw, sw):
+    y = gpu_w8a16(x_bf16, qw, sw)
+    xb = util.bits(x_bf16)
+    ref = oracle.w8a16(xb, qw, sw)
+    assert util.rel_frobenius(y, ref) <= W8A16_FROB
+    bound = w8a16_bound(xb, qw, sw, x_bf16.shape[1]) + np.abs(ref) * 2.0 ** -8
+    assert np.all(np.abs(y - ref) <= bound + 1e-30)
+
+
+@pytest.mark.parametrize("m", [1, 3, 8, 9, 16, 17, 32, 33, 64, 65, 100])
+@pytest.mark.parametrize("n,k", [(1, 16), (31, 48), (100, 80), (64, 1040), (2560, 2560)])
+def test_w8a16_shapes(m, n, k):
+    qw, sw = oracle.quant_rows(util.bits(synthetic.weight(n, k, n + k)))
+    check_w8a16(synthetic.activations(m, k, m + 3 * k), qw, sw)
+
+
+def test_w8a16_tiny_layer():
+    w, x = synthetic.tiny_layer(0)
+    qw, sw = check_quant(w, True)
+    check_w8a16(x, qw, sw)
+
+
+@pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
+def test_w8a16_qwen3_4b_decode_full(shape):
+    n, k = synthetic.QWEN3_4B_SHAPES[shape]
+    qw, sw = check_quant(synthetic.weight(n, k, 1), True)
+    for m in (1, 4, 8):
+        check_w8a16(synthetic.activations(m, k, 10 + m), qw, sw)
+
+
+@pytest.mark.parametrize("m", [16, 64])
+def test_w8a16_qwen3_8b_sampled(m):
+    n, k = synthetic.QWEN3_8B_SHAPES["down"]
+    qw, sw = oracle.quant_rows(util.bits(synthetic.weight(n, k, 4)))
+    x = synthetic.activations(m, k, 4)
+    y = gpu_w8a16(x, qw, sw)
+    pm, pn = _points(m, n, 4000, m)
+    ref = oracle.w8a16_points(util.bits(x), qw, sw, pm, pn)
+    assert util.rel_frobenius(y[pm, pn], ref) <= W8A16_FROB
+
+
+# ------------------------------------------------------------------ grouped W8A16
+
+def gpu_grouped(x_bf16, offsets, qw, sw):
+    t, k = x_bf16.shape
+    e, n, _ = qw.shape
+    ybuf, y = util.guarded((t, n), torch.int16, "cuda", 0x7F7F)
+    capi.grouped_w8a16_gemm(dev(x_bf16), dev(torch.from_numpy(offsets)), dev(torch.from_numpy(qw)),
+                            dev(torch.from_numpy(sw)), y=y.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert util.guard_intact(ybuf, t * n, 0x7F7F)
+    return util.from_bits(y.cpu().numpy().view(np.uint16)).double().numpy()
+
+
+def _experts(e_count, n, k, seed):
+    q = np.empty((e_count, n, k), np.int8)
+    s = np.empty((e_count, n), np.float32)
+    for e in range(e_count):
+        q[e], s[e] = oracle.quant_rows(util.bits(synthetic.weight(n, k, seed + e)))
+    return q, s
+
+
+@pytest.mark.parametrize("counts", [[3, 0, 4, 2, 0], [0, 0, 0, 0, 9], [1, 1, 1, 1, 1], [70, 0, 0, 0, 5],
+                                    [0, 17, 0, 33, 0]])
+def test_grouped_small(counts):
+    n, k = 40, 80
+    q, s = _experts(len(counts), n, k, 50)
+    off = np.zeros(len(counts) + 1, np.int32)
+    off[1:] = np.cumsum(counts)
+    x = synthetic.activations(int(off[-1]), k, 51)
+    y = gpu_grouped(x, off, q, s)
+    ref = oracle.grouped_w8a16(util.bits(x), off, q, s)
+    assert util.rel_frobenius(y, ref) <= W8A16_FROB
+    for e in range(len(counts)):
+        lo, hi = off[e], off[e + 1]
+        if hi > lo:
+            assert util.rel_frobenius(y[lo:hi], ref[lo:hi]) <= W8A16_FROB
+
+
+@pytest.fixture(scope="module")
+def dsmoe_experts():
+    out = {}
+    for i, (name, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
+        w = torch.stack([synthetic.weight(n, k, 300 + 100 * i + e) for e in range(66)])
+        q, s = gpu_quant(w.view(66 * n, k), True)
+        out[name] = (q.reshape(66, n, k), s.reshape(66, n), w)
+    return out
+
+
+@pytest.mark.parametrize("tokens", [1, 8, 64])
+@pytest.mark.parametrize("proj", ["gate_up", "down"])
+def test_grouped_dsmoe_sampled(dsmoe_experts, tokens, proj):
+    q, s, w = dsmoe_experts[proj]
+    n, k = synthetic.DSMOE_SHAPES[proj]
+    # the GPU codes of a sample of experts equal the oracle's
+    for e in (0, 33, 65):
+        q_ref, s_ref = oracle.quant_rows(util.bits(w[e]))
+        assert np.array_equal(q[e], q_ref) and np.array_equal(s[e], s_ref)
+    r = synthetic.moe_routing(tokens, seed=3)
+    x_tok = synthetic.activations(tokens, k, 60 + tokens)
+    x = x_tok[torch.from_numpy(r.rows)]
+    y = gpu_grouped(x, r.offsets, q, s)
+    xb = util.bits(x)
+    g = np.random.default_rng(tokens)
+    for e in range(66):
+        lo, hi = int(r.offsets[e]), int(r.offsets[e + 1])
+        if hi == lo:
+            continue
+        pm = g.integers(lo, hi, 24) - lo
+        pn = g.integers(0, n, 24)
+        ref = oracle.w8a16_points(xb[lo:hi], q[e], s[e], pm, pn)
+        assert util.rel_frobenius(y[lo + pm, pn], ref) <= W8A16_FROB
+
+
+def test_grouped_bad_offsets_reported():
+    n, k = 16, 32
+    q, s = _experts(3, n, k, 70)
+    x = synthetic.activations(6, k, 71)
+    good = np.array([0, 2, 4, 6], np.int32)
+    y_good = gpu_grouped(x, good, q, s)
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    bad = np.array([0, 4, 2, 6], np.int32)  # expert 1 runs backwards
+    y_bad = gpu_grouped(x, bad, q, s)
+    assert capi.i8ql_get_device_error() == capi.I8QL_ERR_BAD_OFFSETS
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK  # read clears it
+    # expert 2 (rows 2..5) was still computed
+    assert np.array_equal(y_bad[4:6], y_good[4:6])
+    bad_end = np.array([0, 2, 4, 5], np.int32)  # does not end at T_total
+    gpu_grouped(x, bad_end, q, s)
+    assert capi.i8ql_get_device_error() == capi.I8QL_ERR_BAD_OFFSETS
+
+
+def test_no_fault_recorded_by_normal_use():
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
