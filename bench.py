@@ -1,0 +1,621 @@
+#!/usr/bin/env python
+"""Benchmark of the int8 quantized linear layer on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+
+  decode (default; Qwen3-4B-shaped decode linears plus the DeepSeek-MoE-16B
+  grouped experts):
+    * per-channel weight quantization of the four bf16 projection weights
+      (fused QKV [6144, 2560], o [2560, 2560], fused gate_up [19456, 2560],
+      down [2560, 9728]);
+    * for M in {1, 4, 8} and each projection: per-token activation
+      quantization, the W8A8 GEMM and the W8A16 GEMM;
+    * the grouped W8A16 GEMM over 66 experts (64 routed, top-6, + 2 shared)
+      for T = 8 decode tokens, gate_up [2816, 2048] then down [2048, 1408].
+  prefill (--workload prefill; Qwen3-4B W8A8 prefill, bias on):
+    * for M in {128, 512, 2048, 4096} and each projection: activation
+      quantization and the W8A8 GEMM.
+
+Every GEMM launch of a step reads its own copy of the int8 weights, and a
+step touches more than 1 GB, so no launch finds its weights in the 129 MB L2
+(between timed steps nothing is reused either).  The step is captured once as
+a CUDA graph; the timed region replays K steps back to back, with an external
+CUDA event pair around every launch to time each kernel live.
+
+value (decode) = algorithmic HBM bytes of all launches / step time (GB/s);
+value (prefill) = 2*M*N*K summed over the W8A8 launches / step time (TOPS).
+Algorithmic bytes per launch: quantization 3*R*K + 4*R; W8A8
+M*K + N*K + 4*(M+N) + 2*M*N; W8A16 N*K + 4*N + 2*M*K + 2*M*N; grouped
+sum over experts with rows of (N*K + 4*N) + 2*rows*(K+N).
+
+--impl reference times the CPU oracle (the only reference implementation:
+the pages ship no code) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "int8 GEMM TOPS (prefill) & weight GB/s (decode) vs GB300 roofline"
+DECODE_MS = (1, 4, 8)
+PREFILL_MS = (128, 512, 2048, 4096)
+MOE_TOKENS = 8
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- accounting
+
+def bytes_quant(r, k):
+    return 3 * r * k + 4 * r
+
+
+def bytes_w8a8(m, n, k, bias):
+    return m * k + n * k + 4 * (m + n) + 2 * m * n + (2 * n if bias else 0)
+
+
+def bytes_w8a16(m, n, k):
+    return n * k + 4 * n + 2 * m * k + 2 * m * n
+
+
+def bytes_grouped(counts, n, k):
+    active = [c for c in counts if c > 0]
+    return len(active) * (n * k + 4 * n) + 2 * sum(active) * (k + n)
+
+
+def workload_name(kind):
+    if kind == "decode":
+        return ("Qwen3-4B decode linears (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, "
+                "down 9728->2560; M in {1,4,8}; weight quant + act quant + W8A8 + W8A16) + "
+                "DeepSeek-MoE-16B grouped W8A16 (66 experts, top-6 + 2 shared, T=8; "
+                "gate_up 2816x2048, down 2048x1408)")
+    return ("Qwen3-4B prefill W8A8 (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, down 9728->2560; "
+            "M in {128,512,2048,4096}; act quant + W8A8, bias on)")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash(kernel):
+    src = {"w8a8": "w8a8.cu", "w8a16": "w8a16.cu", "grouped": "w8a16.cu", "quant_w": "quant.cu",
+           "quant_x": "quant.cu"}[kernel]
+    path = os.path.join(ROOT, "int8_quantized_linear_gb300", "csrc", src)
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        table = json.load(fh)
+    entry = table.get(workload, {}).get(kernel)
+    if not entry or entry.get("source_sha256_16") != kernel_source_hash(kernel):
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- GPU workload
+
+class Launch:
+    __slots__ = ("kernel", "fn", "bytes", "flops", "label")
+
+    def __init__(self, kernel, fn, nbytes, flops, label):
+        self.kernel, self.fn, self.bytes, self.flops, self.label = kernel, fn, nbytes, flops, label
+
+
+class Workload:
+    """Device buffers and the ordered launch list of one step."""
+
+    def __init__(self, kind, device, seed=1):
+        from int8_quantized_linear_gb300 import capi, synthetic
+        self.kind = kind
+        self.device = device
+        self.launches: list[Launch] = []
+        self.h2d: list[tuple[torch.Tensor, torch.Tensor]] = []  # (pinned host, device) inputs
+        self.d2h: list[tuple[torch.Tensor, torch.Tensor]] = []  # (device, pinned host) results
+        self.cpu_inputs = {}
+        shapes = synthetic.QWEN3_4B_SHAPES
+        ms = DECODE_MS if kind == "decode" else PREFILL_MS
+        dev = device
+        kinds = ("w8a8", "w8a16") if kind == "decode" else ("w8a8",)
+        copies = len(ms) * len(kinds)
+
+        for si, (name, (n, k)) in enumerate(shapes.items()):
+            w = synthetic.weight(n, k, seed + si, device=dev)
+            qs = [torch.empty((n, k), dtype=torch.int8, device=dev) for _ in range(copies)]
+            s = torch.empty((n,), dtype=torch.float32, device=dev)
+            capi.quantize_weight_per_channel_int8(w, q=qs[0], scale=s)
+            for c in range(1, copies):
+                qs[c].copy_(qs[0])
+            bias = synthetic.bias(n, seed + si, device=dev) if kind == "prefill" else None
+            self.cpu_inputs[name] = {"w": w}
+            if kind == "decode":
+                self.launches.append(Launch(
+                    "quant_w", lambda w=w, q=qs[0], s=s: capi.quantize_weight_per_channel_int8(w, q=q, scale=s),
+                    bytes_quant(n, k), 0, f"quant_w {name} {n}x{k}"))
+                self.h2d.append((torch.empty(w.shape, dtype=w.dtype, pin_memory=True).copy_(w), w))
+            for mi, m in enumerate(ms):
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=dev)
+                self.h2d.append((torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x), x))
+                qx = torch.empty((m, k), dtype=torch.int8, device=dev)
+                sx = torch.empty((m,), dtype=torch.float32, device=dev)
+                self.launches.append(Launch(
+                    "quant_x", lambda x=x, qx=qx, sx=sx: capi.quantize_act_per_token_int8(x, q=qx, scale=sx),
+                    bytes_quant(m, k), 0, f"quant_x {name} M={m}"))
+                y8 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                q8 = qs[mi * len(kinds)]
+                self.launches.append(Launch(
+                    "w8a8", lambda qx=qx, sx=sx, q=q8, s=s, b=bias, y=y8: capi.w8a8_gemm(qx, sx, q, s, bias=b, y=y),
+                    bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k, f"w8a8 {name} M={m}"))
+                self.d2h.append((y8, torch.empty(y8.shape, dtype=y8.dtype, pin_memory=True)))
+                if kind == "decode":
+                    y16 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                    q16 = qs[mi * len(kinds) + 1]
+                    self.launches.append(Launch(
+                        "w8a16", lambda x=x, q=q16, s=s, y=y16: capi.w8a16_gemm(x, q, s, y=y),
+                        bytes_w8a16(m, n, k), 2 * m * n * k, f"w8a16 {name} M={m}"))
+                    self.d2h.append((y16, torch.empty(y16.shape, dtype=y16.dtype, pin_memory=True)))
+                self.cpu_inputs[name][m] = x
+            self.cpu_inputs[name]["s"] = s
+            del w
+
+        if kind == "decode":
+            route = synthetic.moe_routing(MOE_TOKENS, seed=3)
+            counts = np.diff(route.offsets)
+            off = torch.from_numpy(route.offsets).to(dev)
+            self.h2d.append((torch.from_numpy(route.offsets).pin_memory(), off))
+            self.moe = {"route": route}
+            for pi, (proj, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
+                e_count = route.experts
+                q = torch.empty((e_count, n, k), dtype=torch.int8, device=dev)
+                s = torch.empty((e_count, n), dtype=torch.float32, device=dev)
+                for e in range(e_count):
+                    we = synthetic.weight(n, k, 1000 + 100 * pi + e, device=dev)
+                    capi.quantize_weight_per_channel_int8(we, q=q[e], scale=s[e])
+                x_tok = synthetic.activations(MOE_TOKENS, k, 900 + pi, device=dev)
+                x = x_tok[torch.from_numpy(route.rows).to(dev)].contiguous()
+                self.h2d.append((torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x), x))
+                y = torch.empty((x.shape[0], n), dtype=torch.bfloat16, device=dev)
+                self.launches.append(Launch(
+                    "grouped", lambda x=x, off=off, q=q, s=s, y=y: capi.grouped_w8a16_gemm(x, off, q, s, y=y),
+                    bytes_grouped(counts, n, k), 2 * int(counts.sum()) * n * k, f"grouped {proj} T={MOE_TOKENS}"))
+                self.d2h.append((y, torch.empty(y.shape, dtype=y.dtype, pin_memory=True)))
+                self.moe[proj] = (q, s, x)
+        torch.cuda.synchronize()
+
+    def run(self, events=None):
+        for i, l in enumerate(self.launches):
+            if events is not None:
+                events[i][0].record()
+            l.fn()
+            if events is not None:
+                events[i][1].record()
+
+    @property
+    def step_bytes(self):
+        return sum(l.bytes for l in self.launches)
+
+    @property
+    def step_flops(self):
+        return sum(l.flops for l in self.launches if l.kernel == "w8a8")
+
+
+def _event(external):
+    try:
+        return torch.cuda.Event(enable_timing=True, external=external)
+    except TypeError:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_step(sample, threads_note=False):
+    """Time the CPU oracle over a row sample of the workload; returns
+    (algorithmic bytes, seconds)."""
+    import oracle
+    total_b, total_s = 0, 0.0
+    for item in sample:
+        t0 = time.perf_counter()
+        kind = item[0]
+        if kind == "quant":
+            _, src = item
+            oracle.quant_rows(src)
+            total_b += bytes_quant(*src.shape)
+        elif kind == "w8a8":
+            _, xb, qw, sw = item
+            qx, sx = oracle.quant_rows(xb)
+            oracle.w8a8(qx, sx, qw, sw)
+            m, k = xb.shape
+            total_b += bytes_quant(m, k) + bytes_w8a8(m, qw.shape[0], k, False)
+        elif kind == "w8a16":
+            _, xb, qw, sw = item
+            oracle.w8a16(xb, qw, sw)
+            total_b += bytes_w8a16(xb.shape[0], qw.shape[0], xb.shape[1])
+        elif kind == "grouped":
+            _, xb, off, q, s = item
+            oracle.grouped_w8a16(xb, off, q, s)
+            total_b += bytes_grouped(np.diff(off), q.shape[1], q.shape[2])
+        total_s += time.perf_counter() - t0
+    return total_b, total_s
+
+
+def build_oracle_sample(kind, row_frac, seed=1):
+    """The workload with every weight cut to a fraction of its output rows
+    (and the grouped experts to a fraction of their rows), drawn on the CPU
+    from the same generators."""
+    import oracle
+    from int8_quantized_linear_gb300 import synthetic
+    sample = []
+    ms = DECODE_MS if kind == "decode" else PREFILL_MS
+    for si, (name, (n, k)) in enumerate(synthetic.QWEN3_4B_SHAPES.items()):
+        nr = max(16, int(n * row_frac))
+        w = synthetic.bf16_bits(synthetic.weight(nr, k, seed + si))
+        qw, sw = oracle.quant_rows(w)
+        if kind == "decode":
+            sample.append(("quant", w))
+        for mi, m in enumerate(ms):
+            mr = m if kind == "decode" else max(1, int(m * row_frac))
+            xb = synthetic.bf16_bits(synthetic.activations(mr, k, 100 * seed + 10 * si + mi))
+            sample.append(("w8a8", xb, qw, sw))
+            if kind == "decode":
+                sample.append(("w8a16", xb, qw, sw))
+    if kind == "decode":
+        route = synthetic.moe_routing(MOE_TOKENS, seed=3)
+        for pi, (proj, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
+            nr = max(16, int(n * row_frac))
+            q = np.empty((route.experts, nr, k), np.int8)
+            s = np.empty((route.experts, nr), np.float32)
+            for e in range(route.experts):
+                q[e], s[e] = oracle.quant_rows(synthetic.bf16_bits(synthetic.weight(nr, k, 1000 + 100 * pi + e)))
+            x_tok = synthetic.activations(MOE_TOKENS, k, 900 + pi)
+            xb = synthetic.bf16_bits(x_tok[torch.from_numpy(route.rows)])
+            sample.append(("grouped", xb, route.offsets, q, s))
+    return sample
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank sets the job time)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    """The oracle on the host cores: each step is a bounded row sample."""
+    if rank != 0:
+        return 0
+    frac = args.ref_row_frac
+    sample = build_oracle_sample(args.workload, frac)
+    for _ in range(args.warmup):
+        oracle_step(sample)
+    b_tot, s_tot = 0, 0.0
+    for _ in range(args.steps):
+        b, s = oracle_step(sample)
+        b_tot += b
+        s_tot += s
+    gbs = b_tot / s_tot / 1e9
+    desc = (f"every weight cut to {frac:.4g} of its output rows (grouped experts too), "
+            f"{'M in {1,4,8}' if args.workload == 'decode' else 'M scaled by the same fraction'}; "
+            "single-threaded C oracle")
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000 * s_tot / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": workload_name(args.workload), "sample": desc},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    from int8_quantized_linear_gb300 import capi
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wl = Workload(args.workload, device)
+    n_launch = len(wl.launches)
+    stream = torch.cuda.Stream(device)
+
+    # eager pass: per-device initialisation happens outside graph capture
+    with torch.cuda.stream(stream):
+        wl.run()
+    torch.cuda.synchronize()
+    if capi.i8ql_get_device_error(stream) != capi.I8QL_OK:
+        raise RuntimeError("kernel fault word set after the eager pass")
+
+    external = _event(True) is not None
+    use_graph = not args.no_graph and external
+    steps = args.steps
+    if use_graph:
+        g_warm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_warm, stream=stream):
+            wl.run()
+        events = [[(_event(True), _event(True)) for _ in range(n_launch)] for _ in range(steps)]
+        g_timed = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_timed, stream=stream):
+            for s in range(steps):
+                wl.run(events[s])
+    else:
+        events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_launch)] for _ in range(steps)]
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            if use_graph:
+                g_warm.replay()
+            else:
+                wl.run()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        if use_graph:
+            g_timed.replay()
+        else:
+            for s in range(steps):
+                wl.run(events[s])
+        end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / steps
+    fault = capi.i8ql_get_device_error(stream)
+    if fault != capi.I8QL_OK:
+        raise RuntimeError(f"kernel fault word set: {capi.status_string(fault)}")
+
+    # per-kernel live timings over the timed region
+    per = {}
+    for s in range(steps):
+        for i, l in enumerate(wl.launches):
+            a, b = events[s][i]
+            d = a.elapsed_time(b)
+            e = per.setdefault(l.kernel, {"launches": 0, "ms": 0.0, "bytes": 0, "flops": 0})
+            e["launches"] += 1
+            e["ms"] += d
+            e["bytes"] += l.bytes
+            e["flops"] += l.flops
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    tflops_peak = peaks["bf16_tflops_sustained"]
+    kernels = {}
+    for name, e in per.items():
+        gbs = e["bytes"] / (e["ms"] / 1e3) / 1e9
+        entry = {"launches": e["launches"], "us_per_launch": 1e3 * e["ms"] / e["launches"],
+                 "share": e["ms"] / sum(v["ms"] for v in per.values()),
+                 "GB/s": gbs, "hbm_frac": gbs / hbm}
+        if e["flops"]:
+            entry["TOPS"] = e["flops"] / (e["ms"] / 1e3) / 1e12
+        kernels[name] = entry
+    dom = max(per, key=lambda k: per[k]["ms"])
+    d = per[dom]
+    if args.workload == "decode" or dom != "w8a8":
+        achieved = d["bytes"] / d["launches"] / (d["ms"] / d["launches"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
+                "kernel": dom}
+        per_launch_bytes = d["bytes"] / d["launches"]
+    else:
+        achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
+                "frac": achieved / tflops_peak,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 kind::f16 pipe, nominal ratio 1)",
+                "kernel": dom}
+        per_launch_bytes = d["bytes"] / d["launches"]
+    roof["traffic"] = ncu_traffic(dom, args.workload)
+    roof["algorithmic_bytes_per_launch"] = per_launch_bytes
+
+    if args.workload == "decode":
+        value = world * wl.step_bytes / (ms_step / 1e3) / 1e9
+        unit = "GB/s"
+    else:
+        value = world * wl.step_flops / (ms_step / 1e3) / 1e12
+        unit = "TOPS"
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = run_e2e(args, wl, stream, g_warm if use_graph else None, world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": workload_name(args.workload), "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: every GEMM launch reads its own weight copy, "
+                         ">1 GB touched per step",
+                   "graph": use_graph},
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": n_launch * steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        sample = build_oracle_sample(args.workload, args.cpu_row_frac)
+        b, s = oracle_step(sample)
+        line["cpu_baseline"] = {
+            "value": (b / s / 1e9) if args.workload == "decode" else None,
+            "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"one pass of the workload with every weight cut to {args.cpu_row_frac:.4g} of its "
+                      f"rows; {s:.1f} s single-threaded"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(args, wl, stream, graph, world):
+    """Same step through the public API with host buffers: H2D of every input
+    from pinned memory, the step, D2H of every result, all inside the timed
+    region."""
+    steps = max(1, min(args.steps, 5))
+    h2d = sum(h.numel() * h.element_size() for h, _ in wl.h2d)
+    d2h = sum(h.numel() * h.element_size() for _, h in wl.d2h)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            for host, devt in wl.h2d:
+                devt.copy_(host, non_blocking=True)
+            if graph is not None:
+                graph.replay()
+            else:
+                wl.run()
+            for devt, host in wl.d2h:
+                host.copy_(devt, non_blocking=True)
+        end.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), world) / steps
+    if wl.kind == "decode":
+        value = world * wl.step_bytes / (ms / 1e3) / 1e9
+        unit = "GB/s"
+    else:
+        value = world * wl.step_flops / (ms / 1e3) / 1e12
+        unit = "TOPS"
+    return {"value": value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-row-frac", type=float, default=0.25)
+    ap.add_argument("--ref-row-frac", type=float, default=1 / 32)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            dist.init_process_group("gloo")
+        else:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        from int8_quantized_linear_gb300 import build
+        if rank == 0 or world == 1:
+            build.build()
+        barrier(world)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

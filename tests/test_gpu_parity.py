@@ -228,10 +228,21 @@ def gpu_w8a16(x_bf16, qw, sw):
 
 
 def w8a16_bound(x_bits, qw, sw, k):
-    """Worst-case |error|: fp32 accumulation (k terms) plus one bf16 rounding."""
+    """k * sum_k |s q x| (the magnitude that scales fp32 accumulation error)."""
     absx = x_bits & np.uint16(0x7FFF)
     mag = oracle.w8a16(absx, np.abs(qw.astype(np.int16)).astype(np.int8), sw)
-    return mag * (k * 2.0 ** -23)
+    return mag * k
+
+
+def _abs_inputs(x_bits, q):
+    return x_bits & np.uint16(0x7FFF), np.abs(q.astype(np.int16)).astype(np.int8)
+
+
+def check_elementwise(y, ref, mag, k):
+    """|y - ref| <= k * 2^-23 * sum|s q x| (fp32 accumulation, any order)
+    + 2^-8 * |ref| (one bf16 rounding of the output, relative half-ulp)."""
+    bound = mag * (k * 2.0 ** -23) + np.abs(ref) * 2.0 ** -8
+    assert np.all(np.abs(y - ref) <= bound + 1e-30)
 
 
 def check_w8a16(x_bf16, qw, sw):
@@ -239,8 +250,7 @@ def check_w8a16(x_bf16, qw, sw):
     xb = util.bits(x_bf16)
     ref = oracle.w8a16(xb, qw, sw)
     assert util.rel_frobenius(y, ref) <= W8A16_FROB
-    bound = w8a16_bound(xb, qw, sw, x_bf16.shape[1]) + np.abs(ref) * 2.0 ** -8
-    assert np.all(np.abs(y - ref) <= bound + 1e-30)
+    check_elementwise(y, ref, w8a16_bound(xb, qw, sw, 1), x_bf16.shape[1])
 
 
 @pytest.mark.parametrize("m", [1, 3, 8, 9, 16, 17, 32, 33, 64, 65, 100])
@@ -271,8 +281,11 @@ def test_w8a16_qwen3_8b_sampled(m):
     x = synthetic.activations(m, k, 4)
     y = gpu_w8a16(x, qw, sw)
     pm, pn = _points(m, n, 4000, m)
-    ref = oracle.w8a16_points(util.bits(x), qw, sw, pm, pn)
+    xb = util.bits(x)
+    ref = oracle.w8a16_points(xb, qw, sw, pm, pn)
     assert util.rel_frobenius(y[pm, pn], ref) <= W8A16_FROB
+    ax, aq = _abs_inputs(xb, qw)
+    check_elementwise(y[pm, pn], ref, oracle.w8a16_points(ax, aq, sw, pm, pn), k)
 
 
 # ------------------------------------------------------------------ grouped W8A16
@@ -305,12 +318,12 @@ def test_grouped_small(counts):
     off[1:] = np.cumsum(counts)
     x = synthetic.activations(int(off[-1]), k, 51)
     y = gpu_grouped(x, off, q, s)
-    ref = oracle.grouped_w8a16(util.bits(x), off, q, s)
+    xb = util.bits(x)
+    ref = oracle.grouped_w8a16(xb, off, q, s)
     assert util.rel_frobenius(y, ref) <= W8A16_FROB
-    for e in range(len(counts)):
-        lo, hi = off[e], off[e + 1]
-        if hi > lo:
-            assert util.rel_frobenius(y[lo:hi], ref[lo:hi]) <= W8A16_FROB
+    ax, aq = _abs_inputs(xb, q)
+    mag = oracle.grouped_w8a16(ax, off, aq, s)
+    check_elementwise(y, ref, mag, k)
 
 
 @pytest.fixture(scope="module")
@@ -338,14 +351,20 @@ def test_grouped_dsmoe_sampled(dsmoe_experts, tokens, proj):
     y = gpu_grouped(x, r.offsets, q, s)
     xb = util.bits(x)
     g = np.random.default_rng(tokens)
+    got, want, mags = [], [], []
     for e in range(66):
         lo, hi = int(r.offsets[e]), int(r.offsets[e + 1])
         if hi == lo:
             continue
-        pm = g.integers(lo, hi, 24) - lo
-        pn = g.integers(0, n, 24)
+        pm = g.integers(lo, hi, 160) - lo
+        pn = g.integers(0, n, 160)
         ref = oracle.w8a16_points(xb[lo:hi], q[e], s[e], pm, pn)
-        assert util.rel_frobenius(y[lo + pm, pn], ref) <= W8A16_FROB
+        ax, aq = _abs_inputs(xb[lo:hi], q[e])
+        mag = oracle.w8a16_points(ax, aq, s[e], pm, pn)
+        check_elementwise(y[lo + pm, pn], ref, mag, k)
+        got.append(y[lo + pm, pn])
+        want.append(ref)
+    assert util.rel_frobenius(np.concatenate(got), np.concatenate(want)) <= W8A16_FROB
 
 
 def test_grouped_bad_offsets_reported():
