@@ -45,12 +45,18 @@ struct LaunchEnv {
 // on first use.  Returns false (and sets *status) on failure.
 bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status);
 
-// Kernel launchers (one per operation).  They assume validated arguments.
+// Kernel launchers.  They assume validated arguments.
+// W8A8 up to this many tokens runs on the decode kernel (int8 mma.sync,
+// weight streaming); larger M runs on the tcgen05 kernel.
+constexpr int64_t kW8A8DecodeMaxM = 64;
 cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
                               const LaunchEnv& env);
 cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw,
                          const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
                          const LaunchEnv& env);
+cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                               const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
+                               int64_t K, const LaunchEnv& env);
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                         const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                         int64_t K, const LaunchEnv& env);

@@ -1,0 +1,423 @@
+// Decode-size GEMMs (few tokens, weight streaming): W8A16, grouped W8A16 over
+// MoE experts, and W8A8 for small M.
+//
+// Sources: "Day 6 -- Quantize It Yourself", The mechanism, block 5 (weight-
+// only int8 is dequantized inside the kernel and multiplied on bf16 math, a
+// pure memory-bandwidth win for decode; W8A8 multiplies 8-bit operands on the
+// tensor cores); "Phase 5a: int8 weight-only quantization", Summary (grouped
+// GEMM over MoE experts with stacked [E, N, K] int8 weights and per-output-
+// channel scales); "feat(quantization): support compressed-tensors W8A8 and
+// mixed modules", Design and Supported Execution Scheme (per-channel int8
+// weights, per-token int8 activations, no output quantization).
+//
+//   W8A16: y[m,n] = bf16_rne(sw[n] * sum_k q[n,k] * x[m,k])          (fp32 acc)
+//   W8A8:  y[m,n] = bf16_rne(((float)acc * sx[m]) * sw[n] (+ bias[n])),
+//          acc = sum_k qx[m,k] * qw[n,k]                              (exact int32)
+//
+// Design (bandwidth kernel, one HBM pass over the int8 weights):
+//  * Each lane streams 16-byte vectors of int8 weights (ld.global.nc) through
+//    a 4-deep register ring (three k-steps in flight per lane while one is
+//    computed): a warp reads 64 contiguous bytes of each of its 32 rows per
+//    64-wide k-step.  The grid is one wave of resident CTAs.
+//  * Weights are the 16-row A operand of legacy warp-level mma.sync and the
+//    tokens the 8-wide B operand ("swap AB"), so the MMA does no work on
+//    absent tokens beyond the 8-token granule.
+//      W8A16: int8 codes become bf16 in registers (exact, |q| <= 127) and run
+//      m16n8k16 bf16 with fp32 accumulation; the fp32 scale is applied once
+//      per output, so s * q is never rounded to bf16.
+//      W8A8: codes and token codes go straight into m16n8k32 s8 x s8 -> s32,
+//      with no conversion at all and an exact int32 accumulator.
+//  * The k order inside a 64-wide k-step is permuted identically for A and B
+//    (lane t owns k = 16t .. 16t+15), so every lane loads weights and tokens
+//    with plain 16-byte vectors and no shuffles.
+//  * Split-K without global scratch: the S CTAs of a thread-block cluster own
+//    disjoint k-ranges of the same rows; the four warps of a CTA are reduced
+//    in shared memory, then the cluster through distributed shared memory, in
+//    a fixed rank order (deterministic; exact for the int32 W8A8 sums).
+//  * Grouped: blockIdx.z is the expert; an expert without rows exits before
+//    reading any weight.  Offsets are validated on the device; a bad expert
+//    is skipped and reported through the sticky fault word.
+// HBM traffic per launch: N*K weight bytes + 4N scale bytes (per active
+// expert) + token and output bytes.
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace i8ql {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxClusterSplit = 8;
+
+enum class Op { kW8A16, kW8A8 };
+
+struct DecodeParams {
+    const void* x;           // bf16 [rows, K] (W8A16) or int8 [rows, K] (W8A8)
+    const float* sx;         // W8A8 per-token scales [rows]
+    const int32_t* offsets;  // grouped: [E + 1]; null otherwise
+    const int8_t* qw;
+    const float* sw;
+    const uint16_t* bias;    // W8A8 only, nullable
+    uint16_t* y;
+    int32_t* acc;            // W8A8 only, nullable
+    int64_t rows;            // M (plain) or T_total (grouped)
+    int64_t N;
+    int64_t K;
+    int64_t E;
+    unsigned* err;
+};
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_cached(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+// Four int8 codes -> two bf16x2 words (exact).  Each byte b is biased to
+// u = b + 128, placed in the low mantissa bits of 2^23 (float 2^23 + u),
+// and 2^23 + 128 is subtracted (packed f32x2); the upper halves of the exact
+// fp32 results are the bf16 values.
+__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t f0 = __byte_perm(u, 0x4b000000u, 0x7440);
+    const uint32_t f1 = __byte_perm(u, 0x4b000000u, 0x7441);
+    const uint32_t f2 = __byte_perm(u, 0x4b000000u, 0x7442);
+    const uint32_t f3 = __byte_perm(u, 0x4b000000u, 0x7443);
+    const uint64_t bias = 0xcb000080cb000080ull;  // (-(2^23 + 128), -(2^23 + 128))
+    uint64_t p01 = ((uint64_t)f1 << 32) | f0;
+    uint64_t p23 = ((uint64_t)f3 << 32) | f2;
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p01) : "l"(bias));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p23) : "l"(bias));
+    lo = __byte_perm((uint32_t)p01, (uint32_t)(p01 >> 32), 0x7632);
+    hi = __byte_perm((uint32_t)p23, (uint32_t)(p23 >> 32), 0x7632);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_s8(int32_t (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                       uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+template <int MT>
+struct WeightRegs {
+    uint4 r[MT][2];  // rows g and g+8 of each 16-row m-tile
+};
+
+// Depth of the per-lane register ring of weight loads: while one k-step is
+// converted and multiplied, the next kStages - 1 are in flight.
+constexpr int kStages = 4;
+
+// MT 16-row m-tiles per warp, NT 8-token n-tiles per pass.
+template <Op OP, int MT, int NT, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
+    decode_gemm_kernel(const DecodeParams p) {
+    using Acc = std::conditional_t<OP == Op::kW8A8, int32_t, float>;
+    constexpr int kRows = 16 * MT;
+    constexpr int kToks = 8 * NT;
+    __shared__ Acc part[kWarps][kToks * kRows];
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int64_t N = p.N, K = p.K;
+    const int64_t n0 = (int64_t)blockIdx.x * kRows;
+
+    // Row range of this expert (grouped) or of the whole batch.
+    int64_t lo = 0, hi = p.rows;
+    const int8_t* qw = p.qw;
+    const float* sw = p.sw;
+    if constexpr (GROUPED) {
+        const int64_t e = blockIdx.z;
+        const int64_t a = p.offsets[e], b = p.offsets[e + 1];
+        const bool bad = a < 0 || b < a || b > p.rows || (e == 0 && a != 0) || (e == p.E - 1 && b != p.rows);
+        if (bad) {
+            if (blockIdx.x == 0 && rank == 0 && threadIdx.x == 0) record_fault(p.err, kErrBitBadOffsets);
+            return;  // the whole cluster shares e, so all of it leaves here
+        }
+        lo = a;
+        hi = b;
+        qw += e * N * K;
+        sw += e * N;
+    }
+    if (hi <= lo) return;  // an empty expert reads no weights
+
+    // This warp's k-steps (64 k each) within the cluster's split of K.
+    const int64_t ksteps = (K + 63) / 64;
+    const int units = S * kWarps;
+    const int unit = rank * kWarps + warp;
+    const int64_t ks_begin = ksteps * unit / units;
+    const int64_t ks_end = ksteps * (unit + 1) / units;
+
+    // Weight row pointers of this lane (rows past N are never loaded).
+    const int8_t* wrow[MT][2];
+    bool wok[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t n = n0 + mt * 16 + g + 8 * h;
+            wok[mt][h] = n < N;
+            wrow[mt][h] = qw + (wok[mt][h] ? n : 0) * K + 16 * t;
+        }
+
+    auto load_w = [&](WeightRegs<MT>& w, int64_t ks) {
+        const int64_t k0 = ks * 64;
+        const bool kok = k0 + 16 * t < K;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                w.r[mt][h] = (kok && wok[mt][h]) ? ldg_stream(wrow[mt][h] + k0) : make_uint4(0, 0, 0, 0);
+    };
+
+    for (int64_t c0 = lo; c0 < hi; c0 += kToks) {
+        const int64_t chunk = min((int64_t)kToks, hi - c0);
+        const int nt_active = (int)((chunk + 7) / 8);
+
+        Acc acc[MT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[mt][nt][i] = Acc(0);
+
+        auto compute = [&](const WeightRegs<MT>& w, int64_t ks) {
+            const int64_t k0 = ks * 64 + 16 * t;
+            const bool kok = k0 < K;
+            if constexpr (OP == Op::kW8A16) {
+                uint32_t xb[NT][8];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int64_t m = c0 + nt * 8 + g;
+                    if (nt < nt_active && kok && m < hi) {
+                        const uint16_t* xp = static_cast<const uint16_t*>(p.x) + m * K + k0;
+                        const uint4 v0 = ldg_cached(xp);
+                        const uint4 v1 = ldg_cached(xp + 8);
+                        xb[nt][0] = v0.x; xb[nt][1] = v0.y; xb[nt][2] = v0.z; xb[nt][3] = v0.w;
+                        xb[nt][4] = v1.x; xb[nt][5] = v1.y; xb[nt][6] = v1.z; xb[nt][7] = v1.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) xb[nt][i] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const uint32_t wg[4] = {w.r[mt][0].x, w.r[mt][0].y, w.r[mt][0].z, w.r[mt][0].w};
+                    const uint32_t wh[4] = {w.r[mt][1].x, w.r[mt][1].y, w.r[mt][1].z, w.r[mt][1].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0, a2, a1, a3;
+                        i8x4_to_bf16(wg[j], a0, a2);  // row g:   k 16t+4j+{0,1} | {2,3}
+                        i8x4_to_bf16(wh[j], a1, a3);  // row g+8: same k
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            if (nt < nt_active)
+                                mma_bf16(acc[mt][nt], a0, a1, a2, a3, xb[nt][2 * j], xb[nt][2 * j + 1]);
+                    }
+                }
+            } else {
+                uint32_t xb[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int64_t m = c0 + nt * 8 + g;
+                    if (nt < nt_active && kok && m < hi) {
+                        const uint4 v = ldg_cached(static_cast<const int8_t*>(p.x) + m * K + k0);
+                        xb[nt][0] = v.x; xb[nt][1] = v.y; xb[nt][2] = v.z; xb[nt][3] = v.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) xb[nt][i] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const uint32_t wg[4] = {w.r[mt][0].x, w.r[mt][0].y, w.r[mt][0].z, w.r[mt][0].w};
+                    const uint32_t wh[4] = {w.r[mt][1].x, w.r[mt][1].y, w.r[mt][1].z, w.r[mt][1].w};
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        // k 16t+8j+{0..3} -> fragment slot 4t..4t+3, k 16t+8j+{4..7} -> slot 16+4t..
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            if (nt < nt_active)
+                                mma_s8(acc[mt][nt], wg[2 * j], wh[2 * j], wg[2 * j + 1], wh[2 * j + 1],
+                                       xb[nt][2 * j], xb[nt][2 * j + 1]);
+                    }
+                }
+            }
+        };
+
+        {
+            WeightRegs<MT> ring[kStages];
+#pragma unroll
+            for (int s = 0; s < kStages; ++s)
+                if (ks_begin + s < ks_end) load_w(ring[s], ks_begin + s);
+            for (int64_t ks = ks_begin; ks < ks_end; ks += kStages) {
+#pragma unroll
+                for (int s = 0; s < kStages; ++s) {
+                    if (ks + s < ks_end) {
+                        compute(ring[s], ks + s);
+                        if (ks + s + kStages < ks_end) load_w(ring[s], ks + s + kStages);
+                    }
+                }
+            }
+        }
+
+        // Warp partials -> shared memory, laid out [token][row].
+        Acc* mine = part[warp];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int r = mt * 16 + g;
+                const int c = nt * 8 + 2 * t;
+                mine[c * kRows + r] = acc[mt][nt][0];
+                mine[(c + 1) * kRows + r] = acc[mt][nt][1];
+                mine[c * kRows + r + 8] = acc[mt][nt][2];
+                mine[(c + 1) * kRows + r + 8] = acc[mt][nt][3];
+            }
+        __syncthreads();
+        for (int i = threadIdx.x; i < kToks * kRows; i += kThreads) {
+            Acc s = part[0][i];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) s += part[w][i];
+            part[0][i] = s;
+        }
+        // Publish to the cluster, then each rank finishes a slice of the tile.
+        cluster.sync();
+        const int total = nt_active * 8 * kRows;
+        const int per = (total + S - 1) / S;
+        const int i_begin = rank * per;
+        const int i_end = min(total, i_begin + per);
+        for (int i = i_begin + (int)threadIdx.x; i < i_end; i += kThreads) {
+            Acc s = Acc(0);
+            for (int r = 0; r < S; ++r) s += cluster.map_shared_rank(&part[0][0], r)[i];
+            const int row = i % kRows;
+            const int tok = i / kRows;
+            const int64_t n = n0 + row;
+            const int64_t m = c0 + tok;
+            if (n < N && m < hi) {
+                if constexpr (OP == Op::kW8A16) {
+                    p.y[m * N + n] = f32_to_bf16_rn(s * sw[n]);
+                } else {
+                    float f = __fmul_rn(__fmul_rn(__int2float_rn(s), p.sx[m]), sw[n]);
+                    if (p.bias) f = __fadd_rn(f, bf16_to_f32(p.bias[n]));
+                    p.y[m * N + n] = f32_to_bf16_rn(f);
+                    if (p.acc) p.acc[m * N + n] = s;
+                }
+            }
+        }
+        cluster.sync();  // peers are done reading this CTA's shared memory
+    }
+}
+
+template <Op OP, int MT, int NT, bool GROUPED>
+cudaError_t launch_cfg(const DecodeParams& p, int split, cudaStream_t stream) {
+    constexpr int kRows = 16 * MT;
+    const int64_t row_blocks = (p.N + kRows - 1) / kRows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)row_blocks, (unsigned)split, (unsigned)(GROUPED ? p.E : 1));
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)split;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<OP, MT, NT, GROUPED>, p);
+}
+
+// CTAs of this configuration that fit on one SM at once (cached per device).
+template <Op OP, int MT, int NT, bool GROUPED>
+int resident_ctas() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 1;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_gemm_kernel<OP, MT, NT, GROUPED>, kThreads, 0) !=
+                cudaSuccess || n < 1)
+            n = 1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Split-K factor: fill one wave of resident CTAs (no tail wave), keep at
+// least two k-steps per warp, and stay within one portable cluster.
+int choose_split(int64_t row_blocks, int64_t groups, int64_t K, int64_t capacity) {
+    const int64_t ksteps = (K + 63) / 64;
+    int64_t split = capacity / std::max<int64_t>(1, row_blocks * groups);
+    split = std::min<int64_t>(split, std::max<int64_t>(1, ksteps / (2 * kWarps)));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(split, kMaxClusterSplit));
+}
+
+template <Op OP, int MT, int NT, bool GROUPED>
+cudaError_t launch_auto(const DecodeParams& p, int64_t groups_hint, int sms, cudaStream_t stream) {
+    const int64_t row_blocks = (p.N + 16 * MT - 1) / (16 * MT);
+    const int64_t capacity = (int64_t)sms * resident_ctas<OP, MT, NT, GROUPED>();
+    return launch_cfg<OP, MT, NT, GROUPED>(p, choose_split(row_blocks, groups_hint, p.K, capacity), stream);
+}
+
+template <Op OP, bool GROUPED>
+cudaError_t dispatch(const DecodeParams& p, int64_t tokens_hint, int64_t groups_hint, int sms, cudaStream_t stream) {
+    if (tokens_hint <= 8) return launch_auto<OP, 2, 1, GROUPED>(p, groups_hint, sms, stream);
+    if (tokens_hint <= 16) return launch_auto<OP, 2, 2, GROUPED>(p, groups_hint, sms, stream);
+    if (tokens_hint <= 32) return launch_auto<OP, 2, 4, GROUPED>(p, groups_hint, sms, stream);
+    return launch_auto<OP, 2, 8, GROUPED>(p, groups_hint, sms, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw, const float* sw,
+                         uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env) {
+    DecodeParams p{x, nullptr, offsets, qw, sw, nullptr, y, nullptr, M, N, K, E, env.err};
+    if (offsets == nullptr) return dispatch<Op::kW8A16, false>(p, M, 1, env.sm_count, env.stream);
+    // Grouped: at most min(E, T_total) experts have rows, on average
+    // T_total / active rows each.
+    const int64_t active = std::min<int64_t>(E, M);
+    const int64_t per_expert = (M + active - 1) / active;
+    return dispatch<Op::kW8A16, true>(p, std::max<int64_t>(per_expert, 1), active, env.sm_count, env.stream);
+}
+
+cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                               const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                               const LaunchEnv& env) {
+    DecodeParams p{qx, sx, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err};
+    return dispatch<Op::kW8A8, false>(p, M, 1, env.sm_count, env.stream);
+}
+
+}  // namespace i8ql

@@ -20,13 +20,14 @@
 //    convert it to int32 (exact) and add it to an int32 running sum kept in
 //    a second TMEM region; the next chunk restarts the fp32 accumulator.
 //
-// Warp roles (416 threads, one CTA per output tile, 1 CTA per SM):
+// Warp roles (544 threads, one CTA per output tile, 1 CTA per SM):
 //  * warps 0-3: epilogue (warp w owns TMEM lanes 32w .. 32w+31);
 //  * warp 4: TMEM allocation and the single-thread MMA issuer;
-//  * warps 5-12: converters.  They stream 16-byte int8 vectors from global
-//    memory, turn them into fp16 in registers (bias-and-subtract trick, exact),
-//    and store them in the 128-byte-swizzled K-major layout the MMA reads,
-//    through a 4-stage shared-memory ring guarded by mbarriers.
+//  * warps 5-16: converters.  They stream 16-byte int8 vectors from global
+//    memory (three stages of loads in flight per thread), turn them into
+//    fp16 in registers (bias-and-subtract trick, exact), and store them in
+//    the 128-byte-swizzled K-major layout the MMA reads, through a 4-stage
+//    shared-memory ring guarded by mbarriers.
 // Tile: 128 rows of operand A x BN rows of operand B x 64 k per stage.
 // Large M: A = activations, B = weights, BN = 256.  M <= 128 ("swap AB"):
 // A = weights, B = tokens, BN = M rounded up to 16, so the tensor core does
@@ -51,8 +52,10 @@ constexpr int kMaxBN = 256;
 constexpr int kChunkKB = 16;  // k-blocks per exact fp32 chunk (1024 k)
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 12;
 constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kConvDepth = 3;  // stages of int8 loads each converter keeps in flight
+constexpr int kGroupA = 8;     // tile rows of A swept together (L2 reuse of B tiles)
 constexpr int kThreads = (kEpiWarps + 1 + kConvWarps) * 32;
 constexpr int kAStageBytes = kBM * kBK * 2;
 constexpr int kBStageBytes = kMaxBN * kBK * 2;
@@ -69,6 +72,7 @@ struct W8A8Params {
     uint16_t* y;
     int32_t* acc;
     int64_t M, N;
+    int64_t tiles_a;
     int64_t tiles_b;
     int bn;
     int swap;
@@ -232,6 +236,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
+    static_assert(kMaxConvItems * kConvThreads == (kBM + kMaxBN) * 4, "converter work must divide evenly");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_stages = smem;
@@ -240,9 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Grouped raster: consecutive CTAs sweep kGroupA tile rows of A for each
+    // tile column of B, so a wave shares a few A row blocks and B tiles in L2.
     const int64_t tile = blockIdx.x;
-    const int64_t tile_b = tile % p.tiles_b;
-    const int64_t tile_a = tile / p.tiles_b;
+    const int64_t group_tiles = (int64_t)kGroupA * p.tiles_b;
+    const int64_t first_a = (tile / group_tiles) * kGroupA;
+    const int64_t rows_in_group = min((int64_t)kGroupA, p.tiles_a - first_a);
+    const int64_t local = tile % group_tiles;
+    const int64_t tile_a = first_a + local % rows_in_group;
+    const int64_t tile_b = local / rows_in_group;
     const int bn = p.bn;
     const int64_t K = p.K;
     const int nkb = (int)((K + kBK - 1) / kBK);
@@ -313,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
         const int items = (kBM + bn) * 4;
         const int64_t a_row0 = tile_a * kBM;
         const int64_t b_row0 = tile_b * bn;
-        uint4 v[kMaxConvItems];
-        auto load_stage = [&](int kb) {
+        uint4 v[kConvDepth][kMaxConvItems];
+        auto load_stage = [&](uint4 (&dst)[kMaxConvItems], int kb) {
             const int64_t k0 = (int64_t)kb * kBK;
 #pragma unroll
             for (int j = 0; j < kMaxConvItems; ++j) {
                 const int item = ct + j * kConvThreads;
-                v[j] = make_uint4(0, 0, 0, 0);
+                dst[j] = make_uint4(0, 0, 0, 0);
                 if (item < items) {
                     const bool is_a = item < kBM * 4;
                     const int it = is_a ? item : item - kBM * 4;
@@ -328,41 +339,52 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
                     const int64_t grow = (is_a ? a_row0 : b_row0) + row;
                     const int64_t k = k0 + 16 * c;
                     if (grow < (is_a ? p.rows_a : p.rows_b) && k < K)
-                        v[j] = ldg_stream((is_a ? p.a : p.b) + grow * K + k);
+                        dst[j] = ldg_stream((is_a ? p.a : p.b) + grow * K + k);
                 }
             }
         };
-        load_stage(0);
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb % kStages;
-            if (!warp_wait(&ctl->empty[st], (uint32_t)(((kb / kStages) & 1) ^ 1), ctl, p.err)) break;
-            const uint32_t a_buf = smem_u32(a_stages + st * kAStageBytes);
-            const uint32_t b_buf = smem_u32(b_stages + st * kBStageBytes);
 #pragma unroll
-            for (int j = 0; j < kMaxConvItems; ++j) {
-                const int item = ct + j * kConvThreads;
-                if (item < items) {
-                    const bool is_a = item < kBM * 4;
-                    const int it = is_a ? item : item - kBM * 4;
-                    const int row = it >> 2;
-                    const int c = it & 3;
-                    uint32_t h[8];
-                    i8x4_to_f16(v[j].x, h[0], h[1]);
-                    i8x4_to_f16(v[j].y, h[2], h[3]);
-                    i8x4_to_f16(v[j].z, h[4], h[5]);
-                    i8x4_to_f16(v[j].w, h[6], h[7]);
-                    const uint32_t row_base = (is_a ? a_buf : b_buf) + (row >> 3) * 1024 + (row & 7) * 128;
-                    const uint32_t c0 = (uint32_t)((2 * c) ^ (row & 7));
-                    const uint32_t c1 = (uint32_t)((2 * c + 1) ^ (row & 7));
-                    st_shared_v4(row_base + c0 * 16, h[0], h[1], h[2], h[3]);
-                    st_shared_v4(row_base + c1 * 16, h[4], h[5], h[6], h[7]);
+        for (int d = 0; d < kConvDepth; ++d)
+            if (d < nkb) load_stage(v[d], d);
+        bool alive = true;
+        for (int kb0 = 0; kb0 < nkb && alive; kb0 += kConvDepth) {
+#pragma unroll
+            for (int d = 0; d < kConvDepth; ++d) {
+                const int kb = kb0 + d;
+                if (kb >= nkb || !alive) break;
+                const int st = kb % kStages;
+                if (!warp_wait(&ctl->empty[st], (uint32_t)(((kb / kStages) & 1) ^ 1), ctl, p.err)) {
+                    alive = false;
+                    break;
                 }
+                const uint32_t a_buf = smem_u32(a_stages + st * kAStageBytes);
+                const uint32_t b_buf = smem_u32(b_stages + st * kBStageBytes);
+#pragma unroll
+                for (int j = 0; j < kMaxConvItems; ++j) {
+                    const int item = ct + j * kConvThreads;
+                    if (item < items) {
+                        const bool is_a = item < kBM * 4;
+                        const int it = is_a ? item : item - kBM * 4;
+                        const int row = it >> 2;
+                        const int c = it & 3;
+                        uint32_t h[8];
+                        i8x4_to_f16(v[d][j].x, h[0], h[1]);
+                        i8x4_to_f16(v[d][j].y, h[2], h[3]);
+                        i8x4_to_f16(v[d][j].z, h[4], h[5]);
+                        i8x4_to_f16(v[d][j].w, h[6], h[7]);
+                        const uint32_t row_base = (is_a ? a_buf : b_buf) + (row >> 3) * 1024 + (row & 7) * 128;
+                        const uint32_t c0 = (uint32_t)((2 * c) ^ (row & 7));
+                        const uint32_t c1 = (uint32_t)((2 * c + 1) ^ (row & 7));
+                        st_shared_v4(row_base + c0 * 16, h[0], h[1], h[2], h[3]);
+                        st_shared_v4(row_base + c1 * 16, h[4], h[5], h[6], h[7]);
+                    }
+                }
+                // make the generic-proxy stores visible to the tensor core
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->full[st]);
+                if (kb + kConvDepth < nkb) load_stage(v[d], kb + kConvDepth);
             }
-            // make the generic-proxy stores visible to the tensor core
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->full[st]);
-            if (kb + 1 < nkb) load_stage(kb + 1);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -401,14 +423,39 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
                     const int64_t m = arow;
                     if (m < p.M) {
                         const float sxm = p.sx[m];
+                        if (bcol0 + 16 <= p.N && (p.N & 7) == 0) {
+                            // whole group in range and 16-byte aligned: vector stores
+                            uint32_t packed[8];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int64_t n = bcol0 + j;
-                            if (n < p.N) {
-                                float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), sxm), __ldg(p.sw + n));
-                                if (p.bias) f = __fadd_rn(f, bf16_to_f32(__ldg(p.bias + n)));
-                                p.y[m * p.N + n] = f32_to_bf16_rn(f);
-                                if (p.acc) p.acc[m * p.N + n] = v[j];
+                            for (int j = 0; j < 16; j += 2) {
+                                float f0 = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), sxm), __ldg(p.sw + bcol0 + j));
+                                float f1 =
+                                    __fmul_rn(__fmul_rn(__int2float_rn(v[j + 1]), sxm), __ldg(p.sw + bcol0 + j + 1));
+                                if (p.bias) {
+                                    f0 = __fadd_rn(f0, bf16_to_f32(__ldg(p.bias + bcol0 + j)));
+                                    f1 = __fadd_rn(f1, bf16_to_f32(__ldg(p.bias + bcol0 + j + 1)));
+                                }
+                                packed[j / 2] = (uint32_t)f32_to_bf16_rn(f0) | ((uint32_t)f32_to_bf16_rn(f1) << 16);
+                            }
+                            uint4* yp = reinterpret_cast<uint4*>(p.y + m * p.N + bcol0);
+                            yp[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            yp[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                            if (p.acc) {
+                                int4* ap = reinterpret_cast<int4*>(p.acc + m * p.N + bcol0);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    ap[q] = make_int4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int64_t n = bcol0 + j;
+                                if (n < p.N) {
+                                    float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), sxm), __ldg(p.sw + n));
+                                    if (p.bias) f = __fadd_rn(f, bf16_to_f32(__ldg(p.bias + n)));
+                                    p.y[m * p.N + n] = f32_to_bf16_rn(f);
+                                    if (p.acc) p.acc[m * p.N + n] = v[j];
+                                }
                             }
                         }
                     }
@@ -459,6 +506,7 @@ uint32_t pow2_cols(int need) {
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                         const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
                         const LaunchEnv& env) {
+    if (M <= kW8A8DecodeMaxM) return launch_w8a8_decode(qx, sx, qw, sw, bias, y, acc, M, N, K, env);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -499,6 +547,7 @@ cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, con
         p.tiles_b = (N + kMaxBN - 1) / kMaxBN;
         tiles_a = (M + kBM - 1) / kBM;
     }
+    p.tiles_a = tiles_a;
     p.tmem_cols = pow2_cols(2 * p.bn);
     const int64_t tiles = tiles_a * p.tiles_b;
     w8a8_kernel<<<dim3((unsigned)tiles), kThreads, kSmemBytes, env.stream>>>(p);
