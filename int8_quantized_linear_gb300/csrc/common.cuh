@@ -34,6 +34,43 @@ __device__ __forceinline__ void record_fault(unsigned* err, unsigned bit) {
     if (err) atomicOr(err, bit);
 }
 
+// Programmatic dependent launch: every kernel is launched with programmatic
+// stream serialization and waits here, before touching global memory, for the
+// grids it depends on to complete (a no-op when launched without it).  Its
+// launch and prologue can then overlap the tail of the previous kernel.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream begin launching (its CTAs still wait in
+// pdl_wait() for this grid to finish).  Called only by grids that fit in one
+// wave, so early dependents never take SM slots this grid still needs.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// cudaLaunchKernelEx with programmatic stream serialization and, when
+// cluster_y > 0, a (1, cluster_y, 1) thread-block cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          unsigned cluster_y, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    unsigned n = 0;
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_y > 0) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = 1;
+        attrs[n].val.clusterDim.y = cluster_y;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launch parameters every entry point passes down.
 struct LaunchEnv {
     cudaStream_t stream;

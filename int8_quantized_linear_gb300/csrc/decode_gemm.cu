@@ -73,6 +73,7 @@ struct DecodeParams {
     int64_t K;
     int64_t E;
     unsigned* err;
+    int one_wave;            // every CTA of the grid is resident at once
 };
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
@@ -143,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
     constexpr int kToks = 8 * NT;
     __shared__ Acc part[kWarps][kToks * kRows];
 
+    pdl_wait();
+    if (p.one_wave) pdl_launch_dependents();
     cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -345,19 +348,9 @@ template <Op OP, int MT, int NT, bool GROUPED>
 cudaError_t launch_cfg(const DecodeParams& p, int split, cudaStream_t stream) {
     constexpr int kRows = 16 * MT;
     const int64_t row_blocks = (p.N + kRows - 1) / kRows;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)row_blocks, (unsigned)split, (unsigned)(GROUPED ? p.E : 1));
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)split;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_gemm_kernel<OP, MT, NT, GROUPED>, p);
+    return launch_kernel(decode_gemm_kernel<OP, MT, NT, GROUPED>,
+                         dim3((unsigned)row_blocks, (unsigned)split, (unsigned)(GROUPED ? p.E : 1)), dim3(kThreads),
+                         0, stream, (unsigned)split, p);
 }
 
 // CTAs of this configuration that fit on one SM at once (cached per device).
@@ -386,10 +379,12 @@ int choose_split(int64_t row_blocks, int64_t groups, int64_t K, int64_t capacity
 }
 
 template <Op OP, int MT, int NT, bool GROUPED>
-cudaError_t launch_auto(const DecodeParams& p, int64_t groups_hint, int sms, cudaStream_t stream) {
+cudaError_t launch_auto(DecodeParams p, int64_t groups_hint, int sms, cudaStream_t stream) {
     const int64_t row_blocks = (p.N + 16 * MT - 1) / (16 * MT);
     const int64_t capacity = (int64_t)sms * resident_ctas<OP, MT, NT, GROUPED>();
-    return launch_cfg<OP, MT, NT, GROUPED>(p, choose_split(row_blocks, groups_hint, p.K, capacity), stream);
+    const int split = choose_split(row_blocks, groups_hint, p.K, capacity);
+    p.one_wave = row_blocks * split * (GROUPED ? p.E : 1) <= capacity ? 1 : 0;
+    return launch_cfg<OP, MT, NT, GROUPED>(p, split, stream);
 }
 
 template <Op OP, bool GROUPED>
@@ -404,7 +399,7 @@ cudaError_t dispatch(const DecodeParams& p, int64_t tokens_hint, int64_t groups_
 
 cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw, const float* sw,
                          uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env) {
-    DecodeParams p{x, nullptr, offsets, qw, sw, nullptr, y, nullptr, M, N, K, E, env.err};
+    DecodeParams p{x, nullptr, offsets, qw, sw, nullptr, y, nullptr, M, N, K, E, env.err, 0};
     if (offsets == nullptr) return dispatch<Op::kW8A16, false>(p, M, 1, env.sm_count, env.stream);
     // Grouped: at most min(E, T_total) experts have rows, on average
     // T_total / active rows each.
@@ -416,7 +411,7 @@ cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, c
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                const LaunchEnv& env) {
-    DecodeParams p{qx, sx, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err};
+    DecodeParams p{qx, sx, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err, 0};
     return dispatch<Op::kW8A8, false>(p, M, 1, env.sm_count, env.stream);
 }
 

@@ -11,8 +11,10 @@
 // vector loads), its absmax is reduced across the threads that own it, and
 // the codes are written from the same registers.  Rows longer than the
 // register budget are read a second time (an L2 hit).  The arithmetic is
-// IEEE fp32: __fdiv_rn for both a / 127 and v / s, __float2int_rn (ties to
-// even) for the rounding, no flush of subnormals (built without fast math).
+// IEEE fp32: __fdiv_rn for a / 127; the code of each element is the
+// round-half-even of the IEEE quotient v / s, obtained from a multiply by the
+// correctly rounded reciprocal except near ties, where the division itself
+// is taken (see code()); no flush of subnormals (built without fast math).
 // HBM traffic: 2 bytes read + 1 byte written per element, plus 4 bytes per row.
 
 #include <cuda_runtime.h>
@@ -39,15 +41,38 @@ __device__ __forceinline__ float absmax8(const uint4& v, float a) {
     return a;
 }
 
-__device__ __forceinline__ uint32_t code(float v, float s) {
-    int c = __float2int_rn(__fdiv_rn(v, s));
+// The code of v is rint(fl32(v / s)).  Fast path: t = fl32(v * r) with
+// r = fl32(1 / s) (correctly rounded).  Each of the two roundings is within
+// half an ulp, so |t - v/s| <= |v/s| * (2^-23 + 2^-48), and fl32(v/s) is
+// within |v/s| * 2^-24 of v/s; with |v/s| <= 127 * (1 + 2^-23) the two
+// quotients differ by less than 2.3e-5.  rint changes value only at
+// half-integers, so when t is farther than kNearTie = 2^-15 from the nearest
+// half-integer, rint(t) == rint(fl32(v/s)).  Near-ties (and a reciprocal that
+// overflowed, when s is subnormal) take the IEEE division.
+constexpr float kNearTie = 3.0517578125e-05f;  // 2^-15
+
+struct RowScale {
+    float s;     // the scale
+    float r;     // fl32(1 / s)
+    bool fast;   // r is finite
+};
+
+__device__ __forceinline__ uint32_t code(float v, const RowScale& rs) {
+    int c;
+    const float t = __fmul_rn(v, rs.r);
+    const float fl = floorf(t);
+    if (rs.fast && fabsf(t - fl - 0.5f) > kNearTie) {
+        c = __float2int_rn(t);
+    } else {
+        c = __float2int_rn(__fdiv_rn(v, rs.s));
+    }
     c = max(-127, min(127, c));
     return static_cast<uint32_t>(c) & 0xffu;
 }
 
-__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float s) {
-    return code(lo_bf16(w0), s) | (code(hi_bf16(w0), s) << 8) | (code(lo_bf16(w1), s) << 16) |
-           (code(hi_bf16(w1), s) << 24);
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, const RowScale& rs) {
+    return code(lo_bf16(w0), rs) | (code(hi_bf16(w0), rs) << 8) | (code(lo_bf16(w1), rs) << 16) |
+           (code(hi_bf16(w1), rs) << 24);
 }
 
 __device__ __forceinline__ uint4 load_nc(const uint4* p) {
@@ -63,7 +88,9 @@ __device__ __forceinline__ uint4 load_nc(const uint4* p) {
 template <int TPR, int VPT>
 __global__ void __launch_bounds__(kQuantThreads)
 quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
-                  int8_t* __restrict__ q, float* __restrict__ scale) {
+                  int8_t* __restrict__ q, float* __restrict__ scale, int one_wave) {
+    pdl_wait();
+    if (one_wave) pdl_launch_dependents();
     constexpr int kRowsPerCta = kQuantThreads / TPR;
     constexpr int kWarpsPerRow = TPR / 32;
     __shared__ float warp_max[kQuantThreads / 32];
@@ -110,29 +137,35 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
     const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 127.0f);
     if (!valid) return;
     if (lt == 0) scale[row] = s;
+    RowScale rs;
+    rs.s = s;
+    rs.r = __frcp_rn(s);
+    rs.fast = isfinite(rs.r);
 
     uint2* qp = reinterpret_cast<uint2*>(q + row * K);
     if constexpr (VPT > 0) {
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t idx = lt + (int64_t)i * TPR;
-            if (idx < nvec) qp[idx] = make_uint2(codes4(v[i].x, v[i].y, s), codes4(v[i].z, v[i].w, s));
+            if (idx < nvec) qp[idx] = make_uint2(codes4(v[i].x, v[i].y, rs), codes4(v[i].z, v[i].w, rs));
         }
     } else {
         for (int64_t idx = lt; idx < nvec; idx += TPR) {
             const uint4 u = rp[idx];
-            qp[idx] = make_uint2(codes4(u.x, u.y, s), codes4(u.z, u.w, s));
+            qp[idx] = make_uint2(codes4(u.x, u.y, rs), codes4(u.z, u.w, rs));
         }
     }
 }
 
 template <int TPR, int VPT>
 cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
-                       cudaStream_t stream) {
+                       const LaunchEnv& env) {
     constexpr int kRowsPerCta = kQuantThreads / TPR;
     const int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
-    quant_rows_kernel<TPR, VPT><<<dim3((unsigned)blocks), kQuantThreads, 0, stream>>>(src, rows, K, q, s);
-    return cudaGetLastError();
+    // one wave: every CTA resident at once (at least 2 per SM fit, 256 threads each)
+    const int one_wave = blocks <= 2LL * env.sm_count ? 1 : 0;
+    return launch_kernel(quant_rows_kernel<TPR, VPT>, dim3((unsigned)blocks), dim3(kQuantThreads), 0, env.stream, 0,
+                         src, rows, K, q, s, one_wave);
 }
 
 }  // namespace
@@ -140,10 +173,10 @@ cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, 
 cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
                               const LaunchEnv& env) {
     const int64_t nvec = K / 8;
-    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, s, env.stream);
-    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, s, env.stream);
-    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, s, env.stream);
-    return launch_cfg<256, 0>(src, rows, K, q, s, env.stream);
+    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, s, env);
+    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, s, env);
+    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, s, env);
+    return launch_cfg<256, 0>(src, rows, K, q, s, env);
 }
 
 }  // namespace i8ql

@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
     const int nkb = (int)((K + kBK - 1) / kBK);
     const int nchunks = (nkb + kChunkKB - 1) / kChunkKB;
 
+    pdl_wait();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], kConvWarps);
@@ -550,8 +551,7 @@ cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, con
     p.tiles_a = tiles_a;
     p.tmem_cols = pow2_cols(2 * p.bn);
     const int64_t tiles = tiles_a * p.tiles_b;
-    w8a8_kernel<<<dim3((unsigned)tiles), kThreads, kSmemBytes, env.stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(w8a8_kernel, dim3((unsigned)tiles), dim3(kThreads), kSmemBytes, env.stream, 0, p);
 }
 
 }  // namespace i8ql

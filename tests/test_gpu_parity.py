@@ -101,6 +101,22 @@ def test_quant_shapes(rows, k):
     check_quant(_adversarial_rows(rows, k, rows * 11 + k), False)
 
 
+def test_quant_near_ties():
+    """Rows whose quotients w / s land next to half-integers: the rounding of
+    the binary32 quotient must match the oracle code for code, whichever way
+    the kernel computes it."""
+    g = np.random.default_rng(7)
+    rows = []
+    for e in (-3, 0, 6):
+        for m in range(128):
+            a = (1 + m / 128) * 2.0 ** e * 64
+            js = g.integers(0, 127, 15)
+            rows.append([a] + [a * (j + 0.5) / 127 * (1 if j % 2 else -1) for j in js])
+    src = torch.tensor(np.array(rows), dtype=torch.float64).to(torch.bfloat16)
+    for weight in (True, False):
+        check_quant(src, weight)
+
+
 @pytest.mark.parametrize("name", list(synthetic.QWEN3_4B_SHAPES) + ["qwen3_8b_gate_up"])
 def test_quant_full_size_weights(name):
     if name == "qwen3_8b_gate_up":
