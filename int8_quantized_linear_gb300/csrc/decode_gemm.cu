@@ -88,21 +88,28 @@ __device__ __forceinline__ uint4 ldg_cached(const void* p) { return __ldg(reinte
 
 // Four int8 codes -> two bf16x2 words (exact).  Each byte b is biased to
 // u = b + 128, placed in the low mantissa bits of 2^23 (float 2^23 + u),
-// and 2^23 + 128 is subtracted (packed f32x2); the upper halves of the exact
-// fp32 results are the bf16 values.
+// and 2^23 + 128 is subtracted with packed f32x2 adds; the upper halves of
+// the exact fp32 results are the bf16 values.
 __device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t f0 = __byte_perm(u, 0x4b000000u, 0x7440);
-    const uint32_t f1 = __byte_perm(u, 0x4b000000u, 0x7441);
-    const uint32_t f2 = __byte_perm(u, 0x4b000000u, 0x7442);
-    const uint32_t f3 = __byte_perm(u, 0x4b000000u, 0x7443);
-    const uint64_t bias = 0xcb000080cb000080ull;  // (-(2^23 + 128), -(2^23 + 128))
-    uint64_t p01 = ((uint64_t)f1 << 32) | f0;
-    uint64_t p23 = ((uint64_t)f3 << 32) | f2;
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p01) : "l"(bias));
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(p23) : "l"(bias));
-    lo = __byte_perm((uint32_t)p01, (uint32_t)(p01 >> 32), 0x7632);
-    hi = __byte_perm((uint32_t)p23, (uint32_t)(p23 >> 32), 0x7632);
+    asm("{\n\t"
+        ".reg .b32 u, f0, f1, f2, f3;\n\t"
+        ".reg .b64 pa, pb;\n\t"
+        "xor.b32 u, %2, 0x80808080;\n\t"
+        "prmt.b32 f0, u, 0x4b000000, 0x7440;\n\t"
+        "prmt.b32 f1, u, 0x4b000000, 0x7441;\n\t"
+        "prmt.b32 f2, u, 0x4b000000, 0x7442;\n\t"
+        "prmt.b32 f3, u, 0x4b000000, 0x7443;\n\t"
+        "mov.b64 pa, {f0, f1};\n\t"
+        "mov.b64 pb, {f2, f3};\n\t"
+        "add.rn.f32x2 pa, pa, %3;\n\t"
+        "add.rn.f32x2 pb, pb, %3;\n\t"
+        "mov.b64 {f0, f1}, pa;\n\t"
+        "mov.b64 {f2, f3}, pb;\n\t"
+        "prmt.b32 %0, f0, f1, 0x7632;\n\t"
+        "prmt.b32 %1, f2, f3, 0x7632;\n\t"
+        "}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w), "l"(0xcb000080cb000080ull));  // (-(2^23 + 128), -(2^23 + 128))
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -137,7 +144,7 @@ constexpr int kStages = 4;
 
 // MT 16-row m-tiles per warp, NT 8-token n-tiles per pass.
 template <Op OP, int MT, int NT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
+__global__ void __launch_bounds__(kThreads, OP == Op::kW8A16 ? (NT <= 2 ? 3 : 2) : (NT <= 2 ? 4 : (NT <= 4 ? 3 : 2)))
     decode_gemm_kernel(const DecodeParams p) {
     using Acc = std::conditional_t<OP == Op::kW8A8, int32_t, float>;
     constexpr int kRows = 16 * MT;
@@ -175,38 +182,39 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
     }
     if (hi <= lo) return;  // an empty expert reads no weights
 
-    // This warp's k-steps (64 k each) within the cluster's split of K.
+    // This warp's k-steps (64 k each) within the cluster's split of K.  All
+    // k-steps are full except possibly the last of the matrix (K % 64 != 0),
+    // which is handled once, with predicates, after the main loop.
     const int64_t ksteps = (K + 63) / 64;
+    const int64_t full_steps = K / 64;
     const int units = S * kWarps;
     const int unit = rank * kWarps + warp;
     const int64_t ks_begin = ksteps * unit / units;
     const int64_t ks_end = ksteps * (unit + 1) / units;
+    const int64_t main_end = min(ks_end, full_steps);
+    const int main_count = (int)max((int64_t)0, main_end - ks_begin);
+    const bool has_tail = ks_end > full_steps;  // this warp owns the partial k-step
 
-    // Weight row pointers of this lane (rows past N are never loaded).
-    const int8_t* wrow[MT][2];
-    bool wok[MT][2];
+    // Lane base pointers.  Rows past N read row N-1 and tokens past the
+    // chunk read its last token: their products land only in outputs that
+    // are never stored, so the main loop needs no predicates.
+    const int8_t* wbase[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t n = n0 + mt * 16 + g + 8 * h;
-            wok[mt][h] = n < N;
-            wrow[mt][h] = qw + (wok[mt][h] ? n : 0) * K + 16 * t;
-        }
+        for (int h = 0; h < 2; ++h)
+            wbase[mt][h] = qw + min(n0 + mt * 16 + g + 8 * h, N - 1) * K + 16 * t + ks_begin * 64;
 
-    auto load_w = [&](WeightRegs<MT>& w, int64_t ks) {
-        const int64_t k0 = ks * 64;
-        const bool kok = k0 + 16 * t < K;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                w.r[mt][h] = (kok && wok[mt][h]) ? ldg_stream(wrow[mt][h] + k0) : make_uint4(0, 0, 0, 0);
-    };
+    using XT = std::conditional_t<OP == Op::kW8A16, uint16_t, int8_t>;
+    constexpr int kXW = OP == Op::kW8A16 ? 8 : 4;  // 32-bit words of x per lane per k-step
 
     for (int64_t c0 = lo; c0 < hi; c0 += kToks) {
-        const int64_t chunk = min((int64_t)kToks, hi - c0);
-        const int nt_active = (int)((chunk + 7) / 8);
+        const int64_t chunk_hi = min(hi, c0 + (int64_t)kToks);
+        const int nt_active = (int)((chunk_hi - c0 + 7) / 8);
+        const XT* xbase[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            xbase[nt] = static_cast<const XT*>(p.x) + min(c0 + nt * 8 + g, chunk_hi - 1) * K + 16 * t + ks_begin * 64;
 
         Acc acc[MT][NT][4];
 #pragma unroll
@@ -216,29 +224,29 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[mt][nt][i] = Acc(0);
 
-        auto compute = [&](const WeightRegs<MT>& w, int64_t ks) {
-            const int64_t k0 = ks * 64 + 16 * t;
-            const bool kok = k0 < K;
-            if constexpr (OP == Op::kW8A16) {
-                uint32_t xb[NT][8];
+        auto load_x = [&](uint32_t (&xb)[NT][kXW], int i, bool ok) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int64_t m = c0 + nt * 8 + g;
-                    if (nt < nt_active && kok && m < hi) {
-                        const uint16_t* xp = static_cast<const uint16_t*>(p.x) + m * K + k0;
-                        const uint4 v0 = ldg_cached(xp);
+            for (int nt = 0; nt < NT; ++nt) {
+                if (nt < nt_active && ok) {
+                    const XT* xp = xbase[nt] + (int64_t)i * 64;
+                    const uint4 v0 = ldg_cached(xp);
+                    xb[nt][0] = v0.x; xb[nt][1] = v0.y; xb[nt][2] = v0.z; xb[nt][3] = v0.w;
+                    if constexpr (OP == Op::kW8A16) {
                         const uint4 v1 = ldg_cached(xp + 8);
-                        xb[nt][0] = v0.x; xb[nt][1] = v0.y; xb[nt][2] = v0.z; xb[nt][3] = v0.w;
                         xb[nt][4] = v1.x; xb[nt][5] = v1.y; xb[nt][6] = v1.z; xb[nt][7] = v1.w;
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) xb[nt][i] = 0u;
                     }
-                }
+                } else {
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const uint32_t wg[4] = {w.r[mt][0].x, w.r[mt][0].y, w.r[mt][0].z, w.r[mt][0].w};
-                    const uint32_t wh[4] = {w.r[mt][1].x, w.r[mt][1].y, w.r[mt][1].z, w.r[mt][1].w};
+                    for (int q = 0; q < kXW; ++q) xb[nt][q] = 0u;
+                }
+            }
+        };
+        auto mma_step = [&](const WeightRegs<MT>& w, const uint32_t (&xb)[NT][kXW]) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const uint32_t wg[4] = {w.r[mt][0].x, w.r[mt][0].y, w.r[mt][0].z, w.r[mt][0].w};
+                const uint32_t wh[4] = {w.r[mt][1].x, w.r[mt][1].y, w.r[mt][1].z, w.r[mt][1].w};
+                if constexpr (OP == Op::kW8A16) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t a0, a2, a1, a3;
@@ -249,27 +257,10 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
                             if (nt < nt_active)
                                 mma_bf16(acc[mt][nt], a0, a1, a2, a3, xb[nt][2 * j], xb[nt][2 * j + 1]);
                     }
-                }
-            } else {
-                uint32_t xb[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int64_t m = c0 + nt * 8 + g;
-                    if (nt < nt_active && kok && m < hi) {
-                        const uint4 v = ldg_cached(static_cast<const int8_t*>(p.x) + m * K + k0);
-                        xb[nt][0] = v.x; xb[nt][1] = v.y; xb[nt][2] = v.z; xb[nt][3] = v.w;
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) xb[nt][i] = 0u;
-                    }
-                }
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const uint32_t wg[4] = {w.r[mt][0].x, w.r[mt][0].y, w.r[mt][0].z, w.r[mt][0].w};
-                    const uint32_t wh[4] = {w.r[mt][1].x, w.r[mt][1].y, w.r[mt][1].z, w.r[mt][1].w};
+                } else {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        // k 16t+8j+{0..3} -> fragment slot 4t..4t+3, k 16t+8j+{4..7} -> slot 16+4t..
+                        // k 16t+8j+{0..3} -> fragment slot 4t.., k 16t+8j+{4..7} -> slot 16+4t..
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
                             if (nt < nt_active)
@@ -279,21 +270,45 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
                 }
             }
         };
+        auto load_w = [&](WeightRegs<MT>& w, int i) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) w.r[mt][h] = ldg_stream(wbase[mt][h] + (int64_t)i * 64);
+        };
 
         {
+            // main loop: full k-steps through a kStages-deep register ring
             WeightRegs<MT> ring[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s)
-                if (ks_begin + s < ks_end) load_w(ring[s], ks_begin + s);
-            for (int64_t ks = ks_begin; ks < ks_end; ks += kStages) {
+                if (s < main_count) load_w(ring[s], s);
+            for (int i0 = 0; i0 < main_count; i0 += kStages) {
 #pragma unroll
                 for (int s = 0; s < kStages; ++s) {
-                    if (ks + s < ks_end) {
-                        compute(ring[s], ks + s);
-                        if (ks + s + kStages < ks_end) load_w(ring[s], ks + s + kStages);
+                    const int i = i0 + s;
+                    if (i < main_count) {
+                        uint32_t xb[NT][kXW];
+                        load_x(xb, i, true);
+                        mma_step(ring[s], xb);
+                        if (i + kStages < main_count) load_w(ring[s], i + kStages);
                     }
                 }
             }
+        }
+        if (has_tail) {
+            // the partial last k-step of the matrix: lanes past K load zeros
+            const int i = main_count;
+            const bool kok = full_steps * 64 + 16 * t < K;
+            WeightRegs<MT> w;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    w.r[mt][h] = kok ? ldg_stream(wbase[mt][h] + (int64_t)i * 64) : make_uint4(0, 0, 0, 0);
+            uint32_t xb[NT][kXW];
+            load_x(xb, i, kok);
+            mma_step(w, xb);
         }
 
         // Warp partials -> shared memory, laid out [token][row].

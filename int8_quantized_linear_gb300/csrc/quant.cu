@@ -14,7 +14,7 @@
 // IEEE fp32: __fdiv_rn for a / 127; the code of each element is the
 // round-half-even of the IEEE quotient v / s, obtained from a multiply by the
 // correctly rounded reciprocal except near ties, where the division itself
-// is taken (see code()); no flush of subnormals (built without fast math).
+// is taken (see codes8()); no flush of subnormals (built without fast math).
 // HBM traffic: 2 bytes read + 1 byte written per element, plus 4 bytes per row.
 
 #include <cuda_runtime.h>
@@ -49,7 +49,13 @@ __device__ __forceinline__ float absmax8(const uint4& v, float a) {
 // half-integers, so when t is farther than kNearTie = 2^-15 from the nearest
 // half-integer, rint(t) == rint(fl32(v/s)).  Near-ties (and a reciprocal that
 // overflowed, when s is subnormal) take the IEEE division.
+//
+// Rounding: adding 1.5 * 2^23 to |t| < 2^22 leaves round-half-even(t) in the
+// low mantissa bits, so the low byte of the sum's bit pattern is the code in
+// two's complement and subtracting 1.5 * 2^23 back gives it as a float.  The
+// code never leaves [-127, 127] (|v/s| <= 127 * (1 + 2^-23)), so no clamp.
 constexpr float kNearTie = 3.0517578125e-05f;  // 2^-15
+constexpr float kRoundMagic = 12582912.0f;     // 1.5 * 2^23
 
 struct RowScale {
     float s;     // the scale
@@ -57,22 +63,27 @@ struct RowScale {
     bool fast;   // r is finite
 };
 
-__device__ __forceinline__ uint32_t code(float v, const RowScale& rs) {
-    int c;
-    const float t = __fmul_rn(v, rs.r);
-    const float fl = floorf(t);
-    if (rs.fast && fabsf(t - fl - 0.5f) > kNearTie) {
-        c = __float2int_rn(t);
-    } else {
-        c = __float2int_rn(__fdiv_rn(v, rs.s));
+// Codes of 8 values (two words of bf16 pairs) packed into two words.
+__device__ __forceinline__ uint2 codes8(const uint4& v, const RowScale& rs) {
+    float x[8] = {lo_bf16(v.x), hi_bf16(v.x), lo_bf16(v.y), hi_bf16(v.y),
+                  lo_bf16(v.z), hi_bf16(v.z), lo_bf16(v.w), hi_bf16(v.w)};
+    uint32_t b[8];
+    float worst = 0.0f;  // largest |t - round(t)| over the 8 values
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float t = __fmul_rn(x[i], rs.r);
+        const float m = __fadd_rn(t, kRoundMagic);
+        const float c = __fsub_rn(m, kRoundMagic);
+        worst = fmaxf(worst, fabsf(__fsub_rn(t, c)));
+        b[i] = __float_as_uint(m);
     }
-    c = max(-127, min(127, c));
-    return static_cast<uint32_t>(c) & 0xffu;
-}
-
-__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, const RowScale& rs) {
-    return code(lo_bf16(w0), rs) | (code(hi_bf16(w0), rs) << 8) | (code(lo_bf16(w1), rs) << 16) |
-           (code(hi_bf16(w1), rs) << 24);
+    if (!rs.fast || worst > 0.5f - kNearTie) {
+        // rare: some value lies next to a half-integer; take the division
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b[i] = (uint32_t)__float2int_rn(__fdiv_rn(x[i], rs.s));
+    }
+    return make_uint2(__byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410),
+                      __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410));
 }
 
 __device__ __forceinline__ uint4 load_nc(const uint4* p) {
@@ -147,12 +158,12 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t idx = lt + (int64_t)i * TPR;
-            if (idx < nvec) qp[idx] = make_uint2(codes4(v[i].x, v[i].y, rs), codes4(v[i].z, v[i].w, rs));
+            if (idx < nvec) qp[idx] = codes8(v[i], rs);
         }
     } else {
         for (int64_t idx = lt; idx < nvec; idx += TPR) {
             const uint4 u = rp[idx];
-            qp[idx] = make_uint2(codes4(u.x, u.y, rs), codes4(u.z, u.w, rs));
+            qp[idx] = codes8(u, rs);
         }
     }
 }
