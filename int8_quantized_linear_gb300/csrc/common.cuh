@@ -94,6 +94,12 @@ cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, c
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                                int64_t K, const LaunchEnv& env);
+// Bytes of workspace launch_w8a8_ws needs (the fp16 codes of both operands
+// when M exceeds the decode range; 0 otherwise).
+size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                           const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                           uint16_t* ws, const LaunchEnv& env);
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                         const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                         int64_t K, const LaunchEnv& env);

@@ -1,4 +1,4 @@
-// W8A8 GEMM: int8 x int8 -> exact int32 -> scale/bias epilogue -> bf16.
+// W8A8 GEMM for M > 64: int8 x int8 -> exact int32 -> scale/bias epilogue -> bf16.
 //
 // Sources: "feat(quantization): support compressed-tensors W8A8 and mixed
 // modules", Design and Supported Execution Scheme (static symmetric int8
@@ -20,25 +20,30 @@
 //    convert it to int32 (exact) and add it to an int32 running sum kept in
 //    a second TMEM region; the next chunk restarts the fp32 accumulator.
 //
-// Warp roles (544 threads, one CTA per output tile, 1 CTA per SM):
-//  * warps 0-3: epilogue (warp w owns TMEM lanes 32w .. 32w+31);
-//  * warp 4: TMEM allocation and the single-thread MMA issuer;
-//  * warps 5-16: converters.  They stream 16-byte int8 vectors from global
-//    memory (three stages of loads in flight per thread), turn them into
-//    fp16 in registers (bias-and-subtract trick, exact), and store them in
-//    the 128-byte-swizzled K-major layout the MMA reads, through a 4-stage
-//    shared-memory ring guarded by mbarriers.
-// Tile: 128 rows of operand A x BN rows of operand B x 64 k per stage.
-// Large M: A = activations, B = weights, BN = 256.  M <= 128 ("swap AB"):
-// A = weights, B = tokens, BN = M rounded up to 16, so the tensor core does
-// no work on padding rows.
+// Two launches per call:
+//  1. i8_to_f16_kernel turns both code matrices into fp16 codes (exact) in a
+//     workspace, one HBM pass.  Converting once per call instead of once per
+//     output tile cuts the conversion work from M*N*K*3/256 to (M+N)*K
+//     elements, and lets the GEMM stream operands with TMA.
+//  2. w8a8_tc_kernel: one CTA per output tile, 192 threads.  Warp 5 issues
+//     TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle, ragged edges
+//     zero-filled by the tensor map) into a 4-stage ring; warp 4 allocates
+//     TMEM and issues tcgen05.mma.cta_group::1.kind::f16 (M = 128, N = 256;
+//     for M <= 128, "swap AB": weights fill the 128-row operand and tokens
+//     the N side, N = M rounded up to 16); warps 0-3 drain TMEM and write the
+//     epilogue.  Tiles are rasterized in groups of 8 A row-blocks for L2 reuse.
 //
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
 // records I8QL_ERR_TIMEOUT in the sticky fault word, all roles leave their
 // loops, the MMA issuer waits (bounded) for its outstanding MMAs, and the
 // TMEM is freed before the CTA exits.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -46,25 +51,20 @@ namespace i8ql {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;
+constexpr int kBK = 64;  // fp16 per stage row: one 128-byte swizzle atom
 constexpr int kStages = 4;
 constexpr int kMaxBN = 256;
 constexpr int kChunkKB = 16;  // k-blocks per exact fp32 chunk (1024 k)
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
-constexpr int kConvWarps = 12;
-constexpr int kConvThreads = kConvWarps * 32;
-constexpr int kConvDepth = 3;  // stages of int8 loads each converter keeps in flight
-constexpr int kGroupA = 8;     // tile rows of A swept together (L2 reuse of B tiles)
-constexpr int kThreads = (kEpiWarps + 1 + kConvWarps) * 32;
+constexpr int kTmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr int kGroupA = 8;  // tile rows of A swept together (L2 reuse of B tiles)
 constexpr int kAStageBytes = kBM * kBK * 2;
 constexpr int kBStageBytes = kMaxBN * kBK * 2;
-constexpr int kMaxConvItems = (kBM + kMaxBN) * 4 / kConvThreads;  // 16-byte vectors per thread per stage
 constexpr int kSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256 /*barriers*/;
 
 struct W8A8Params {
-    const int8_t* a;  // operand A rows (K contiguous)
-    const int8_t* b;  // operand B rows (K contiguous)
     int64_t rows_a, rows_b, K;
     const float* sx;
     const float* sw;
@@ -206,14 +206,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 // Four int8 codes -> two fp16x2 words (exact): the biased byte u = q + 128
 // becomes the low mantissa byte of fp16 1024 (value 1024 + u); subtracting
 // 1152 leaves q.
@@ -225,18 +217,51 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
     asm("sub.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-__global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
-    static_assert(kMaxConvItems * kConvThreads == (kBM + kMaxBN) * 4, "converter work must divide evenly");
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// int8 codes -> fp16 codes, both matrices in one grid-stride pass (exact).
+__global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ a, int64_t a_vec,
+                                                        const int8_t* __restrict__ b, int64_t b_vec,
+                                                        uint16_t* __restrict__ out_a, uint16_t* __restrict__ out_b) {
+    pdl_wait();
+    const int64_t total = a_vec + b_vec;  // 16-byte vectors of int8
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const bool in_a = i < a_vec;
+        const int64_t j = in_a ? i : i - a_vec;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(in_a ? a : b) + j);
+        uint32_t h[8];
+        i8x4_to_f16(v.x, h[0], h[1]);
+        i8x4_to_f16(v.y, h[2], h[3]);
+        i8x4_to_f16(v.z, h[4], h[5]);
+        i8x4_to_f16(v.w, h[6], h[7]);
+        uint4* o = reinterpret_cast<uint4*>(in_a ? out_a : out_b) + 2 * j;
+        o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const W8A8Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_stages = smem;
@@ -258,11 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
     const int64_t K = p.K;
     const int nkb = (int)((K + kBK - 1) / kBK);
     const int nchunks = (nkb + kChunkKB - 1) / kChunkKB;
+    const uint32_t stage_tx = (uint32_t)(kAStageBytes + bn * kBK * 2);
 
-    pdl_wait();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl->full[s], kConvWarps);
+            mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
         mbar_init(&ctl->acc_full, 1);
@@ -270,6 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
         mbar_init(&ctl->drained, 1);
         ctl->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -281,10 +310,25 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();  // the fp16 codes come from the conversion launch
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t run_col = p.tmem_cols / 2;  // int32 running sum region
 
-    if (warp == kMmaWarp) {
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t a_base = smem_u32(a_stages);
+            const uint32_t b_base = smem_u32(b_stages);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int st = kb % kStages;
+                if (!mbar_wait(&ctl->empty[st], (uint32_t)(((kb / kStages) & 1) ^ 1), ctl, p.err)) break;
+                mbar_expect_tx(&ctl->full[st], stage_tx);
+                tma_load_2d(a_base + st * kAStageBytes, &map_a, kb * kBK, (int32_t)(tile_a * kBM), &ctl->full[st]);
+                tma_load_2d(b_base + st * kBStageBytes, &map_b, kb * kBK, (int32_t)(tile_b * bn), &ctl->full[st]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(bn);
@@ -309,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
             }
             // Wait (bounded) until every MMA issued above has completed.
             mma_commit(&ctl->drained);
-            uint64_t t0 = global_ns();
+            const uint64_t t0 = global_ns();
             while (!mbar_try(smem_u32(&ctl->drained), 0)) {
                 if (global_ns() - t0 > kWaitLimitNs) {
                     record_fault(p.err, kErrBitTimeout);
@@ -319,74 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const W8A8Params p) {
             }
         }
         __syncwarp();
-    } else if (warp > kMmaWarp) {
-        // ------------------------------------------------------------ converters
-        const int ct = threadIdx.x - (kMmaWarp + 1) * 32;
-        const int items = (kBM + bn) * 4;
-        const int64_t a_row0 = tile_a * kBM;
-        const int64_t b_row0 = tile_b * bn;
-        uint4 v[kConvDepth][kMaxConvItems];
-        auto load_stage = [&](uint4 (&dst)[kMaxConvItems], int kb) {
-            const int64_t k0 = (int64_t)kb * kBK;
-#pragma unroll
-            for (int j = 0; j < kMaxConvItems; ++j) {
-                const int item = ct + j * kConvThreads;
-                dst[j] = make_uint4(0, 0, 0, 0);
-                if (item < items) {
-                    const bool is_a = item < kBM * 4;
-                    const int it = is_a ? item : item - kBM * 4;
-                    const int row = it >> 2;
-                    const int c = it & 3;
-                    const int64_t grow = (is_a ? a_row0 : b_row0) + row;
-                    const int64_t k = k0 + 16 * c;
-                    if (grow < (is_a ? p.rows_a : p.rows_b) && k < K)
-                        dst[j] = ldg_stream((is_a ? p.a : p.b) + grow * K + k);
-                }
-            }
-        };
-#pragma unroll
-        for (int d = 0; d < kConvDepth; ++d)
-            if (d < nkb) load_stage(v[d], d);
-        bool alive = true;
-        for (int kb0 = 0; kb0 < nkb && alive; kb0 += kConvDepth) {
-#pragma unroll
-            for (int d = 0; d < kConvDepth; ++d) {
-                const int kb = kb0 + d;
-                if (kb >= nkb || !alive) break;
-                const int st = kb % kStages;
-                if (!warp_wait(&ctl->empty[st], (uint32_t)(((kb / kStages) & 1) ^ 1), ctl, p.err)) {
-                    alive = false;
-                    break;
-                }
-                const uint32_t a_buf = smem_u32(a_stages + st * kAStageBytes);
-                const uint32_t b_buf = smem_u32(b_stages + st * kBStageBytes);
-#pragma unroll
-                for (int j = 0; j < kMaxConvItems; ++j) {
-                    const int item = ct + j * kConvThreads;
-                    if (item < items) {
-                        const bool is_a = item < kBM * 4;
-                        const int it = is_a ? item : item - kBM * 4;
-                        const int row = it >> 2;
-                        const int c = it & 3;
-                        uint32_t h[8];
-                        i8x4_to_f16(v[d][j].x, h[0], h[1]);
-                        i8x4_to_f16(v[d][j].y, h[2], h[3]);
-                        i8x4_to_f16(v[d][j].z, h[4], h[5]);
-                        i8x4_to_f16(v[d][j].w, h[6], h[7]);
-                        const uint32_t row_base = (is_a ? a_buf : b_buf) + (row >> 3) * 1024 + (row & 7) * 128;
-                        const uint32_t c0 = (uint32_t)((2 * c) ^ (row & 7));
-                        const uint32_t c1 = (uint32_t)((2 * c + 1) ^ (row & 7));
-                        st_shared_v4(row_base + c0 * 16, h[0], h[1], h[2], h[3]);
-                        st_shared_v4(row_base + c1 * 16, h[4], h[5], h[6], h[7]);
-                    }
-                }
-                // make the generic-proxy stores visible to the tensor core
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->full[st]);
-                if (kb + kConvDepth < nkb) load_stage(v[d], kb + kConvDepth);
-            }
-        }
     } else {
         // ------------------------------------------------------------ epilogue
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
@@ -502,21 +478,67 @@ uint32_t pow2_cols(int need) {
     return c;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D fp16 tensor map over a row-major [rows, K] matrix, box = 64 k x box_rows
+// rows, 128-byte swizzle (the K-major canonical layout the MMA reads),
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t K, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
-                        const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
-                        const LaunchEnv& env) {
+size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= kW8A8DecodeMaxM) return 0;
+    return (size_t)(M + N) * (size_t)K * 2;
+}
+
+cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                           const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                           uint16_t* ws, const LaunchEnv& env) {
     if (M <= kW8A8DecodeMaxM) return launch_w8a8_decode(qx, sx, qw, sw, bias, y, acc, M, N, K, env);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(w8a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(w8a8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
+    uint16_t* x16 = ws;
+    uint16_t* w16 = ws + M * K;
+    // 1. fp16 codes of both operands
+    {
+        const int64_t vec = (M + N) * K / 16;
+        const int64_t blocks = std::min<int64_t>((vec + 255) / 256, (int64_t)env.sm_count * 8);
+        e = launch_kernel(i8_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, env.stream, 0, qx, M * K / 16, qw,
+                          N * K / 16, x16, w16);
+        if (e != cudaSuccess) return e;
+    }
+    // 2. the tensor-core GEMM
     W8A8Params p{};
     p.K = K;
     p.sx = sx;
@@ -527,31 +549,48 @@ cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, con
     p.M = M;
     p.N = N;
     p.err = env.err;
-    int64_t tiles_a;
+    const uint16_t* a16;
+    const uint16_t* b16;
     if (M <= kBM) {
         // swap AB: weights fill the 128-row MMA operand, tokens the N side
         p.swap = 1;
-        p.a = qw;
+        a16 = w16;
         p.rows_a = N;
-        p.b = qx;
+        b16 = x16;
         p.rows_b = M;
         p.bn = (int)((M + 15) / 16 * 16);
         p.tiles_b = 1;
-        tiles_a = (N + kBM - 1) / kBM;
+        p.tiles_a = (N + kBM - 1) / kBM;
     } else {
         p.swap = 0;
-        p.a = qx;
+        a16 = x16;
         p.rows_a = M;
-        p.b = qw;
+        b16 = w16;
         p.rows_b = N;
         p.bn = kMaxBN;
         p.tiles_b = (N + kMaxBN - 1) / kMaxBN;
-        tiles_a = (M + kBM - 1) / kBM;
+        p.tiles_a = (M + kBM - 1) / kBM;
     }
-    p.tiles_a = tiles_a;
     p.tmem_cols = pow2_cols(2 * p.bn);
-    const int64_t tiles = tiles_a * p.tiles_b;
-    return launch_kernel(w8a8_kernel, dim3((unsigned)tiles), dim3(kThreads), kSmemBytes, env.stream, 0, p);
+    CUtensorMap map_a, map_b;
+    if (!make_map(&map_a, a16, p.rows_a, K, kBM) || !make_map(&map_b, b16, p.rows_b, K, p.bn))
+        return cudaErrorInvalidValue;
+    const int64_t tiles = p.tiles_a * p.tiles_b;
+    return launch_kernel(w8a8_tc_kernel, dim3((unsigned)tiles), dim3(kThreads), kSmemBytes, env.stream, 0, map_a,
+                         map_b, p);
+}
+
+cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, const uint16_t* bias,
+                        uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K, const LaunchEnv& env) {
+    if (M <= kW8A8DecodeMaxM) return launch_w8a8_decode(qx, sx, qw, sw, bias, y, acc, M, N, K, env);
+    // Stream-ordered workspace for the fp16 codes (from the device's default
+    // memory pool, returned when the stream reaches the free).
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, w8a8_workspace_bytes(M, N, K), env.stream);
+    if (e != cudaSuccess) return e;
+    e = launch_w8a8_ws(qx, sx, qw, sw, bias, y, acc, M, N, K, static_cast<uint16_t*>(ws), env);
+    const cudaError_t f = cudaFreeAsync(ws, env.stream);
+    return e != cudaSuccess ? e : f;
 }
 
 }  // namespace i8ql
