@@ -44,7 +44,8 @@ enum {
     I8QL_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed          */
     I8QL_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (sticky word)        */
     I8QL_ERR_BAD_OFFSETS = 5,  /* grouped offsets not 0 .. T_total, non-decreasing     */
-    I8QL_ERR_NO_DEVICE = 6     /* no CUDA device, or not an sm_103 device              */
+    I8QL_ERR_NO_DEVICE = 6,    /* no CUDA device, or not an sm_103 device              */
+    I8QL_ERR_WORKSPACE_LIMIT = 7 /* w8a8_gemm_noalloc: problem exceeds its fixed array  */
 };
 
 /* Largest K whose worst-case int8 dot product fits int32:
@@ -140,6 +141,36 @@ i8ql_status w8a16_gemm(const i8ql_bf16* x, const int8_t* qw, const float* sw, i8
 i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64_t E,
                                const int8_t* qw, const float* sw, i8ql_bf16* y,
                                int64_t T_total, int64_t N, int64_t K, void* stream);
+
+/*
+ * W8A8 GEMM that allocates nothing.
+ *
+ * No counterpart on the pages: this entry point exists for callers that
+ * cannot allocate device memory while they run (code replayed from a CUDA
+ * graph whose memory was fixed at capture, serving loops that forbid
+ * allocator calls on the hot path, hosts that own every buffer).  It computes
+ * exactly what w8a8_gemm computes, with the same arguments, layouts and
+ * errors, but where w8a8_gemm takes a temporary workspace from the
+ * stream-ordered allocator (for M > 64: the fp16 codes of both operands,
+ * 2 * (M + N) * K bytes), this one uses a fixed array compiled into the
+ * library: I8QL_NOALLOC_MAX_ELEMENTS 16-bit elements (32 MiB), held by every
+ * GPU that loads the library until the process exits.
+ *
+ *  - For M > 64, (M + N) * K must not exceed I8QL_NOALLOC_MAX_ELEMENTS, else
+ *    the call returns I8QL_ERR_WORKSPACE_LIMIT and launches nothing.  For
+ *    M <= 64 the computation needs no workspace and any size is accepted.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the array and it keeps the last call's contents (every
+ *    byte a call reads is written by the same call first).  Calls whose work
+ *    may overlap on the GPU, e.g. on two streams without ordering, race on
+ *    the array: order them on one stream or serialise them.
+ */
+#define I8QL_NOALLOC_MAX_ELEMENTS (16 * 1024 * 1024)
+i8ql_status w8a8_gemm_noalloc(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
+                              const i8ql_bf16* bias, i8ql_bf16* y, int32_t* acc_debug,
+                              int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
  * Waits for `stream`, then reads and clears the current device's sticky

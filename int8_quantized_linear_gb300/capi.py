@@ -25,7 +25,9 @@ I8QL_ERR_CUDA = 3
 I8QL_ERR_TIMEOUT = 4
 I8QL_ERR_BAD_OFFSETS = 5
 I8QL_ERR_NO_DEVICE = 6
+I8QL_ERR_WORKSPACE_LIMIT = 7
 I8QL_MAX_K = 133144
+I8QL_NOALLOC_MAX_ELEMENTS = 16 * 1024 * 1024
 
 # Every symbol the C header declares, with its ctypes signature.
 _P, _I64, _S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
@@ -33,6 +35,7 @@ SIGNATURES = {
     "quantize_weight_per_channel_int8": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "quantize_act_per_token_int8": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "w8a8_gemm": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w8a8_gemm_noalloc": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w8a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "grouped_w8a16_gemm": (_S, [_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P]),
     "i8ql_get_device_error": (_S, [_P]),
@@ -144,6 +147,32 @@ def w8a8_gemm(qx, sx, qw, sw, bias=None, y=None, acc_debug=None, stream=None):
     st = lib().w8a8_gemm(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y),
                          _ptr(acc_debug), m, n, k, _stream(stream))
     _check(st, "w8a8_gemm")
+    return y
+
+
+def w8a8_gemm_noalloc(qx, sx, qw, sw, y, bias=None, acc_debug=None, stream=None):
+    """w8a8_gemm through the entry point that allocates no device memory.
+
+    For callers that cannot allocate while they run (graph replay with fixed
+    memory, allocator-free serving loops): the output ``y`` must be passed in,
+    and the large-M workspace comes from a fixed array inside the library, so
+    ``(M + N) * K`` may not exceed ``I8QL_NOALLOC_MAX_ELEMENTS`` when M > 64.
+    Calls that could overlap on the GPU must not be issued (they share it).
+    """
+    m, k = qx.shape
+    n = qw.shape[0]
+    _need(qx, torch.int8, (m, k), "qx")
+    _need(sx, torch.float32, (m,), "sx")
+    _need(qw, torch.int8, (n, k), "qw")
+    _need(sw, torch.float32, (n,), "sw")
+    _need(y, torch.bfloat16, (m, n), "y")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (n,), "bias")
+    if acc_debug is not None:
+        _need(acc_debug, torch.int32, (m, n), "acc_debug")
+    st = lib().w8a8_gemm_noalloc(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y),
+                                 _ptr(acc_debug), m, n, k, _stream(stream))
+    _check(st, "w8a8_gemm_noalloc")
     return y
 
 

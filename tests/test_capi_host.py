@@ -28,6 +28,7 @@ def lib():
 def _declared_functions() -> list[str]:
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = "\n".join(line for line in text.splitlines() if not line.lstrip().startswith("#"))
     names = re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", text)
     return sorted({n for n in names if n not in {"if", "defined"}})
 
@@ -48,8 +49,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    for s in range(0, 7):
-        assert capi.status_string(s)
+    for s in range(0, 8):
+        assert capi.status_string(s) != "unknown status"
     assert capi.status_string(99) == "unknown status"
     assert capi.i8ql_version() >= 10000
 
@@ -117,6 +118,20 @@ def test_grouped_argument_errors(lib):
     assert f(*a) == capi.I8QL_ERR_UNSUPPORTED
     a = list(ok); a[6] = 0
     assert f(*a) == capi.I8QL_OK
+
+
+def test_w8a8_noalloc_argument_errors(lib):
+    f = lib.w8a8_gemm_noalloc
+    ok = (A, B, C, D, None, A, None, 8, 16, 64, None)
+    args = list(ok); args[9] = 40
+    assert f(*args) == capi.I8QL_ERR_UNSUPPORTED
+    args = list(ok); args[2] = None
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG
+    args = list(ok); args[7] = 0
+    assert f(*args) == capi.I8QL_OK
+    # beyond the fixed array on the large-M path: refused before any CUDA call
+    big = list(ok); big[7] = 128; big[8] = capi.I8QL_NOALLOC_MAX_ELEMENTS // 4096; big[9] = 4096
+    assert f(*big) == capi.I8QL_ERR_WORKSPACE_LIMIT
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
