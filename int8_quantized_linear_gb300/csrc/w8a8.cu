@@ -17,21 +17,25 @@
 //    magnitude is below 2^24, which holds for any 1024-deep chunk of k
 //    (1024 * 127^2 = 16,516,096 < 16,777,216);
 //  * after each chunk the epilogue warps drain the fp32 chunk sum from TMEM,
-//    convert it to int32 (exact) and add it to an int32 running sum kept in
-//    a second TMEM region; the next chunk restarts the fp32 accumulator.
+//    convert it to int32 (exact) and add it to int32 running sums held in
+//    their registers; chunks alternate between two TMEM buffers, so the next
+//    chunk accumulates while the previous one drains.
 //
 // Two launches per call:
 //  1. i8_to_f16_kernel turns both code matrices into fp16 codes (exact) in a
 //     workspace, one HBM pass.  Converting once per call instead of once per
 //     output tile cuts the conversion work from M*N*K*3/256 to (M+N)*K
 //     elements, and lets the GEMM stream operands with TMA.
-//  2. w8a8_tc_kernel: one CTA per output tile, 192 threads.  Warp 5 issues
-//     TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle, ragged edges
-//     zero-filled by the tensor map) into a 4-stage ring; warp 4 allocates
-//     TMEM and issues tcgen05.mma.cta_group::1.kind::f16 (M = 128, N = 256;
-//     for M <= 128, "swap AB": weights fill the 128-row operand and tokens
-//     the N side, N = M rounded up to 16); warps 0-3 drain TMEM and write the
-//     epilogue.  Tiles are rasterized in groups of 8 A row-blocks for L2 reuse.
+//  2. w8a8_tc_kernel: persistent, one CTA per SM, 320 threads.  Warp 9
+//     issues TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle, ragged
+//     edges zero-filled by the tensor map) into a 4-stage ring, running ahead
+//     across tiles; warp 8 allocates TMEM and issues
+//     tcgen05.mma.cta_group::1.kind::f16 (M = 128, N = 256; for M <= 128,
+//     "swap AB": weights fill the 128-row operand and tokens the N side,
+//     padded to 128); warps 0-7 drain the chunk buffers into register
+//     running sums and write the epilogue of a tile while the MMA works on
+//     the next.  Tiles are rasterized in groups of 8 A row-blocks for L2
+//     reuse.
 //
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
 // records I8QL_ERR_TIMEOUT in the sticky fault word, all roles leave their
@@ -55,10 +59,10 @@ constexpr int kBK = 64;  // fp16 per stage row: one 128-byte swizzle atom
 constexpr int kStages = 4;
 constexpr int kMaxBN = 256;
 constexpr int kChunkKB = 16;  // k-blocks per exact fp32 chunk (1024 k)
-constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kTmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each owning half of the columns
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr int kThreads = 10 * 32;  // 320 threads; SMSPs 0 and 1 host three warps: <= 168 registers
 constexpr int kGroupA = 8;  // tile rows of A swept together (L2 reuse of B tiles)
 constexpr int kAStageBytes = kBM * kBK * 2;
 constexpr int kBStageBytes = kMaxBN * kBK * 2;
@@ -83,8 +87,8 @@ struct W8A8Params {
 struct SmemCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    uint64_t acc_full;
-    uint64_t acc_empty;
+    uint64_t acc_full[2];   // fp32 chunk accumulator buffers in TMEM
+    uint64_t acc_empty[2];
     uint64_t drained;
     uint32_t tmem_base;
     int abort_flag;
@@ -186,25 +190,13 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Four int8 codes -> two fp16x2 words (exact): the biased byte u = q + 128
 // becomes the low mantissa byte of fp16 1024 (value 1024 + u); subtracting
@@ -259,9 +251,17 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict
     }
 }
 
+// Persistent: CTA b handles tiles b, b + grid, ...  The fp32 chunk sums
+// alternate between two TMEM buffers, and the exact int32 running sums live
+// in the registers of the 8 epilogue warps (warp w owns TMEM lane quarter
+// w % 4 and column half w / 4), so the MMA never waits for a drain and the
+// epilogue of one tile overlaps the main loop of the next.
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const W8A8Params p) {
+    constexpr int kHalf = BN / 2;     // columns per epilogue warp
+    constexpr int kGroups = kHalf / 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_stages = smem;
@@ -270,28 +270,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Grouped raster: consecutive CTAs sweep kGroupA tile rows of A for each
-    // tile column of B, so a wave shares a few A row blocks and B tiles in L2.
-    const int64_t tile = blockIdx.x;
-    const int64_t group_tiles = (int64_t)kGroupA * p.tiles_b;
-    const int64_t first_a = (tile / group_tiles) * kGroupA;
-    const int64_t rows_in_group = min((int64_t)kGroupA, p.tiles_a - first_a);
-    const int64_t local = tile % group_tiles;
-    const int64_t tile_a = first_a + local % rows_in_group;
-    const int64_t tile_b = local / rows_in_group;
-    const int bn = p.bn;
     const int64_t K = p.K;
     const int nkb = (int)((K + kBK - 1) / kBK);
     const int nchunks = (nkb + kChunkKB - 1) / kChunkKB;
-    const uint32_t stage_tx = (uint32_t)(kAStageBytes + bn * kBK * 2);
+    const int64_t tiles = p.tiles_a * p.tiles_b;
+    const uint32_t stage_tx = (uint32_t)(kAStageBytes + BN * kBK * 2);
+
+    // Grouped raster: consecutive tiles sweep kGroupA tile rows of A for each
+    // tile column of B, so CTAs running together share A row blocks and B
+    // tiles in L2.
+    auto coords = [&](int64_t tile, int64_t& ta, int64_t& tb) {
+        const int64_t group_tiles = (int64_t)kGroupA * p.tiles_b;
+        const int64_t first_a = (tile / group_tiles) * kGroupA;
+        const int64_t rows_in_group = min((int64_t)kGroupA, p.tiles_a - first_a);
+        const int64_t local = tile % group_tiles;
+        ta = first_a + local % rows_in_group;
+        tb = local / rows_in_group;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
-        mbar_init(&ctl->acc_full, 1);
-        mbar_init(&ctl->acc_empty, kEpiWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->acc_full[b], 1);
+            mbar_init(&ctl->acc_empty[b], kEpiWarps);
+        }
         mbar_init(&ctl->drained, 1);
         ctl->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -312,44 +317,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     pdl_wait();  // the fp16 codes come from the conversion launch
     const uint32_t tmem = ctl->tmem_base;
-    const uint32_t run_col = p.tmem_cols / 2;  // int32 running sum region
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint32_t a_base = smem_u32(a_stages);
             const uint32_t b_base = smem_u32(b_stages);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb % kStages;
-                if (!mbar_wait(&ctl->empty[st], (uint32_t)(((kb / kStages) & 1) ^ 1), ctl, p.err)) break;
-                mbar_expect_tx(&ctl->full[st], stage_tx);
-                tma_load_2d(a_base + st * kAStageBytes, &map_a, kb * kBK, (int32_t)(tile_a * kBM), &ctl->full[st]);
-                tma_load_2d(b_base + st * kBStageBytes, &map_b, kb * kBK, (int32_t)(tile_b * bn), &ctl->full[st]);
+            int64_t kg = 0;  // k-blocks issued by this CTA
+            bool alive = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && alive; tile += gridDim.x) {
+                int64_t ta, tb;
+                coords(tile, ta, tb);
+                for (int kb = 0; kb < nkb; ++kb, ++kg) {
+                    const int st = (int)(kg % kStages);
+                    if (!mbar_wait(&ctl->empty[st], (uint32_t)(((kg / kStages) & 1) ^ 1), ctl, p.err)) {
+                        alive = false;
+                        break;
+                    }
+                    mbar_expect_tx(&ctl->full[st], stage_tx);
+                    tma_load_2d(a_base + st * kAStageBytes, &map_a, kb * kBK, (int32_t)(ta * kBM), &ctl->full[st]);
+                    tma_load_2d(b_base + st * kBStageBytes, &map_b, kb * kBK, (int32_t)(tb * BN), &ctl->full[st]);
+                }
             }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = f16_idesc(bn);
+            const uint32_t idesc = f16_idesc(BN);
             const uint32_t a_base = smem_u32(a_stages);
             const uint32_t b_base = smem_u32(b_stages);
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb % kStages;
-                if (kb > 0 && kb % kChunkKB == 0) {
-                    // the epilogue must have drained the previous chunk
-                    if (!mbar_wait(&ctl->acc_empty, (uint32_t)((kb / kChunkKB - 1) & 1), ctl, p.err)) break;
-                }
-                if (!mbar_wait(&ctl->full[st], (uint32_t)((kb / kStages) & 1), ctl, p.err)) break;
-                tc_fence_after();
+            int64_t kg = 0;  // k-blocks consumed
+            int64_t cg = 0;  // chunks accumulated
+            bool alive = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && alive; tile += gridDim.x) {
+                for (int c = 0; c < nchunks && alive; ++c, ++cg) {
+                    const int b = (int)(cg & 1);
+                    // the epilogue must have drained this buffer's previous chunk
+                    if (!mbar_wait(&ctl->acc_empty[b], (uint32_t)(((cg >> 1) & 1) ^ 1), ctl, p.err)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(b * BN);
+                    const int kb_end = min(nkb, (c + 1) * kChunkKB);
+                    for (int kb = c * kChunkKB; kb < kb_end; ++kb, ++kg) {
+                        const int st = (int)(kg % kStages);
+                        if (!mbar_wait(&ctl->full[st], (uint32_t)((kg / kStages) & 1), ctl, p.err)) {
+                            alive = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t ad = sw128_desc(a_base + st * kAStageBytes + kk * 32);
-                    const uint64_t bd = sw128_desc(b_base + st * kBStageBytes + kk * 32);
-                    mma_f16(tmem, ad, bd, idesc, (kb % kChunkKB != 0 || kk != 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint64_t ad = sw128_desc(a_base + st * kAStageBytes + kk * 32);
+                            const uint64_t bd = sw128_desc(b_base + st * kBStageBytes + kk * 32);
+                            mma_f16(d, ad, bd, idesc, (kb != c * kChunkKB || kk != 0) ? 1u : 0u);
+                        }
+                        mma_commit(&ctl->empty[st]);
+                    }
+                    if (alive) mma_commit(&ctl->acc_full[b]);
                 }
-                mma_commit(&ctl->empty[st]);
-                if (kb % kChunkKB == kChunkKB - 1 || kb == nkb - 1) mma_commit(&ctl->acc_full);
             }
             // Wait (bounded) until every MMA issued above has completed.
             mma_commit(&ctl->drained);
@@ -365,100 +393,109 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        const int64_t arow = tile_a * kBM + warp * 32 + lane;
-        const int ngrp = bn / 16;
-        for (int c = 0; c < nchunks; ++c) {
-            if (!warp_wait(&ctl->acc_full, (uint32_t)(c & 1), ctl, p.err)) break;
-            tc_fence_after();
-            const bool last = c == nchunks - 1;
-            for (int grp = 0; grp < ngrp; ++grp) {
-                __syncwarp();
-                uint32_t r[16];
-                tmem_ld16(lane_base + grp * 16, r);
-                tmem_wait_ld();
-                int32_t v[16];
+        const int quarter = warp & 3;
+        const int half = warp >> 2;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        int32_t run[kHalf];
+        int64_t cg = 0;
+        bool alive = true;
+        for (int64_t tile = blockIdx.x; tile < tiles && alive; tile += gridDim.x) {
+            int64_t ta, tb;
+            coords(tile, ta, tb);
+            for (int c = 0; c < nchunks; ++c, ++cg) {
+                const int b = (int)(cg & 1);
+                if (!warp_wait(&ctl->acc_full[b], (uint32_t)((cg >> 1) & 1), ctl, p.err)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col0 = (uint32_t)(b * BN + half * kHalf);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = __float2int_rn(__uint_as_float(r[j]));
-                if (c > 0) {
-                    uint32_t s[16];
-                    tmem_ld16(lane_base + run_col + grp * 16, s);
+                for (int grp = 0; grp < 2 * kGroups; ++grp) {
+                    uint32_t r[8];
+                    tmem_ld8(lane_base + col0 + grp * 8, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] += (int32_t)s[j];
+                    for (int j = 0; j < 8; ++j) {
+                        const int32_t v = __float2int_rn(__uint_as_float(r[j]));  // exact: |v| < 2^24
+                        run[grp * 8 + j] = (c == 0) ? v : run[grp * 8 + j] + v;
+                    }
                 }
-                if (!last) {
-                    uint32_t s[16];
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->acc_empty[b]);  // the MMA may refill this buffer
+            }
+            if (!alive) break;
+            // Scale/bias epilogue and stores from the registers, while the MMA
+            // already runs the next tile.
+            const int64_t arow = ta * kBM + quarter * 32 + lane;
+            const int64_t bcol = tb * BN + half * kHalf;
+            if (!p.swap) {
+                const int64_t m = arow;
+                if (m < p.M) {
+                    const float sxm = p.sx[m];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) s[j] = (uint32_t)v[j];
-                    tmem_st16(lane_base + run_col + grp * 16, s);
-                    continue;
-                }
-                // Final chunk: scale/bias epilogue and stores.
-                const int64_t bcol0 = tile_b * bn + grp * 16;
-                if (!p.swap) {
-                    const int64_t m = arow;
-                    if (m < p.M) {
-                        const float sxm = p.sx[m];
-                        if (bcol0 + 16 <= p.N && (p.N & 7) == 0) {
-                            // whole group in range and 16-byte aligned: vector stores
-                            uint32_t packed[8];
+                    for (int grp = 0; grp < kGroups; ++grp) {
+                        const int64_t n0 = bcol + grp * 16;
+                        if (n0 + 16 <= p.N && (p.N & 7) == 0) {
 #pragma unroll
-                            for (int j = 0; j < 16; j += 2) {
-                                float f0 = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), sxm), __ldg(p.sw + bcol0 + j));
-                                float f1 =
-                                    __fmul_rn(__fmul_rn(__int2float_rn(v[j + 1]), sxm), __ldg(p.sw + bcol0 + j + 1));
-                                if (p.bias) {
-                                    f0 = __fadd_rn(f0, bf16_to_f32(__ldg(p.bias + bcol0 + j)));
-                                    f1 = __fadd_rn(f1, bf16_to_f32(__ldg(p.bias + bcol0 + j + 1)));
+                            for (int h8 = 0; h8 < 2; ++h8) {
+                                uint32_t packed[4];
+#pragma unroll
+                                for (int j = 0; j < 8; j += 2) {
+                                    const int64_t n = n0 + h8 * 8 + j;
+                                    const int i = grp * 16 + h8 * 8 + j;
+                                    float f0 = __fmul_rn(__fmul_rn(__int2float_rn(run[i]), sxm), __ldg(p.sw + n));
+                                    float f1 = __fmul_rn(__fmul_rn(__int2float_rn(run[i + 1]), sxm), __ldg(p.sw + n + 1));
+                                    if (p.bias) {
+                                        f0 = __fadd_rn(f0, bf16_to_f32(__ldg(p.bias + n)));
+                                        f1 = __fadd_rn(f1, bf16_to_f32(__ldg(p.bias + n + 1)));
+                                    }
+                                    packed[j / 2] = (uint32_t)f32_to_bf16_rn(f0) | ((uint32_t)f32_to_bf16_rn(f1) << 16);
                                 }
-                                packed[j / 2] = (uint32_t)f32_to_bf16_rn(f0) | ((uint32_t)f32_to_bf16_rn(f1) << 16);
+                                *reinterpret_cast<uint4*>(p.y + m * p.N + n0 + h8 * 8) =
+                                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
                             }
-                            uint4* yp = reinterpret_cast<uint4*>(p.y + m * p.N + bcol0);
-                            yp[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                            yp[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                             if (p.acc) {
-                                int4* ap = reinterpret_cast<int4*>(p.acc + m * p.N + bcol0);
+                                int4* ap = reinterpret_cast<int4*>(p.acc + m * p.N + n0);
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
-                                    ap[q] = make_int4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                                    ap[q] = make_int4(run[grp * 16 + 4 * q], run[grp * 16 + 4 * q + 1],
+                                                      run[grp * 16 + 4 * q + 2], run[grp * 16 + 4 * q + 3]);
                             }
                         } else {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
-                                const int64_t n = bcol0 + j;
+                                const int64_t n = n0 + j;
                                 if (n < p.N) {
-                                    float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), sxm), __ldg(p.sw + n));
+                                    float f = __fmul_rn(__fmul_rn(__int2float_rn(run[grp * 16 + j]), sxm), __ldg(p.sw + n));
                                     if (p.bias) f = __fadd_rn(f, bf16_to_f32(__ldg(p.bias + n)));
                                     p.y[m * p.N + n] = f32_to_bf16_rn(f);
-                                    if (p.acc) p.acc[m * p.N + n] = v[j];
+                                    if (p.acc) p.acc[m * p.N + n] = run[grp * 16 + j];
                                 }
                             }
                         }
                     }
-                } else {
-                    const int64_t n = arow;
-                    if (n < p.N) {
-                        const float swn = p.sw[n];
-                        const float bn_f = p.bias ? bf16_to_f32(p.bias[n]) : 0.0f;
+                }
+            } else {
+                const int64_t n = arow;
+                if (n < p.N) {
+                    const float swn = p.sw[n];
+                    const float bias_n = p.bias ? bf16_to_f32(p.bias[n]) : 0.0f;
+#pragma unroll
+                    for (int grp = 0; grp < kGroups; ++grp) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const int64_t m = bcol0 + j;
+                            const int64_t m = bcol + grp * 16 + j;
                             if (m < p.M) {
-                                float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), __ldg(p.sx + m)), swn);
-                                if (p.bias) f = __fadd_rn(f, bn_f);
+                                float f = __fmul_rn(__fmul_rn(__int2float_rn(run[grp * 16 + j]), __ldg(p.sx + m)), swn);
+                                if (p.bias) f = __fadd_rn(f, bias_n);
                                 p.y[m * p.N + n] = f32_to_bf16_rn(f);
-                                if (p.acc) p.acc[m * p.N + n] = v[j];
+                                if (p.acc) p.acc[m * p.N + n] = run[grp * 16 + j];
                             }
                         }
                     }
                 }
-            }
-            if (!last) {
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->acc_empty);
             }
         }
     }
@@ -524,7 +561,9 @@ cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(w8a8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(w8a8_tc_kernel<kMaxBN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(w8a8_tc_kernel<kBM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -553,12 +592,13 @@ cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, 
     const uint16_t* b16;
     if (M <= kBM) {
         // swap AB: weights fill the 128-row MMA operand, tokens the N side
+        // (padded to 128 columns; the tensor map reads zeros past M)
         p.swap = 1;
         a16 = w16;
         p.rows_a = N;
         b16 = x16;
         p.rows_b = M;
-        p.bn = (int)((M + 15) / 16 * 16);
+        p.bn = kBM;
         p.tiles_b = 1;
         p.tiles_a = (N + kBM - 1) / kBM;
     } else {
@@ -571,13 +611,17 @@ cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, 
         p.tiles_b = (N + kMaxBN - 1) / kMaxBN;
         p.tiles_a = (M + kBM - 1) / kBM;
     }
-    p.tmem_cols = pow2_cols(2 * p.bn);
+    p.tmem_cols = pow2_cols(2 * p.bn);  // two fp32 chunk buffers
     CUtensorMap map_a, map_b;
     if (!make_map(&map_a, a16, p.rows_a, K, kBM) || !make_map(&map_b, b16, p.rows_b, K, p.bn))
         return cudaErrorInvalidValue;
     const int64_t tiles = p.tiles_a * p.tiles_b;
-    return launch_kernel(w8a8_tc_kernel, dim3((unsigned)tiles), dim3(kThreads), kSmemBytes, env.stream, 0, map_a,
-                         map_b, p);
+    const int64_t grid = std::min<int64_t>(tiles, env.sm_count);  // persistent: one CTA per SM
+    if (p.swap)
+        return launch_kernel(w8a8_tc_kernel<kBM>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, env.stream, 0,
+                             map_a, map_b, p);
+    return launch_kernel(w8a8_tc_kernel<kMaxBN>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, env.stream, 0,
+                         map_a, map_b, p);
 }
 
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, const uint16_t* bias,
