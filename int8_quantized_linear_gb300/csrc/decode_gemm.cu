@@ -139,18 +139,46 @@ struct WeightRegs {
 };
 
 // Depth of the per-lane register ring of weight loads: while one k-step is
-// converted and multiplied, the next kStages - 1 are in flight.
-constexpr int kStages = 4;
+// converted and multiplied, the next stages - 1 are in flight (measured best:
+// 3 for W8A16, whose conversion needs more registers, 4 for W8A8).
+template <Op OP>
+struct RingStages {
+    static constexpr int value = OP == Op::kW8A16 ? 3 : 4;
+};
+
+// Warms L2 with `bytes` bytes at p (multiple of 16, 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // MT 16-row m-tiles per warp, NT 8-token n-tiles per pass.
 template <Op OP, int MT, int NT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, OP == Op::kW8A16 ? (NT <= 2 ? 3 : 2) : (NT <= 2 ? 4 : (NT <= 4 ? 3 : 2)))
+__global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
     decode_gemm_kernel(const DecodeParams p) {
     using Acc = std::conditional_t<OP == Op::kW8A8, int32_t, float>;
     constexpr int kRows = 16 * MT;
     constexpr int kToks = 8 * NT;
+    constexpr int kStages = RingStages<OP>::value;
     __shared__ Acc part[kWarps][kToks * kRows];
 
+    // Before waiting for the previous kernel, start streaming this CTA's
+    // weight rows into L2, so the DRAM ramp overlaps that kernel's tail.  This
+    // is safe even if the previous kernel writes these weights: L2 is the
+    // point of coherence (a line it writes later is updated in L2), and the
+    // loads after pdl_wait() read through it.
+    {
+        const int64_t rows_n = p.N;
+        const int64_t r0 = (int64_t)blockIdx.x * kRows;
+        const int8_t* qw0 = p.qw + (GROUPED ? (int64_t)blockIdx.z * rows_n * p.K : 0);
+        const int64_t ksteps = (p.K + 63) / 64;
+        const int S0 = (int)gridDim.y;
+        const int64_t kb0 = ksteps * (int64_t)blockIdx.y / S0, kb1 = ksteps * ((int64_t)blockIdx.y + 1) / S0;
+        const int64_t k_lo = kb0 * 64, k_hi = min(kb1 * 64, p.K);
+        const int r = (int)threadIdx.x;
+        // (not for the grouped kernel: its multi-wave grid measured slower with it)
+        if (!GROUPED && r < kRows && r0 + r < rows_n && k_hi > k_lo)
+            prefetch_l2(qw0 + (r0 + r) * p.K + k_lo, (uint32_t)(k_hi - k_lo));
+    }
     pdl_wait();
     if (p.one_wave) pdl_launch_dependents();
     cg::cluster_group cluster = cg::this_cluster();
