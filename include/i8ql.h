@@ -151,12 +151,12 @@ i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64
  * allocator calls on the hot path, hosts that own every buffer).  It computes
  * exactly what w8a8_gemm computes, with the same arguments, layouts and
  * errors, but where w8a8_gemm takes a temporary workspace from the
- * stream-ordered allocator (for M > 64: the fp16 codes of both operands,
- * 2 * (M + N) * K bytes), this one uses a fixed array compiled into the
+ * stream-ordered allocator (for M > 64: the fp16 codes of the tokens,
+ * 2 * M * K bytes), this one uses a fixed array compiled into the
  * library: I8QL_NOALLOC_MAX_ELEMENTS 16-bit elements (32 MiB), held by every
  * GPU that loads the library until the process exits.
  *
- *  - For M > 64, (M + N) * K must not exceed I8QL_NOALLOC_MAX_ELEMENTS, else
+ *  - For M > 64, M * K must not exceed I8QL_NOALLOC_MAX_ELEMENTS, else
  *    the call returns I8QL_ERR_WORKSPACE_LIMIT and launches nothing.  For
  *    M <= 64 the computation needs no workspace and any size is accepted.
  *  - The first call on a device looks up the array's device address (once
@@ -171,6 +171,20 @@ i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64
 i8ql_status w8a8_gemm_noalloc(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                               const i8ql_bf16* bias, i8ql_bf16* y, int32_t* acc_debug,
                               int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Reports how w8a8_gemm would run a problem of this size on the current
+ * device, without launching anything.
+ *
+ * No counterpart on the pages: a query for tests and profiling.  For
+ * M <= 64 (the decode kernel) both outputs are 0.  Otherwise *tile_n is the
+ * width (N side) of the 128-row output tiles of the tensor-core kernel (128,
+ * 160, 192, 224 or 256; for M <= 128 the operands are swapped and the tokens
+ * fill a 128-wide side) and *split_k the number of CTAs of a thread-block
+ * cluster that share one tile's k range (1: persistent, no split).
+ * Same argument rules as w8a8_gemm; tile_n and split_k are HOST pointers.
+ */
+i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k);
 
 /*
  * Waits for `stream`, then reads and clears the current device's sticky

@@ -45,10 +45,10 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // cudaLaunchKernelEx with programmatic stream serialization and, when
-// cluster_y > 0, a (1, cluster_y, 1) thread-block cluster.
+// cluster.x > 0, thread-block clusters of the given shape.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                          unsigned cluster_y, Args&&... args) {
+                          dim3 cluster, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -59,17 +59,20 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
-    if (cluster_y > 0) {
+    if (cluster.x > 0) {
         attrs[n].id = cudaLaunchAttributeClusterDimension;
-        attrs[n].val.clusterDim.x = 1;
-        attrs[n].val.clusterDim.y = cluster_y;
-        attrs[n].val.clusterDim.z = 1;
+        attrs[n].val.clusterDim.x = cluster.x;
+        attrs[n].val.clusterDim.y = cluster.y;
+        attrs[n].val.clusterDim.z = cluster.z;
         ++n;
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
+
+// No thread-block clusters.
+constexpr dim3 kNoCluster(0, 0, 0);
 
 // Launch parameters every entry point passes down.
 struct LaunchEnv {
@@ -94,12 +97,21 @@ cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, c
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                                int64_t K, const LaunchEnv& env);
-// Bytes of workspace launch_w8a8_ws needs (the fp16 codes of both operands
+// Tile width (N side of the 128-row output tile) and split-K factor the
+// tcgen05 kernel uses for a W8A8 problem; 0 and 0 when M is in the decode
+// range.
+cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k);
+// Bytes of workspace launch_w8a8_ws needs (the fp16 token codes, M * K * 2,
 // when M exceeds the decode range; 0 otherwise).
 size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                            const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
                            uint16_t* ws, const LaunchEnv& env);
+// tcgen05 W8A8 for M > 64: the token codes as fp16 (x16, [M, K]), the weight
+// codes as int8 (converted inside the kernel).
+cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t* qw, const float* sw,
+                              const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                              const LaunchEnv& env);
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                         const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                         int64_t K, const LaunchEnv& env);

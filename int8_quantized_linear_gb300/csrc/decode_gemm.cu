@@ -393,7 +393,7 @@ cudaError_t launch_cfg(const DecodeParams& p, int split, cudaStream_t stream) {
     const int64_t row_blocks = (p.N + kRows - 1) / kRows;
     return launch_kernel(decode_gemm_kernel<OP, MT, NT, GROUPED>,
                          dim3((unsigned)row_blocks, (unsigned)split, (unsigned)(GROUPED ? p.E : 1)), dim3(kThreads),
-                         0, stream, (unsigned)split, p);
+                         0, stream, dim3(1, (unsigned)split, 1), p);
 }
 
 // CTAs of this configuration that fit on one SM at once (cached per device).

@@ -5,7 +5,7 @@
 // loops that forbid allocator calls (and their possible synchronisation or
 // failure) on the hot path, and hosts that hand the library only the tensors
 // they already own.  w8a8_gemm needs a workspace for large M (the fp16 codes
-// of both operands) and takes it from the stream-ordered allocator; this
+// of the tokens) and takes it from the stream-ordered allocator; this
 // entry point instead uses one fixed array compiled into the library.
 //
 // The array lives in device global memory: every GPU that loads the library

@@ -175,7 +175,7 @@ cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, 
     const int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
     // one wave: every CTA resident at once (at least 2 per SM fit, 256 threads each)
     const int one_wave = blocks <= 2LL * env.sm_count ? 1 : 0;
-    return launch_kernel(quant_rows_kernel<TPR, VPT>, dim3((unsigned)blocks), dim3(kQuantThreads), 0, env.stream, 0,
+    return launch_kernel(quant_rows_kernel<TPR, VPT>, dim3((unsigned)blocks), dim3(kQuantThreads), 0, env.stream, kNoCluster,
                          src, rows, K, q, s, one_wave);
 }
 

@@ -1,0 +1,799 @@
+// W8A8 GEMM for M > 64: int8 weight tiles are converted to fp16 codes inside
+// the GEMM, between their TMA loads and the tensor core.
+//
+// Sources: "feat(quantization): support compressed-tensors W8A8 and mixed
+// modules", Design and Supported Execution Scheme (static symmetric int8
+// per-channel weights, dynamic symmetric int8 per-token activations, no
+// output quantization) and "Day 6 -- Quantize It Yourself", The mechanism,
+// block 5 (W8A8: both operands 8-bit, the GEMM on the tensor cores).
+//
+//   acc[m,n] = sum_k qx[m,k] * qw[n,k]          (exact int32)
+//   y[m,n]   = bf16_rne(((float)acc * sx[m]) * sw[n] (+ bias[n]))
+//
+// sm_103a has no integer kind of tcgen05.mma, so the product runs as
+// kind::f16 with exact arithmetic: int8 codes are exact in fp16, every
+// product of two codes is exact in fp32, and the fp32 accumulator in tensor
+// memory (TMEM) stays exact over any 1024-deep chunk of k (1024 * 127^2 <
+// 2^24).  After each chunk the epilogue warps drain the chunk sum, convert it
+// to int32 (exact) and add it to int32 running sums in their registers; the
+// chunks alternate between two TMEM buffers.
+//
+// The token codes arrive already as fp16 (one small pass over M x K before
+// this launch).  The weight codes, the large operand, stay int8 in HBM and
+// L2 and are converted per k-block here, so the weights cross HBM once, at
+// one byte per code, with no conversion pass over them.
+//
+// Warp roles (512 threads, one CTA per SM):
+//   warp 13: token TMA (fp16, 128-byte swizzle, straight into the operand
+//     stage the MMA reads);
+//   warp 14: weight TMA (int8 rows of 64 bytes) into an int8 ring of up to 8
+//     stages; ragged edges of both operands are zero-filled by the maps;
+//   warps 8-12: converters, int8 -> fp16 codes (exact), written in the
+//     128-byte-swizzled K-major layout into the operand stage;
+//   warp 15: TMEM allocation and the MMA issuer (one thread),
+//     tcgen05.mma.cta_group::1.kind::f16, M = 128, N = BN;
+//   warps 0-7: epilogue: TMEM -> exact int32 running sums -> scales, bias,
+//     bf16 stores, overlapping the next tile's main loop.  The scales and
+//     bias of a tile are staged in shared memory before its first chunk
+//     completes.
+// Tiles: tokens on the 128-row MMA side and weights on the BN side, or for
+// M <= 128 the reverse ("swap AB": weights fill the 128 rows, the tokens a
+// 128-wide N side).  Registers are rebalanced with setmaxnreg: the epilogue
+// warpgroups hold the running sums (up to 128 per thread), the others need
+// few.
+//
+// Persistent without split-K (CTA b walks tiles b, b + grid, ... in a grouped
+// raster for L2 reuse).  With split-K (few tiles, deep K) a cluster of S CTAs
+// shares one tile: CTA r runs k-blocks [nkb*r/S, nkb*(r+1)/S), parks its
+// exact int32 partial tile in its idle stage memory, and after a cluster
+// barrier reduces rows [128r/S, 128(r+1)/S) over all partials through
+// distributed shared memory, in rank order (integer sums: identical to the
+// unsplit result).
+//
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
+// records I8QL_ERR_TIMEOUT in the sticky fault word, all roles leave their
+// loops, the MMA issuer waits (bounded) for its outstanding MMAs, and the
+// TMEM is freed before the CTA exits.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace i8ql {
+namespace {
+
+using namespace tc;
+
+constexpr int kEpiWarps = 8;     // warps 0-7: two per TMEM lane quarter, one per column half
+constexpr int kConvWarp0 = 8;    // warps 8-13 convert, in two teams of three
+constexpr int kConvWarps = 6;
+constexpr int kTeamWarps = 3;    // team t converts the k-blocks kg with kg % 2 == t
+constexpr int kLoadWarp = 14;    // token and weight TMA
+constexpr int kMmaWarp = 15;
+constexpr int kThreads = 16 * 32;
+// setmaxnreg split: the launch gives 128 registers to each of the 512
+// threads (65,536); the two epilogue warpgroups take 176 and the two others
+// keep 80.
+constexpr int kLaunchRegs = 128;
+constexpr int kEpiRegs = 176;
+constexpr int kAuxRegs = 80;
+static_assert(256 * kEpiRegs + 256 * kAuxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch allocation");
+constexpr int kSmemOptin = 232448;  // largest dynamic shared memory of one CTA (227 KiB)
+constexpr int kMaxStages8 = 8;
+constexpr int kMaxStages16 = 4;
+constexpr int kTokStages = 4;
+constexpr int kCtlBytes = 5120;  // barriers + two sets of staged epilogue parameters
+
+// Shared-memory rings for tile width BN (all stages 1024-byte aligned):
+//   tokens: fp16, 128 rows x 64 k, 128-byte swizzle (TMA writes the layout
+//     the MMA reads);
+//   weights fp16: BN rows x 64 k, same layout (written by the converters);
+//   weights int8: BN rows x 64 k, 64 bytes per row (TMA).
+// The weights are the BN side, or with swapped operands the 128-row side
+// (swap only uses BN = 128).
+template <int BN>
+struct FusedCfg {
+    static constexpr int kTokStage = kBM * kBK * 2;
+    static constexpr int kStage16 = BN * kBK * 2;
+    static constexpr int kStage8 = BN * kBK;
+    static constexpr int kStages16 = BN <= 128 ? 4 : 3;
+    static constexpr int kFixed = kTokStages * kTokStage + kStages16 * kStage16;
+    static constexpr int kFree = kSmemOptin - 1024 /*alignment slack*/ - kCtlBytes - kFixed;
+    static constexpr int kStages8 = kFree / kStage8 < kMaxStages8 ? kFree / kStage8 : kMaxStages8;
+    static constexpr int kW16Off = kTokStages * kTokStage;
+    static constexpr int kW8Off = kFixed;
+    static constexpr int kStageBytes = kFixed + kStages8 * kStage8;
+    static constexpr int kSmemBytes = kStageBytes + 1024 + kCtlBytes;
+    static constexpr int kGroups = BN / 8;  // 8-row groups of weights per stage
+    static constexpr int kGroupsPerWarp = (kGroups + kTeamWarps - 1) / kTeamWarps;
+    static constexpr int kPartStride = BN + 4;  // split-K partial tile row (int32), padded against bank conflicts
+    static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
+    static_assert(kStages8 >= 3 && kStages16 <= kMaxStages16, "ring depths");
+    static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages keep 1024-byte alignment");
+    static_assert(kBM * kPartStride * 4 <= kStageBytes, "split-K partial tile must fit the stages");
+};
+
+// Epilogue parameters of one tile, staged in shared memory before its first
+// chunk completes: per tile column the column-side scale (sw[n], or sx[m]
+// when swapped) and bias bits, per tile row the row-side scale and bias
+// bits.  Missing entries (past M or N, or no bias) are zero and never used.
+struct EpiParams {
+    float col_scale[256];
+    float row_scale[kBM];
+    uint16_t col_bias[256];
+    uint16_t row_bias[kBM];
+};
+
+struct Ctl {
+    uint64_t tok_full[kTokStages];    // the token TMA landed a stage
+    uint64_t tok_empty[kTokStages];   // the MMA is done with a token stage
+    uint64_t w8_full[kMaxStages8];    // the weight TMA landed an int8 stage
+    uint64_t w8_empty[kMaxStages8];   // a converter team is done with an int8 stage
+    uint64_t w16_full[kMaxStages16];  // a converter team filled an fp16 weight stage
+    uint64_t w16_empty[kMaxStages16]; // the MMA is done with an fp16 weight stage
+    uint64_t acc_full[2];             // fp32 chunk accumulator buffers in TMEM
+    uint64_t acc_empty[2];
+    uint64_t drained;
+    uint64_t epi_ready[2];  // all epilogue warps staged the parameters of a set
+    uint64_t epi_free[2];   // all epilogue warps finished the tile of a set
+    uint32_t tmem_base;
+    int abort_flag;
+    EpiParams epi[2];       // double-buffered by local tile parity
+};
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
+
+// Epilogue threads t = 0..255 stage the parameters of tile (ta, tb).
+__device__ __forceinline__ void stage_epi_params(const W8A8Params& p, int64_t ta, int64_t tb, int bn, EpiParams& e,
+                                                 int t) {
+    if (t < bn) {
+        const int64_t j = tb * bn + t;
+        float scale = 0.0f;
+        uint16_t bias = 0;
+        if (!p.swap) {
+            if (j < p.N) {
+                scale = __ldg(p.sw + j);
+                if (p.bias) bias = __ldg(p.bias + j);
+            }
+        } else if (j < p.M) {
+            scale = __ldg(p.sx + j);
+        }
+        e.col_scale[t] = scale;
+        e.col_bias[t] = bias;
+    }
+    if (t < kBM) {
+        const int64_t i = ta * kBM + t;
+        float scale = 0.0f;
+        uint16_t bias = 0;
+        if (!p.swap) {
+            if (i < p.M) scale = __ldg(p.sx + i);
+        } else if (i < p.N) {
+            scale = __ldg(p.sw + i);
+            if (p.bias) bias = __ldg(p.bias + i);
+        }
+        e.row_scale[t] = scale;
+        e.row_bias[t] = bias;
+    }
+}
+
+// Scale/bias epilogue and stores of W consecutive tile columns c .. c+W-1
+// (W = 4 or 8, c a multiple of W) of tile row `row`, from exact int32 sums,
+// in the order the method defines:
+//   y = bf16_rne(((float)acc * sx[m]) * sw[n] (+ bias[n]))
+// Non-swapped tiles hold tokens on the rows, swapped tiles output channels.
+template <int W>
+__device__ __forceinline__ void store_out(const W8A8Params& p, const EpiParams& e, int64_t ta, int64_t tb, int bn,
+                                          int row, int c, const int32_t* v) {
+    if (!p.swap) {
+        const int64_t m = ta * kBM + row;
+        if (m >= p.M) return;
+        const int64_t n0 = tb * bn + c;
+        const float rs = e.row_scale[row];
+        float f[W];
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            f[j] = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), rs), e.col_scale[c + j]);
+            if (p.bias) f[j] = __fadd_rn(f[j], bf16_to_f32(e.col_bias[c + j]));
+        }
+        if (n0 + W <= p.N && (p.N % W) == 0) {
+            uint32_t packed[W / 2];
+#pragma unroll
+            for (int j = 0; j < W; j += 2)
+                packed[j / 2] = (uint32_t)f32_to_bf16_rn(f[j]) | ((uint32_t)f32_to_bf16_rn(f[j + 1]) << 16);
+            if constexpr (W == 8)
+                *reinterpret_cast<uint4*>(p.y + m * p.N + n0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            else
+                *reinterpret_cast<uint2*>(p.y + m * p.N + n0) = make_uint2(packed[0], packed[1]);
+            if (p.acc) {
+#pragma unroll
+                for (int q = 0; q < W; q += 4)
+                    *reinterpret_cast<int4*>(p.acc + m * p.N + n0 + q) = make_int4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) {
+                if (n0 + j < p.N) {
+                    p.y[m * p.N + n0 + j] = f32_to_bf16_rn(f[j]);
+                    if (p.acc) p.acc[m * p.N + n0 + j] = v[j];
+                }
+            }
+        }
+    } else {
+        const int64_t n = ta * kBM + row;
+        if (n >= p.N) return;
+        const float rs = e.row_scale[row];
+        const float rb = bf16_to_f32(e.row_bias[row]);
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            const int64_t m = tb * bn + c + j;
+            if (m < p.M) {
+                float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), e.col_scale[c + j]), rs);
+                if (p.bias) f = __fadd_rn(f, rb);
+                p.y[m * p.N + n] = f32_to_bf16_rn(f);
+                if (p.acc) p.acc[m * p.N + n] = v[j];
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_fused_kernel(const __grid_constant__ CUtensorMap map_tok, const __grid_constant__ CUtensorMap map_wgt,
+                      const W8A8Params p) {
+    using Cfg = FusedCfg<BN>;
+    constexpr int S8 = Cfg::kStages8;
+    constexpr int S16 = Cfg::kStages16;
+    constexpr int ST = kTokStages;
+    constexpr int kHalf = BN / 2;  // columns per epilogue warp
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + Cfg::kStageBytes);
+    int32_t* part = reinterpret_cast<int32_t*>(smem);  // split-K partial tile (after the main loop)
+    const uint32_t tok_base = smem_u32(smem);
+    const uint32_t w16_base = tok_base + Cfg::kW16Off;
+    const uint32_t w8_base = tok_base + Cfg::kW8Off;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t K = p.K;
+    const int nkb = (int)((K + kBK - 1) / kBK);
+    const int S = p.split;
+    const int rank = S > 1 ? (int)cluster_rank() : 0;
+    const int kb_lo = (int)((int64_t)nkb * rank / S);
+    const int kb_hi = (int)((int64_t)nkb * (rank + 1) / S);
+    const int nchunks = (kb_hi - kb_lo + kChunkKB - 1) / kChunkKB;
+    const int64_t tiles = p.tiles_a * p.tiles_b;
+    const int64_t unit0 = blockIdx.x / S;
+    const int64_t unit_step = gridDim.x / S;
+    int* abort = &ctl->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&ctl->tok_full[s], 1);
+            mbar_init(&ctl->tok_empty[s], 1);
+        }
+        for (int s = 0; s < S8; ++s) {
+            mbar_init(&ctl->w8_full[s], 1);
+            mbar_init(&ctl->w8_empty[s], kTeamWarps);
+        }
+        for (int s = 0; s < S16; ++s) {
+            mbar_init(&ctl->w16_full[s], kTeamWarps);
+            mbar_init(&ctl->w16_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->acc_full[b], 1);
+            mbar_init(&ctl->acc_empty[b], kEpiWarps);
+            mbar_init(&ctl->epi_ready[b], kEpiWarps);
+            mbar_init(&ctl->epi_free[b], kEpiWarps);
+        }
+        mbar_init(&ctl->drained, 1);
+        ctl->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        prefetch_map(&map_tok);
+        prefetch_map(&map_wgt);
+    }
+    if (warp == kMmaWarp) tmem_alloc(&ctl->tmem_base, p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    pdl_wait();  // the codes and scales come from earlier launches
+
+    if (warp < kEpiWarps) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const int half = warp >> 2;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int row = quarter * 32 + lane;  // tile row of this thread
+        int32_t run[kHalf];
+        int64_t cg = 0;
+        int64_t lt = 0;  // tiles of this CTA so far
+        bool alive = true;
+        for (int64_t tile = unit0; tile < tiles && alive; tile += unit_step, ++lt) {
+            int64_t ta, tb;
+            tile_coords(p, tile, ta, tb);
+            // Stage this tile's scales and bias in parameter set lt % 2 once
+            // every epilogue warp is done with the tile that used it before;
+            // the loads overlap the MMA of the first chunk.
+            const int eb = (int)(lt & 1);
+            const uint32_t eu = (uint32_t)((lt >> 1) & 1);
+            if (!warp_wait<true>(&ctl->epi_free[eb], eu ^ 1u, abort, p.err)) break;
+            EpiParams& ep = ctl->epi[eb];
+            stage_epi_params(p, ta, tb, BN, ep, (int)threadIdx.x);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->epi_ready[eb]);
+            if (!warp_wait<true>(&ctl->epi_ready[eb], eu, abort, p.err)) break;
+            for (int c = 0; c < nchunks; ++c, ++cg) {
+                const int b = (int)(cg & 1);
+                if (!warp_wait<true>(&ctl->acc_full[b], (uint32_t)((cg >> 1) & 1), abort, p.err)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col0 = (uint32_t)(b * BN + half * kHalf);
+#pragma unroll
+                for (int grp = 0; grp < kHalf / 8; ++grp) {
+                    uint32_t r[8];
+                    tmem_ld8(lane_base + col0 + grp * 8, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int32_t v = __float2int_rn(__uint_as_float(r[j]));  // exact: |v| < 2^24
+                        run[grp * 8 + j] = (c == 0) ? v : run[grp * 8 + j] + v;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->acc_empty[b]);  // the MMA may refill this buffer
+            }
+            if (!alive) break;
+            if (S > 1) {
+                // Split-K: park the partial tile in the idle stage memory (the
+                // last chunk's completion covers every MMA, hence every load
+                // and conversion of this CTA).
+                int4* dst = reinterpret_cast<int4*>(part + row * Cfg::kPartStride + half * kHalf);
+#pragma unroll
+                for (int q = 0; q < kHalf / 4; ++q)
+                    dst[q] = make_int4(run[4 * q], run[4 * q + 1], run[4 * q + 2], run[4 * q + 3]);
+                continue;
+            }
+#pragma unroll
+            for (int q = 0; q < kHalf / 8; ++q) store_out<8>(p, ep, ta, tb, BN, row, half * kHalf + 8 * q, run + 8 * q);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->epi_free[eb]);
+        }
+        // back to the launch share for the common tail
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kAuxRegs));
+        if (warp == kLoadWarp) {
+            // ---------------------------------------------------------- TMA producer
+            // Token and weight loads of a k-block are issued together; each
+            // waits for its own ring.
+            if (lane == 0) {
+                int64_t kg = 0;  // k-blocks issued by this CTA
+                bool alive = true;
+                for (int64_t tile = unit0; tile < tiles && alive; tile += unit_step) {
+                    int64_t ta, tb;
+                    tile_coords(p, tile, ta, tb);
+                    const int32_t tok_row = (int32_t)((p.swap ? tb : ta) * kBM);
+                    const int32_t wgt_row = (int32_t)((p.swap ? ta : tb) * BN);
+                    for (int kb = kb_lo; kb < kb_hi; ++kb, ++kg) {
+                        const int s8 = (int)(kg % S8);
+                        const int st = (int)(kg % ST);
+                        if (!mbar_wait_inline(&ctl->w8_empty[s8], (uint32_t)(((kg / S8) & 1) ^ 1), abort, p.err)) {
+                            alive = false;
+                            break;
+                        }
+                        mbar_expect_tx(&ctl->w8_full[s8], (uint32_t)Cfg::kStage8);
+                        tma_load_2d(w8_base + (uint32_t)(s8 * Cfg::kStage8), &map_wgt, kb * kBK, wgt_row,
+                                    &ctl->w8_full[s8]);
+                        if (!mbar_wait_inline(&ctl->tok_empty[st], (uint32_t)(((kg / ST) & 1) ^ 1), abort, p.err)) {
+                            alive = false;
+                            break;
+                        }
+                        mbar_expect_tx(&ctl->tok_full[st], (uint32_t)Cfg::kTokStage);
+                        tma_load_2d(tok_base + (uint32_t)(st * Cfg::kTokStage), &map_tok, kb * kBK, tok_row,
+                                    &ctl->tok_full[st]);
+                    }
+                }
+            }
+            __syncwarp();
+        } else if (warp == kMmaWarp) {
+            // ---------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                const uint32_t idesc = f16_idesc(BN);
+                int64_t kg = 0;  // k-blocks consumed
+                int64_t cg = 0;  // chunks accumulated
+                bool alive = true;
+                for (int64_t tile = unit0; tile < tiles && alive; tile += unit_step) {
+                    for (int c = 0; c < nchunks && alive; ++c, ++cg) {
+                        const int b = (int)(cg & 1);
+                        // the epilogue must have drained this buffer's previous chunk
+                        if (!mbar_wait_inline(&ctl->acc_empty[b], (uint32_t)(((cg >> 1) & 1) ^ 1), abort, p.err)) {
+                            alive = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem + (uint32_t)(b * BN);
+                        const int kb_first = kb_lo + c * kChunkKB;
+                        const int kb_end = min(kb_hi, kb_first + kChunkKB);
+                        for (int kb = kb_first; kb < kb_end; ++kb, ++kg) {
+                            const int st = (int)(kg % ST);
+                            const int s16 = (int)(kg % S16);
+                            if (!mbar_wait_inline(&ctl->tok_full[st], (uint32_t)((kg / ST) & 1), abort, p.err) ||
+                                !mbar_wait_inline(&ctl->w16_full[s16], (uint32_t)((kg / S16) & 1), abort, p.err)) {
+                                alive = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t tok_st = tok_base + (uint32_t)(st * Cfg::kTokStage);
+                            const uint32_t wgt_st = w16_base + (uint32_t)(s16 * Cfg::kStage16);
+                            const uint32_t a_st = p.swap ? wgt_st : tok_st;
+                            const uint32_t b_st = p.swap ? tok_st : wgt_st;
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                mma_f16(d, sw128_desc(a_st + kk * 32), sw128_desc(b_st + kk * 32), idesc,
+                                        (kb != kb_first || kk != 0) ? 1u : 0u);
+                            mma_commit(&ctl->tok_empty[st]);
+                            mma_commit(&ctl->w16_empty[s16]);
+                        }
+                        if (alive) mma_commit(&ctl->acc_full[b]);
+                    }
+                }
+                // Wait (bounded) until every MMA issued above has completed.
+                mma_commit(&ctl->drained);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try(smem_u32(&ctl->drained), 0)) {
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        record_fault(p.err, kErrBitTimeout);
+                        ctl->abort_flag = 1;
+                        break;
+                    }
+                }
+            }
+            __syncwarp();
+        } else {
+            // ---------------------------------------------------------- converters
+            // Two teams of three warps take alternate k-blocks, so one team's
+            // waits and fences overlap the other team's conversions.  Lane l
+            // of a warp handles 16 int8 codes (k = 16j .. 16j+15, j = l % 4)
+            // of weight row 8g + l / 4 of 8-row group g; a warp issues all its
+            // loads before its conversions.  Reads are contiguous; the two
+            // 16-byte fp16 writes land in 16-byte chunks 2j and 2j+1 of the
+            // row, XOR-swizzled by the row index mod 8 (128-byte swizzle),
+            // which spreads every quarter-warp over all 32 banks.
+            constexpr int G = Cfg::kGroups;
+            constexpr int GPW = Cfg::kGroupsPerWarp;
+            const int cw = warp - kConvWarp0;
+            const int team = cw / kTeamWarps;
+            const int tw = cw % kTeamWarps;
+            const int r_in = lane >> 2;
+            const int j = lane & 3;
+            const uint32_t src0 = w8_base + (uint32_t)(r_in * kBK + j * 16);
+            const uint32_t dst0 = w16_base + (uint32_t)(r_in * (kBK * 2));
+            const uint32_t c0 = (uint32_t)(((2 * j) ^ r_in) << 4);  // swizzled chunk offsets (row mod 8 = r_in)
+            const uint32_t c1 = (uint32_t)(((2 * j + 1) ^ r_in) << 4);
+            const int64_t per_tile = kb_hi - kb_lo;
+            const int64_t total = (tiles > unit0 ? (tiles - unit0 + unit_step - 1) / unit_step : 0) * per_tile;
+            for (int64_t kg = team; kg < total; kg += 2) {
+                const int s8 = (int)(kg % S8);
+                const int s16 = (int)(kg % S16);
+                if (!warp_wait<true>(&ctl->w8_full[s8], (uint32_t)((kg / S8) & 1), abort, p.err) ||
+                    !warp_wait<true>(&ctl->w16_empty[s16], (uint32_t)(((kg / S16) & 1) ^ 1), abort, p.err))
+                    break;
+                const uint32_t src = src0 + (uint32_t)(s8 * Cfg::kStage8);
+                const uint32_t dst = dst0 + (uint32_t)(s16 * Cfg::kStage16);
+                uint4 v[GPW];
+#pragma unroll
+                for (int i = 0; i < GPW; ++i) {
+                    const int g = tw + i * kTeamWarps;
+                    if (g < G) v[i] = lds128(src + (uint32_t)(g * 8 * kBK));
+                }
+#pragma unroll
+                for (int i = 0; i < GPW; ++i) {
+                    const int g = tw + i * kTeamWarps;
+                    if (g < G) {
+                        uint32_t h[8];
+                        i8x4_to_f16(v[i].x, h[0], h[1]);
+                        i8x4_to_f16(v[i].y, h[2], h[3]);
+                        i8x4_to_f16(v[i].z, h[4], h[5]);
+                        i8x4_to_f16(v[i].w, h[6], h[7]);
+                        const uint32_t rbase = dst + (uint32_t)(g * 8 * (kBK * 2));
+                        sts128(rbase + c0, h[0], h[1], h[2], h[3]);
+                        sts128(rbase + c1, h[4], h[5], h[6], h[7]);
+                    }
+                }
+                fence_proxy_async_smem();  // the tensor core reads these stores
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ctl->w16_full[s16]);
+                    mbar_arrive(&ctl->w8_empty[s8]);
+                }
+            }
+        }
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kLaunchRegs));
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, p.tmem_cols);
+    if (S > 1) {
+        // Every CTA of the cluster reaches both barriers, on the abort path too.
+        cluster_sync_all();  // all partial tiles are in place
+        if (unit0 < tiles && !*reinterpret_cast<volatile int*>(&ctl->abort_flag)) {
+            int64_t ta, tb;
+            tile_coords(p, unit0, ta, tb);
+            const int r0 = kBM * rank / S, r1 = kBM * (rank + 1) / S;
+            const int nrows = r1 - r0;
+            constexpr int kVecs = BN / 4;
+            const uint32_t part_addr = smem_u32(part);
+            const EpiParams& ep = ctl->epi[0];  // the CTA's only tile staged set 0
+            for (int i = threadIdx.x; i < nrows * kVecs; i += kThreads) {
+                // consecutive threads take consecutive output channels, so
+                // the stores coalesce in both orientations
+                const int row = p.swap ? r0 + i % nrows : r0 + i / kVecs;
+                const int c = (p.swap ? i / nrows : i % kVecs) * 4;
+                const uint32_t off = part_addr + (uint32_t)(row * Cfg::kPartStride + c) * 4u;
+                int32_t v[4] = {0, 0, 0, 0};
+                for (int q = 0; q < S; ++q) {
+                    const int4 t = ld_dsmem_v4(off, (uint32_t)q);
+                    v[0] += t.x;
+                    v[1] += t.y;
+                    v[2] += t.z;
+                    v[3] += t.w;
+                }
+                store_out<4>(p, ep, ta, tb, BN, row, c, v);
+            }
+        }
+        cluster_sync_all();  // peers are done reading this CTA's partial tile
+    }
+}
+
+// 2-D int8 tensor map over a row-major [rows, K] code matrix: box = 64 k x
+// box_rows rows, no swizzle (rows of 64 bytes in shared memory),
+// out-of-range elements read as zero.
+bool make_map_i8(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows) {
+    auto enc = tc::tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D fp16 tensor map over the row-major [rows, K] token codes: box = 64 k x
+// 128 rows, 128-byte swizzle (the K-major canonical layout the MMA reads),
+// out-of-range elements read as zero.
+bool make_map_f16(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t K) {
+    auto enc = tc::tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tile widths the kernel is built for.
+constexpr int kTileWidths[] = {256, 224, 192, 160, 128};
+
+template <typename F>
+auto with_bn(int bn, F&& f) {
+    switch (bn) {
+        case 256: return f(std::integral_constant<int, 256>{});
+        case 224: return f(std::integral_constant<int, 224>{});
+        case 192: return f(std::integral_constant<int, 192>{});
+        case 160: return f(std::integral_constant<int, 160>{});
+        default: return f(std::integral_constant<int, 128>{});
+    }
+}
+
+// Opt every tile width into its dynamic shared memory, once per device.
+// Occupancy queries and launches both need it.
+cudaError_t prepare_device(int dev) {
+    static std::mutex mu;
+    static bool done[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    for (int bn : kTileWidths) {
+        const cudaError_t e = with_bn(bn, [](auto w) {
+            constexpr int BN = decltype(w)::value;
+            return cudaFuncSetAttribute(w8a8_fused_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        FusedCfg<BN>::kSmemBytes);
+        });
+        if (e != cudaSuccess) return e;
+    }
+    done[dev] = true;
+    return cudaSuccess;
+}
+
+// Clusters of `split` CTAs of the kernel for tile width bn that can run at
+// once on device `dev` (cached; 0 if none or on error).  Needs
+// prepare_device(dev).
+int active_clusters(int dev, int bn, int split) {
+    static std::mutex mu;
+    static int cache[64][5][kMaxSplit + 1] = {};
+    int bi = 0;
+    while (kTileWidths[bi] != bn) ++bi;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return 0;
+    int& slot = cache[dev][bi][split];
+    if (slot == 0) {
+        int n = 0;
+        cudaError_t e = with_bn(bn, [&](auto w) {
+            constexpr int BN = decltype(w)::value;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)split);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = FusedCfg<BN>::kSmemBytes;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = (unsigned)split;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            return cudaOccupancyMaxActiveClusters(&n, w8a8_fused_kernel<BN>, &cfg);
+        });
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        slot = n > 0 ? n : -1;
+    }
+    return slot > 0 ? slot : 0;
+}
+
+struct Plan {
+    int bn;
+    int split;
+    int64_t tiles_a, tiles_b;
+};
+
+// Tile width and split-K factor.  A k-block of a 128 x BN tile is costed
+// BN + 96 (MMA work plus the fixed A-side work); a persistent launch costs
+// its number of waves of tiles, a split launch one wave of clusters plus a
+// fixed allowance for the cross-CTA reduction.
+Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap) {
+    const int64_t nkb = (K + kBK - 1) / kBK;
+    Plan best{128, 1, 1, 1};
+    double best_cost = 1e300;
+    for (int bn : kTileWidths) {
+        if (swap && bn != kBM) continue;  // tokens fill a 128-wide N side
+        const int64_t ta = swap ? (N + kBM - 1) / kBM : (M + kBM - 1) / kBM;
+        const int64_t tb = swap ? 1 : (N + bn - 1) / bn;
+        const int64_t tiles = ta * tb;
+        const double per_kb = bn + 96.0;
+        const double waves = (double)((tiles + sms - 1) / sms);
+        double cost = waves * (double)nkb * per_kb + 4.0 * per_kb;
+        int split = 1;
+        if (tiles < sms) {
+            for (int s = 2; s <= kMaxSplit && s * 4 <= nkb; ++s) {
+                if (tiles * s > sms || tiles > active_clusters(dev, bn, s)) continue;
+                const double c = ((double)((nkb + s - 1) / s) + 8.0) * per_kb;
+                if (c < cost) {
+                    cost = c;
+                    split = s;
+                }
+            }
+        }
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = Plan{bn, split, ta, tb};
+        }
+    }
+    return best;
+}
+
+uint32_t pow2_cols(int need) {
+    uint32_t c = 32;
+    while ((int)c < need) c <<= 1;
+    return c;
+}
+
+}  // namespace
+
+namespace tc {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+}  // namespace tc
+
+cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k) {
+    if (M <= kW8A8DecodeMaxM) {
+        *tile_n = 0;
+        *split_k = 0;
+        return cudaSuccess;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare_device(dev)) != cudaSuccess) return e;
+    const Plan plan = choose_plan(dev, M, N, K, sms, M <= kBM);
+    *tile_n = plan.bn;
+    *split_k = plan.split;
+    return cudaSuccess;
+}
+
+cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t* qw, const float* sw,
+                              const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                              const LaunchEnv& env) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare_device(dev)) != cudaSuccess) return e;
+    W8A8Params p = {};
+    p.K = K;
+    p.sx = sx;
+    p.sw = sw;
+    p.bias = bias;
+    p.y = y;
+    p.acc = acc;
+    p.M = M;
+    p.N = N;
+    p.err = env.err;
+    // For M <= 128, "swap AB": weights fill the 128-row MMA operand and the
+    // tokens the N side (a 128-row box; the tensor map reads zeros past M).
+    p.swap = M <= kBM ? 1 : 0;
+    const Plan plan = choose_plan(dev, M, N, K, env.sm_count, p.swap != 0);
+    p.bn = plan.bn;
+    p.split = plan.split;
+    p.tiles_a = plan.tiles_a;
+    p.tiles_b = plan.tiles_b;
+    p.rows_a = p.swap ? N : M;
+    p.rows_b = p.swap ? M : N;
+    p.tmem_cols = pow2_cols(2 * p.bn);  // two fp32 chunk buffers
+    CUtensorMap map_tok, map_wgt;
+    if (!make_map_f16(&map_tok, x16, M, K) || !make_map_i8(&map_wgt, qw, N, K, p.bn)) return cudaErrorInvalidValue;
+    const int64_t tiles = p.tiles_a * p.tiles_b;
+    // split: one tile per cluster; otherwise persistent, one CTA per SM
+    const int64_t grid = p.split > 1 ? tiles * p.split : std::min<int64_t>(tiles, env.sm_count);
+    const dim3 cluster = p.split > 1 ? dim3((unsigned)p.split, 1, 1) : kNoCluster;
+    return with_bn(p.bn, [&](auto w) {
+        constexpr int BN = decltype(w)::value;
+        return launch_kernel(w8a8_fused_kernel<BN>, dim3((unsigned)grid), dim3(kThreads), FusedCfg<BN>::kSmemBytes,
+                             env.stream, cluster, map_tok, map_wgt, p);
+    });
+}
+
+}  // namespace i8ql

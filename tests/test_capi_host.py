@@ -130,10 +130,22 @@ def test_w8a8_noalloc_argument_errors(lib):
     args = list(ok); args[7] = 0
     assert f(*args) == capi.I8QL_OK
     # beyond the fixed array on the large-M path: refused before any CUDA call
-    big = list(ok); big[7] = 128; big[8] = capi.I8QL_NOALLOC_MAX_ELEMENTS // 4096; big[9] = 4096
+    big = list(ok); big[7] = capi.I8QL_NOALLOC_MAX_ELEMENTS // 4096 + 1; big[8] = 48; big[9] = 4096
     assert f(*big) == capi.I8QL_ERR_WORKSPACE_LIMIT
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_call_without_device_reports_no_device(lib):
     assert lib.w8a16_gemm(A, B, C, D, 4, 16, 64, None) == capi.I8QL_ERR_NO_DEVICE
+
+
+def test_w8a8_plan_argument_errors(lib):
+    import ctypes
+    a, b = ctypes.c_int32(0), ctypes.c_int32(0)
+    f = lib.i8ql_w8a8_plan
+    assert f(256, 512, 40, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_UNSUPPORTED
+    assert f(256, 0, 64, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_INVALID_ARG
+    assert f(-1, 16, 64, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_INVALID_ARG
+    assert f(256, 16, 64, None, ctypes.byref(b)) == capi.I8QL_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert f(256, 16, 64, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_NO_DEVICE

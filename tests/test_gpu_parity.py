@@ -231,6 +231,38 @@ def test_w8a8_qwen3_4b_prefill_sampled(shape, m):
     assert util.max_ulp_diff(y[pm, pn], ref_y) <= 1
 
 
+# Shapes that drive the tensor-core kernel through every tile width and
+# through split-K clusters (deep K, few tiles), swapped and not, with ragged
+# M, N and K edges.
+PLAN_SHAPES = [(65, 640, 9728), (100, 2560, 2560), (128, 200, 12288), (129, 2560, 9728), (256, 512, 4096),
+               (300, 1000, 4160), (512, 6144, 2560), (1024, 2560, 2560), (2048, 6144, 2560),
+               (2048, 19456, 2560), (4096, 2560, 2560), (777, 3000, 1040)]
+
+
+def test_w8a8_plans_cover_tile_widths_and_split_k():
+    plans = {capi.i8ql_w8a8_plan(m, n, k) for m, n, k in PLAN_SHAPES}
+    assert {bn for bn, _ in plans} >= {128, 160, 192, 224, 256}, plans
+    assert any(s > 1 for _, s in plans) and any(s == 1 for _, s in plans), plans
+    assert capi.i8ql_w8a8_plan(64, 4096, 4096) == (0, 0)
+
+
+@pytest.mark.parametrize("m,n,k", PLAN_SHAPES)
+def test_w8a8_plan_shapes_sampled(m, n, k):
+    qx, qw = _codes(m, k, m + 7 * k), _codes(n, k, n + 11 * k)
+    sx, sw = _scales(m, m + 3, 0.01, 1.0), _scales(n, n + 4)
+    bias = util.bits(synthetic.bias(n, n + 1)) if m % 2 else None
+    acc, y = gpu_w8a8(qx, sx, qw, sw, bias)
+    pm, pn = _points(m, n, 4000, m * n + k)
+    ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, bias, pm, pn)
+    assert np.array_equal(acc[pm, pn].astype(np.int64), ref_acc)
+    assert util.max_ulp_diff(y[pm, pn], ref_y) <= 1
+    # whole tiles agree with the exact integer product (int64 on the host)
+    rows = slice(max(0, m - 130), m)
+    cols = slice(0, min(n, 300))
+    ref_block = qx[rows].astype(np.int64) @ qw[cols].astype(np.int64).T
+    assert np.array_equal(acc[rows, cols].astype(np.int64), ref_block)
+
+
 # ------------------------------------------------------------------ W8A16
 
 def gpu_w8a16(x_bf16, qw, sw):

@@ -65,8 +65,8 @@ def test_noalloc_matches_w8a8_gemm_on_consecutive_calls(shapes):
 
 def test_noalloc_rejects_problems_beyond_its_array():
     k = 4096
-    m = 128
-    n = capi.I8QL_NOALLOC_MAX_ELEMENTS // k  # (m + n) * k just over the limit
+    m = capi.I8QL_NOALLOC_MAX_ELEMENTS // k + 1  # m * k just over the limit
+    n = 48
     qx = torch.zeros((m, k), dtype=torch.int8, device="cuda")
     qw = torch.zeros((n, k), dtype=torch.int8, device="cuda")
     sx = torch.ones(m, device="cuda")
@@ -75,7 +75,7 @@ def test_noalloc_rejects_problems_beyond_its_array():
     with pytest.raises(capi.I8qlError) as err:
         capi.w8a8_gemm_noalloc(qx, sx, qw, sw, y)
     assert err.value.status == capi.I8QL_ERR_WORKSPACE_LIMIT
-    # the decode range needs no workspace, whatever N * K is
+    # the decode range needs no workspace, whatever M * K would be
     qx8, sx8 = qx[:8].contiguous(), sx[:8].contiguous()
     y8 = torch.zeros((8, n), dtype=torch.bfloat16, device="cuda")
     capi.w8a8_gemm_noalloc(qx8, sx8, qw, sw, y8)
