@@ -177,14 +177,17 @@ i8ql_status w8a8_gemm_noalloc(const int8_t* qx, const float* sx, const int8_t* q
  * device, without launching anything.
  *
  * No counterpart on the pages: a query for tests and profiling.  For
- * M <= 64 (the decode kernel) both outputs are 0.  Otherwise *tile_n is the
- * width (N side) of the 128-row output tiles of the tensor-core kernel (128,
- * 160, 192, 224 or 256; for M <= 128 the operands are swapped and the tokens
- * fill a 128-wide side) and *split_k the number of CTAs of a thread-block
- * cluster that share one tile's k range (1: persistent, no split).
- * Same argument rules as w8a8_gemm; tile_n and split_k are HOST pointers.
+ * M <= 64 (the decode kernel) all outputs are 0.  Otherwise *tile_n is the
+ * width (N side) of the output tiles of the tensor-core kernel (128, 160,
+ * 192, 224 or 256; for M <= 128 the operands are swapped and the tokens fill
+ * a 128-wide side), *split_k the number of CTAs of a thread-block cluster
+ * that share one tile's k range (1: no split), and *cta_pair 1 when pairs of
+ * CTAs on two SMs share 256-row tiles through one two-SM MMA (0: one CTA per
+ * 128-row tile).  Same argument rules as w8a8_gemm; the outputs are HOST
+ * pointers.
  */
-i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k);
+i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k,
+                           int32_t* cta_pair);
 
 /*
  * Waits for `stream`, then reads and clears the current device's sticky

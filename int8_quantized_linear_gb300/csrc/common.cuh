@@ -97,10 +97,10 @@ cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, c
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                                int64_t K, const LaunchEnv& env);
-// Tile width (N side of the 128-row output tile) and split-K factor the
-// tcgen05 kernel uses for a W8A8 problem; 0 and 0 when M is in the decode
+// Tile width (N side of the output tile), split-K factor and CTA-pair flag
+// the tcgen05 kernel uses for a W8A8 problem; all 0 when M is in the decode
 // range.
-cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k);
+cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k, int* pair);
 // Bytes of workspace launch_w8a8_ws needs (the fp16 token codes, M * K * 2,
 // when M exceeds the decode range; 0 otherwise).
 size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K);

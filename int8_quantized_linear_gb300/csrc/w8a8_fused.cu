@@ -91,19 +91,22 @@ constexpr int kMaxStages16 = 4;
 constexpr int kTokStages = 4;
 constexpr int kCtlBytes = 5120;  // barriers + two sets of staged epilogue parameters
 
-// Shared-memory rings for tile width BN (all stages 1024-byte aligned):
+// Shared-memory rings of one CTA for tile width BN (all stages 1024-byte
+// aligned), with W = BN weight rows per CTA, or BN / 2 for a CTA pair:
 //   tokens: fp16, 128 rows x 64 k, 128-byte swizzle (TMA writes the layout
 //     the MMA reads);
-//   weights fp16: BN rows x 64 k, same layout (written by the converters);
-//   weights int8: BN rows x 64 k, 64 bytes per row (TMA).
+//   weights fp16: W rows x 64 k, same layout (written by the converters);
+//   weights int8: W rows x 64 k, 64 bytes per row (TMA).
 // The weights are the BN side, or with swapped operands the 128-row side
-// (swap only uses BN = 128).
-template <int BN>
+// (swap only uses BN = 128, never pairs).
+template <int BN, bool PAIR>
 struct FusedCfg {
+    static constexpr int kWRows = PAIR ? BN / 2 : BN;
+    static constexpr int kTileM = PAIR ? 2 * kBM : kBM;  // token rows of a (non-swapped) tile
     static constexpr int kTokStage = kBM * kBK * 2;
-    static constexpr int kStage16 = BN * kBK * 2;
-    static constexpr int kStage8 = BN * kBK;
-    static constexpr int kStages16 = BN <= 128 ? 4 : 3;
+    static constexpr int kStage16 = kWRows * kBK * 2;
+    static constexpr int kStage8 = kWRows * kBK;
+    static constexpr int kStages16 = kWRows <= 128 ? 4 : 3;
     static constexpr int kFixed = kTokStages * kTokStage + kStages16 * kStage16;
     static constexpr int kFree = kSmemOptin - 1024 /*alignment slack*/ - kCtlBytes - kFixed;
     static constexpr int kStages8 = kFree / kStage8 < kMaxStages8 ? kFree / kStage8 : kMaxStages8;
@@ -111,13 +114,14 @@ struct FusedCfg {
     static constexpr int kW8Off = kFixed;
     static constexpr int kStageBytes = kFixed + kStages8 * kStage8;
     static constexpr int kSmemBytes = kStageBytes + 1024 + kCtlBytes;
-    static constexpr int kGroups = BN / 8;  // 8-row groups of weights per stage
+    static constexpr int kGroups = kWRows / 8;  // 8-row groups of weights per stage
     static constexpr int kGroupsPerWarp = (kGroups + kTeamWarps - 1) / kTeamWarps;
     static constexpr int kPartStride = BN + 4;  // split-K partial tile row (int32), padded against bank conflicts
     static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
     static_assert(kStages8 >= 3 && kStages16 <= kMaxStages16, "ring depths");
     static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(kBM * kPartStride * 4 <= kStageBytes, "split-K partial tile must fit the stages");
+    static_assert(kWRows % 8 == 0, "weight rows fill whole swizzle atoms");
 };
 
 // Epilogue parameters of one tile, staged in shared memory before its first
@@ -150,10 +154,10 @@ struct Ctl {
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 // Epilogue threads t = 0..255 stage the parameters of tile (ta, tb).
-__device__ __forceinline__ void stage_epi_params(const W8A8Params& p, int64_t ta, int64_t tb, int bn, EpiParams& e,
-                                                 int t) {
+__device__ __forceinline__ void stage_epi_params(const W8A8Params& p, int64_t row_base, int64_t col_base, int bn,
+                                                 EpiParams& e, int t) {
     if (t < bn) {
-        const int64_t j = tb * bn + t;
+        const int64_t j = col_base + t;
         float scale = 0.0f;
         uint16_t bias = 0;
         if (!p.swap) {
@@ -168,7 +172,7 @@ __device__ __forceinline__ void stage_epi_params(const W8A8Params& p, int64_t ta
         e.col_bias[t] = bias;
     }
     if (t < kBM) {
-        const int64_t i = ta * kBM + t;
+        const int64_t i = row_base + t;
         float scale = 0.0f;
         uint16_t bias = 0;
         if (!p.swap) {
@@ -188,12 +192,12 @@ __device__ __forceinline__ void stage_epi_params(const W8A8Params& p, int64_t ta
 //   y = bf16_rne(((float)acc * sx[m]) * sw[n] (+ bias[n]))
 // Non-swapped tiles hold tokens on the rows, swapped tiles output channels.
 template <int W>
-__device__ __forceinline__ void store_out(const W8A8Params& p, const EpiParams& e, int64_t ta, int64_t tb, int bn,
-                                          int row, int c, const int32_t* v) {
+__device__ __forceinline__ void store_out(const W8A8Params& p, const EpiParams& e, int64_t row_base,
+                                          int64_t col_base, int row, int c, const int32_t* v) {
     if (!p.swap) {
-        const int64_t m = ta * kBM + row;
+        const int64_t m = row_base + row;
         if (m >= p.M) return;
-        const int64_t n0 = tb * bn + c;
+        const int64_t n0 = col_base + c;
         const float rs = e.row_scale[row];
         float f[W];
 #pragma unroll
@@ -225,13 +229,13 @@ __device__ __forceinline__ void store_out(const W8A8Params& p, const EpiParams& 
             }
         }
     } else {
-        const int64_t n = ta * kBM + row;
+        const int64_t n = row_base + row;
         if (n >= p.N) return;
         const float rs = e.row_scale[row];
         const float rb = bf16_to_f32(e.row_bias[row]);
 #pragma unroll
         for (int j = 0; j < W; ++j) {
-            const int64_t m = tb * bn + c + j;
+            const int64_t m = col_base + c + j;
             if (m < p.M) {
                 float f = __fmul_rn(__fmul_rn(__int2float_rn(v[j]), e.col_scale[c + j]), rs);
                 if (p.bias) f = __fadd_rn(f, rb);
@@ -252,11 +256,11 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_fused_kernel(const __grid_constant__ CUtensorMap map_tok, const __grid_constant__ CUtensorMap map_wgt,
                       const W8A8Params p) {
-    using Cfg = FusedCfg<BN>;
+    using Cfg = FusedCfg<BN, PAIR>;
     constexpr int S8 = Cfg::kStages8;
     constexpr int S16 = Cfg::kStages16;
     constexpr int ST = kTokStages;
@@ -273,19 +277,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int64_t K = p.K;
     const int nkb = (int)((K + kBK - 1) / kBK);
-    const int S = p.split;
-    const int rank = S > 1 ? (int)cluster_rank() : 0;
-    const int kb_lo = (int)((int64_t)nkb * rank / S);
-    const int kb_hi = (int)((int64_t)nkb * (rank + 1) / S);
+    // A pair (cluster of 2) shares every tile; split-K clusters (p.split
+    // CTAs, never pairs) share one tile's k range.
+    const int S = PAIR ? 1 : p.split;
+    const int csize = PAIR ? 2 : S;
+    const int rank = csize > 1 ? (int)cluster_rank() : 0;
+    const int krank = PAIR ? 0 : rank;
+    const int prank = PAIR ? rank : 0;  // half of the pair this CTA holds
+    const bool leader = prank == 0;
+    const int kb_lo = (int)((int64_t)nkb * krank / S);
+    const int kb_hi = (int)((int64_t)nkb * (krank + 1) / S);
     const int nchunks = (kb_hi - kb_lo + kChunkKB - 1) / kChunkKB;
     const int64_t tiles = p.tiles_a * p.tiles_b;
-    const int64_t unit0 = blockIdx.x / S;
-    const int64_t unit_step = gridDim.x / S;
+    const int64_t unit0 = blockIdx.x / csize;
+    const int64_t unit_step = gridDim.x / csize;
     int* abort = &ctl->abort_flag;
+    // Barriers the MMA issuer waits on live in the leader; a pair's CTAs
+    // arrive on them through cluster addresses.
+    constexpr uint32_t kArrivers = PAIR ? 2 : 1;
+    auto leader_addr = [&](uint64_t* bar) -> uint32_t { return PAIR ? mapa(smem_u32(bar), 0) : smem_u32(bar); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
-            mbar_init(&ctl->tok_full[s], 1);
+            mbar_init(&ctl->tok_full[s], kArrivers);
             mbar_init(&ctl->tok_empty[s], 1);
         }
         for (int s = 0; s < S8; ++s) {
@@ -293,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ctl->w8_empty[s], kTeamWarps);
         }
         for (int s = 0; s < S16; ++s) {
-            mbar_init(&ctl->w16_full[s], kTeamWarps);
+            mbar_init(&ctl->w16_full[s], kArrivers * kTeamWarps);
             mbar_init(&ctl->w16_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->acc_full[b], 1);
-            mbar_init(&ctl->acc_empty[b], kEpiWarps);
+            mbar_init(&ctl->acc_empty[b], kArrivers * kEpiWarps);
             mbar_init(&ctl->epi_ready[b], kEpiWarps);
             mbar_init(&ctl->epi_free[b], kEpiWarps);
         }
@@ -310,9 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_map(&map_tok);
         prefetch_map(&map_wgt);
     }
-    if (warp == kMmaWarp) tmem_alloc(&ctl->tmem_base, p.tmem_cols);
+    if (warp == kMmaWarp) {
+        if constexpr (PAIR)
+            tmem_alloc_pair(&ctl->tmem_base, p.tmem_cols);
+        else
+            tmem_alloc(&ctl->tmem_base, p.tmem_cols);
+    }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     pdl_wait();  // the codes and scales come from earlier launches
@@ -338,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t eu = (uint32_t)((lt >> 1) & 1);
             if (!warp_wait<true>(&ctl->epi_free[eb], eu ^ 1u, abort, p.err)) break;
             EpiParams& ep = ctl->epi[eb];
-            stage_epi_params(p, ta, tb, BN, ep, (int)threadIdx.x);
+            const int64_t row_base = ta * Cfg::kTileM + prank * kBM;
+            const int64_t col_base = tb * BN;
+            stage_epi_params(p, row_base, col_base, BN, ep, (int)threadIdx.x);
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->epi_ready[eb]);
             if (!warp_wait<true>(&ctl->epi_ready[eb], eu, abort, p.err)) break;
@@ -363,7 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->acc_empty[b]);  // the MMA may refill this buffer
+                if (lane == 0) {  // the MMA may refill this buffer
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(leader_addr(&ctl->acc_empty[b]));
+                    else
+                        mbar_arrive(&ctl->acc_empty[b]);
+                }
             }
             if (!alive) break;
             if (S > 1) {
@@ -377,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 #pragma unroll
-            for (int q = 0; q < kHalf / 8; ++q) store_out<8>(p, ep, ta, tb, BN, row, half * kHalf + 8 * q, run + 8 * q);
+            for (int q = 0; q < kHalf / 8; ++q)
+                store_out<8>(p, ep, row_base, col_base, row, half * kHalf + 8 * q, run + 8 * q);
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->epi_free[eb]);
         }
@@ -395,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t tile = unit0; tile < tiles && alive; tile += unit_step) {
                     int64_t ta, tb;
                     tile_coords(p, tile, ta, tb);
-                    const int32_t tok_row = (int32_t)((p.swap ? tb : ta) * kBM);
-                    const int32_t wgt_row = (int32_t)((p.swap ? ta : tb) * BN);
+                    const int32_t tok_row = (int32_t)(p.swap ? tb * kBM : ta * Cfg::kTileM + prank * kBM);
+                    const int32_t wgt_row = (int32_t)(p.swap ? ta * kBM : tb * BN + prank * Cfg::kWRows);
                     for (int kb = kb_lo; kb < kb_hi; ++kb, ++kg) {
                         const int s8 = (int)(kg % S8);
                         const int st = (int)(kg % ST);
@@ -411,17 +441,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                             alive = false;
                             break;
                         }
-                        mbar_expect_tx(&ctl->tok_full[st], (uint32_t)Cfg::kTokStage);
-                        tma_load_2d(tok_base + (uint32_t)(st * Cfg::kTokStage), &map_tok, kb * kBK, tok_row,
-                                    &ctl->tok_full[st]);
+                        if constexpr (PAIR) {
+                            // both halves of the token tile complete on the leader's barrier
+                            const uint32_t bar = leader_addr(&ctl->tok_full[st]);
+                            mbar_expect_tx_cluster(bar, (uint32_t)Cfg::kTokStage);
+                            tma_load_2d_pair(tok_base + (uint32_t)(st * Cfg::kTokStage), &map_tok, kb * kBK, tok_row,
+                                             bar);
+                        } else {
+                            mbar_expect_tx(&ctl->tok_full[st], (uint32_t)Cfg::kTokStage);
+                            tma_load_2d(tok_base + (uint32_t)(st * Cfg::kTokStage), &map_tok, kb * kBK, tok_row,
+                                        &ctl->tok_full[st]);
+                        }
                     }
                 }
             }
             __syncwarp();
         } else if (warp == kMmaWarp) {
             // ---------------------------------------------------------- MMA issuer
-            if (lane == 0) {
-                const uint32_t idesc = f16_idesc(BN);
+            if (lane == 0 && leader) {
+                const uint32_t idesc = PAIR ? f16_idesc_pair(BN) : f16_idesc(BN);
+                auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_inline(bar, parity, abort, p.err); };
+                auto commit = [&](uint64_t* bar) {
+                    if constexpr (PAIR)
+                        mma_commit_pair(bar);
+                    else
+                        mma_commit(bar);
+                };
                 int64_t kg = 0;  // k-blocks consumed
                 int64_t cg = 0;  // chunks accumulated
                 bool alive = true;
@@ -429,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < nchunks && alive; ++c, ++cg) {
                         const int b = (int)(cg & 1);
                         // the epilogue must have drained this buffer's previous chunk
-                        if (!mbar_wait_inline(&ctl->acc_empty[b], (uint32_t)(((cg >> 1) & 1) ^ 1), abort, p.err)) {
+                        if (!wait(&ctl->acc_empty[b], (uint32_t)(((cg >> 1) & 1) ^ 1))) {
                             alive = false;
                             break;
                         }
@@ -440,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int kb = kb_first; kb < kb_end; ++kb, ++kg) {
                             const int st = (int)(kg % ST);
                             const int s16 = (int)(kg % S16);
-                            if (!mbar_wait_inline(&ctl->tok_full[st], (uint32_t)((kg / ST) & 1), abort, p.err) ||
-                                !mbar_wait_inline(&ctl->w16_full[s16], (uint32_t)((kg / S16) & 1), abort, p.err)) {
+                            if (!wait(&ctl->tok_full[st], (uint32_t)((kg / ST) & 1)) ||
+                                !wait(&ctl->w16_full[s16], (uint32_t)((kg / S16) & 1))) {
                                 alive = false;
                                 break;
                             }
@@ -451,17 +496,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t a_st = p.swap ? wgt_st : tok_st;
                             const uint32_t b_st = p.swap ? tok_st : wgt_st;
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk)
-                                mma_f16(d, sw128_desc(a_st + kk * 32), sw128_desc(b_st + kk * 32), idesc,
-                                        (kb != kb_first || kk != 0) ? 1u : 0u);
-                            mma_commit(&ctl->tok_empty[st]);
-                            mma_commit(&ctl->w16_empty[s16]);
+                            for (int kk = 0; kk < kBK / 16; ++kk) {
+                                const uint64_t ad = sw128_desc(a_st + kk * 32);
+                                const uint64_t bd = sw128_desc(b_st + kk * 32);
+                                const uint32_t acc = (kb != kb_first || kk != 0) ? 1u : 0u;
+                                if constexpr (PAIR)
+                                    mma_f16_pair(d, ad, bd, idesc, acc);
+                                else
+                                    mma_f16(d, ad, bd, idesc, acc);
+                            }
+                            commit(&ctl->tok_empty[st]);
+                            commit(&ctl->w16_empty[s16]);
                         }
-                        if (alive) mma_commit(&ctl->acc_full[b]);
+                        if (alive) commit(&ctl->acc_full[b]);
                     }
                 }
                 // Wait (bounded) until every MMA issued above has completed.
-                mma_commit(&ctl->drained);
+                commit(&ctl->drained);
                 const uint64_t t0 = global_ns();
                 while (!mbar_try(smem_u32(&ctl->drained), 0)) {
                     if (global_ns() - t0 > kWaitLimitNs) {
@@ -526,7 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();  // the tensor core reads these stores
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&ctl->w16_full[s16]);
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(leader_addr(&ctl->w16_full[s16]));
+                    else
+                        mbar_arrive(&ctl->w16_full[s16]);
                     mbar_arrive(&ctl->w8_empty[s8]);
                 }
             }
@@ -537,6 +591,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (PAIR) {
+        // Neither CTA leaves (or frees TMEM) while the pair's MMAs, TMA
+        // completions or remote arrives may still touch it.
+        cluster_sync_all();
+        tc_fence_after();
+        if (warp == kMmaWarp) tmem_dealloc_pair(tmem, p.tmem_cols);
+        return;
+    }
     if (warp == kMmaWarp) tmem_dealloc(tmem, p.tmem_cols);
     if (S > 1) {
         // Every CTA of the cluster reaches both barriers, on the abort path too.
@@ -544,6 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (unit0 < tiles && !*reinterpret_cast<volatile int*>(&ctl->abort_flag)) {
             int64_t ta, tb;
             tile_coords(p, unit0, ta, tb);
+            const int64_t row_base = ta * kBM, col_base = tb * BN;
             const int r0 = kBM * rank / S, r1 = kBM * (rank + 1) / S;
             const int nrows = r1 - r0;
             constexpr int kVecs = BN / 4;
@@ -563,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[2] += t.z;
                     v[3] += t.w;
                 }
-                store_out<4>(p, ep, ta, tb, BN, row, c, v);
+                store_out<4>(p, ep, row_base, col_base, row, c, v);
             }
         }
         cluster_sync_all();  // peers are done reading this CTA's partial tile
@@ -600,21 +663,37 @@ bool make_map_f16(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The tile widths the kernel is built for.
+// The tile widths the kernel is built for (single CTAs), and those of CTA
+// pairs.
 constexpr int kTileWidths[] = {256, 224, 192, 160, 128};
+constexpr int kPairWidths[] = {256, 192, 128};
+// A pair moves a 256 x BN tile through two SMs with half the shared-memory
+// operand traffic and conversion work per SM of a single-CTA 128 x BN tile;
+// its k-blocks are costed at this fraction of the single-CTA ones.
+constexpr double kPairCost = 0.75;
 
+// Calls f with (integral_constant BN, integral_constant PAIR) for a built
+// configuration.
 template <typename F>
-auto with_bn(int bn, F&& f) {
+auto with_cfg(int bn, bool pair, F&& f) {
+    using std::integral_constant;
+    if (pair) {
+        switch (bn) {
+            case 256: return f(integral_constant<int, 256>{}, integral_constant<bool, true>{});
+            case 192: return f(integral_constant<int, 192>{}, integral_constant<bool, true>{});
+            default: return f(integral_constant<int, 128>{}, integral_constant<bool, true>{});
+        }
+    }
     switch (bn) {
-        case 256: return f(std::integral_constant<int, 256>{});
-        case 224: return f(std::integral_constant<int, 224>{});
-        case 192: return f(std::integral_constant<int, 192>{});
-        case 160: return f(std::integral_constant<int, 160>{});
-        default: return f(std::integral_constant<int, 128>{});
+        case 256: return f(integral_constant<int, 256>{}, integral_constant<bool, false>{});
+        case 224: return f(integral_constant<int, 224>{}, integral_constant<bool, false>{});
+        case 192: return f(integral_constant<int, 192>{}, integral_constant<bool, false>{});
+        case 160: return f(integral_constant<int, 160>{}, integral_constant<bool, false>{});
+        default: return f(integral_constant<int, 128>{}, integral_constant<bool, false>{});
     }
 }
 
-// Opt every tile width into its dynamic shared memory, once per device.
+// Opt every configuration into its dynamic shared memory, once per device.
 // Occupancy queries and launches both need it.
 cudaError_t prepare_device(int dev) {
     static std::mutex mu;
@@ -622,45 +701,51 @@ cudaError_t prepare_device(int dev) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
+    auto set = [](auto w, auto pr) {
+        constexpr int BN = decltype(w)::value;
+        constexpr bool PAIR = decltype(pr)::value;
+        return cudaFuncSetAttribute(w8a8_fused_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    FusedCfg<BN, PAIR>::kSmemBytes);
+    };
     for (int bn : kTileWidths) {
-        const cudaError_t e = with_bn(bn, [](auto w) {
-            constexpr int BN = decltype(w)::value;
-            return cudaFuncSetAttribute(w8a8_fused_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        FusedCfg<BN>::kSmemBytes);
-        });
+        const cudaError_t e = with_cfg(bn, false, set);
+        if (e != cudaSuccess) return e;
+    }
+    for (int bn : kPairWidths) {
+        const cudaError_t e = with_cfg(bn, true, set);
         if (e != cudaSuccess) return e;
     }
     done[dev] = true;
     return cudaSuccess;
 }
 
-// Clusters of `split` CTAs of the kernel for tile width bn that can run at
-// once on device `dev` (cached; 0 if none or on error).  Needs
-// prepare_device(dev).
-int active_clusters(int dev, int bn, int split) {
+// Clusters of `csize` CTAs of a configuration that can run at once on
+// device `dev` (cached; 0 if none or on error).  Needs prepare_device(dev).
+int active_clusters(int dev, int bn, bool pair, int csize) {
     static std::mutex mu;
-    static int cache[64][5][kMaxSplit + 1] = {};
+    static int cache[64][2][5][kMaxSplit + 1] = {};
     int bi = 0;
     while (kTileWidths[bi] != bn) ++bi;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= 64) return 0;
-    int& slot = cache[dev][bi][split];
+    if (dev < 0 || dev >= 64 || csize < 1 || csize > kMaxSplit) return 0;
+    int& slot = cache[dev][pair ? 1 : 0][bi][csize];
     if (slot == 0) {
         int n = 0;
-        cudaError_t e = with_bn(bn, [&](auto w) {
+        cudaError_t e = with_cfg(bn, pair, [&](auto w, auto pr) {
             constexpr int BN = decltype(w)::value;
+            constexpr bool PAIR = decltype(pr)::value;
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)split);
+            cfg.gridDim = dim3((unsigned)csize);
             cfg.blockDim = dim3(kThreads);
-            cfg.dynamicSmemBytes = FusedCfg<BN>::kSmemBytes;
+            cfg.dynamicSmemBytes = FusedCfg<BN, PAIR>::kSmemBytes;
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = (unsigned)split;
+            attr.val.clusterDim.x = (unsigned)csize;
             attr.val.clusterDim.y = 1;
             attr.val.clusterDim.z = 1;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            return cudaOccupancyMaxActiveClusters(&n, w8a8_fused_kernel<BN>, &cfg);
+            return cudaOccupancyMaxActiveClusters(&n, w8a8_fused_kernel<BN, PAIR>, &cfg);
         });
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -674,16 +759,18 @@ int active_clusters(int dev, int bn, int split) {
 struct Plan {
     int bn;
     int split;
+    bool pair;
+    int64_t units;  // CTAs (or clusters) the persistent grid runs
     int64_t tiles_a, tiles_b;
 };
 
-// Tile width and split-K factor.  A k-block of a 128 x BN tile is costed
-// BN + 96 (MMA work plus the fixed A-side work); a persistent launch costs
-// its number of waves of tiles, a split launch one wave of clusters plus a
-// fixed allowance for the cross-CTA reduction.
+// Tile width, CTA pairs or single CTAs, and split-K factor.  A k-block of a
+// 128 x BN tile is costed BN + 96 (MMA work plus the fixed A-side work); a
+// persistent launch costs its number of waves of tiles, a split launch one
+// wave of clusters plus a fixed allowance for the cross-CTA reduction.
 Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap) {
     const int64_t nkb = (K + kBK - 1) / kBK;
-    Plan best{128, 1, 1, 1};
+    Plan best{128, 1, false, 1, 1, 1};
     double best_cost = 1e300;
     for (int bn : kTileWidths) {
         if (swap && bn != kBM) continue;  // tokens fill a 128-wide N side
@@ -696,7 +783,7 @@ Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap) {
         int split = 1;
         if (tiles < sms) {
             for (int s = 2; s <= kMaxSplit && s * 4 <= nkb; ++s) {
-                if (tiles * s > sms || tiles > active_clusters(dev, bn, s)) continue;
+                if (tiles * s > sms || tiles > active_clusters(dev, bn, false, s)) continue;
                 const double c = ((double)((nkb + s - 1) / s) + 8.0) * per_kb;
                 if (c < cost) {
                     cost = c;
@@ -706,7 +793,23 @@ Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap) {
         }
         if (cost < best_cost) {
             best_cost = cost;
-            best = Plan{bn, split, ta, tb};
+            best = Plan{bn, split, false, split > 1 ? tiles : std::min<int64_t>(tiles, sms), ta, tb};
+        }
+    }
+    if (!swap) {
+        for (int bn : kPairWidths) {
+            const int64_t pairs = active_clusters(dev, bn, true, 2);
+            if (pairs == 0) continue;
+            const int64_t ta = (M + 2 * kBM - 1) / (2 * kBM);
+            const int64_t tb = (N + bn - 1) / bn;
+            const int64_t tiles = ta * tb;
+            const double per_kb = bn + 96.0;
+            const double waves = (double)((tiles + pairs - 1) / pairs);
+            const double cost = (waves * (double)nkb * kPairCost + 4.0) * per_kb;
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = Plan{bn, 1, true, std::min<int64_t>(tiles, pairs), ta, tb};
+            }
         }
     }
     return best;
@@ -739,10 +842,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace tc
 
-cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k) {
+cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k, int* pair) {
     if (M <= kW8A8DecodeMaxM) {
         *tile_n = 0;
         *split_k = 0;
+        *pair = 0;
         return cudaSuccess;
     }
     int dev = 0;
@@ -752,6 +856,7 @@ cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int
     const Plan plan = choose_plan(dev, M, N, K, sms, M <= kBM);
     *tile_n = plan.bn;
     *split_k = plan.split;
+    *pair = plan.pair ? 1 : 0;
     return cudaSuccess;
 }
 
@@ -783,16 +888,18 @@ cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t
     p.rows_a = p.swap ? N : M;
     p.rows_b = p.swap ? M : N;
     p.tmem_cols = pow2_cols(2 * p.bn);  // two fp32 chunk buffers
+    const int wgt_box = p.swap ? kBM : (plan.pair ? p.bn / 2 : p.bn);
     CUtensorMap map_tok, map_wgt;
-    if (!make_map_f16(&map_tok, x16, M, K) || !make_map_i8(&map_wgt, qw, N, K, p.bn)) return cudaErrorInvalidValue;
-    const int64_t tiles = p.tiles_a * p.tiles_b;
-    // split: one tile per cluster; otherwise persistent, one CTA per SM
-    const int64_t grid = p.split > 1 ? tiles * p.split : std::min<int64_t>(tiles, env.sm_count);
-    const dim3 cluster = p.split > 1 ? dim3((unsigned)p.split, 1, 1) : kNoCluster;
-    return with_bn(p.bn, [&](auto w) {
+    if (!make_map_f16(&map_tok, x16, M, K) || !make_map_i8(&map_wgt, qw, N, K, wgt_box)) return cudaErrorInvalidValue;
+    // pairs and split-K run clusters; otherwise one CTA per SM, persistent
+    const int csize = plan.pair ? 2 : plan.split;
+    const int64_t grid = plan.units * csize;
+    const dim3 cluster = csize > 1 ? dim3((unsigned)csize, 1, 1) : kNoCluster;
+    return with_cfg(p.bn, plan.pair, [&](auto w, auto pr) {
         constexpr int BN = decltype(w)::value;
-        return launch_kernel(w8a8_fused_kernel<BN>, dim3((unsigned)grid), dim3(kThreads), FusedCfg<BN>::kSmemBytes,
-                             env.stream, cluster, map_tok, map_wgt, p);
+        constexpr bool PAIR = decltype(pr)::value;
+        return launch_kernel(w8a8_fused_kernel<BN, PAIR>, dim3((unsigned)grid), dim3(kThreads),
+                             FusedCfg<BN, PAIR>::kSmemBytes, env.stream, cluster, map_tok, map_wgt, p);
     });
 }
 

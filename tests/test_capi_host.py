@@ -141,11 +141,13 @@ def test_valid_call_without_device_reports_no_device(lib):
 
 def test_w8a8_plan_argument_errors(lib):
     import ctypes
-    a, b = ctypes.c_int32(0), ctypes.c_int32(0)
+    a, b, c = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    ra, rb, rc = ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)
     f = lib.i8ql_w8a8_plan
-    assert f(256, 512, 40, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_UNSUPPORTED
-    assert f(256, 0, 64, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_INVALID_ARG
-    assert f(-1, 16, 64, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_INVALID_ARG
-    assert f(256, 16, 64, None, ctypes.byref(b)) == capi.I8QL_ERR_INVALID_ARG
+    assert f(256, 512, 40, ra, rb, rc) == capi.I8QL_ERR_UNSUPPORTED
+    assert f(256, 0, 64, ra, rb, rc) == capi.I8QL_ERR_INVALID_ARG
+    assert f(-1, 16, 64, ra, rb, rc) == capi.I8QL_ERR_INVALID_ARG
+    assert f(256, 16, 64, None, rb, rc) == capi.I8QL_ERR_INVALID_ARG
+    assert f(256, 16, 64, ra, rb, None) == capi.I8QL_ERR_INVALID_ARG
     if not torch.cuda.is_available():
-        assert f(256, 16, 64, ctypes.byref(a), ctypes.byref(b)) == capi.I8QL_ERR_NO_DEVICE
+        assert f(256, 16, 64, ra, rb, rc) == capi.I8QL_ERR_NO_DEVICE

@@ -236,14 +236,17 @@ def test_w8a8_qwen3_4b_prefill_sampled(shape, m):
 # M, N and K edges.
 PLAN_SHAPES = [(65, 640, 9728), (100, 2560, 2560), (128, 200, 12288), (129, 2560, 9728), (256, 512, 4096),
                (300, 1000, 4160), (512, 6144, 2560), (1024, 2560, 2560), (2048, 6144, 2560),
-               (2048, 19456, 2560), (4096, 2560, 2560), (777, 3000, 1040)]
+               (2048, 19456, 2560), (4096, 2560, 2560), (777, 3000, 1040), (512, 4096, 4096),
+               (512, 2560, 2560), (512, 2560, 9728), (128, 19456, 2560)]
 
 
 def test_w8a8_plans_cover_tile_widths_and_split_k():
     plans = {capi.i8ql_w8a8_plan(m, n, k) for m, n, k in PLAN_SHAPES}
-    assert {bn for bn, _ in plans} >= {128, 160, 192, 224, 256}, plans
-    assert any(s > 1 for _, s in plans) and any(s == 1 for _, s in plans), plans
-    assert capi.i8ql_w8a8_plan(64, 4096, 4096) == (0, 0)
+    assert {bn for bn, _, pair in plans if not pair} >= {128, 160, 192, 256}, plans
+    assert {bn for bn, _, pair in plans if pair} == {128, 192, 256}, plans
+    assert any(s > 1 for _, s, _ in plans) and any(s == 1 and not pair for _, s, pair in plans), plans
+    assert all(s == 1 for _, s, pair in plans if pair), plans
+    assert capi.i8ql_w8a8_plan(64, 4096, 4096) == (0, 0, 0)
 
 
 @pytest.mark.parametrize("m,n,k", PLAN_SHAPES)
