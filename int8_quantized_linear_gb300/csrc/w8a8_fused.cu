@@ -87,16 +87,18 @@ constexpr int kAuxRegs = 80;
 static_assert(256 * kEpiRegs + 256 * kAuxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch allocation");
 constexpr int kSmemOptin = 232448;  // largest dynamic shared memory of one CTA (227 KiB)
 constexpr int kMaxStages8 = 8;
-constexpr int kMaxStages16 = 4;
-constexpr int kTokStages = 4;
+constexpr int kMaxStagesOp = 4;
 constexpr int kCtlBytes = 5120;  // barriers + two sets of staged epilogue parameters
 
 // Shared-memory rings of one CTA for tile width BN (all stages 1024-byte
 // aligned), with W = BN weight rows per CTA, or BN / 2 for a CTA pair:
-//   tokens: fp16, 128 rows x 64 k, 128-byte swizzle (TMA writes the layout
-//     the MMA reads);
-//   weights fp16: W rows x 64 k, same layout (written by the converters);
-//   weights int8: W rows x 64 k, 64 bytes per row (TMA).
+//   operand stages, each the two MMA operands of one k-block:
+//     tokens: fp16, 128 rows x 64 k, 128-byte swizzle (TMA writes the
+//       layout the MMA reads);
+//     weights fp16: W rows x 64 k, same layout (written by the converters);
+//   weight stages: int8, W rows x 64 k, 64 bytes per row (TMA).
+// One full and one empty barrier per operand stage: the MMA issuer waits
+// once and commits once per k-block.
 // The weights are the BN side, or with swapped operands the 128-row side
 // (swap only uses BN = 128, never pairs).
 template <int BN, bool PAIR>
@@ -106,11 +108,13 @@ struct FusedCfg {
     static constexpr int kTokStage = kBM * kBK * 2;
     static constexpr int kStage16 = kWRows * kBK * 2;
     static constexpr int kStage8 = kWRows * kBK;
-    static constexpr int kStages16 = kWRows <= 128 ? 4 : 3;
-    static constexpr int kFixed = kTokStages * kTokStage + kStages16 * kStage16;
+    static constexpr int kOpStage = kTokStage + kStage16;
+    // deeper operand rings measured no faster: the main loop is bound by
+    // throughput, not by load latency
+    static constexpr int kStagesOp = kWRows <= 128 ? 4 : 3;
+    static constexpr int kFixed = kStagesOp * kOpStage;
     static constexpr int kFree = kSmemOptin - 1024 /*alignment slack*/ - kCtlBytes - kFixed;
     static constexpr int kStages8 = kFree / kStage8 < kMaxStages8 ? kFree / kStage8 : kMaxStages8;
-    static constexpr int kW16Off = kTokStages * kTokStage;
     static constexpr int kW8Off = kFixed;
     static constexpr int kStageBytes = kFixed + kStages8 * kStage8;
     static constexpr int kSmemBytes = kStageBytes + 1024 + kCtlBytes;
@@ -118,7 +122,7 @@ struct FusedCfg {
     static constexpr int kGroupsPerWarp = (kGroups + kTeamWarps - 1) / kTeamWarps;
     static constexpr int kPartStride = BN + 4;  // split-K partial tile row (int32), padded against bank conflicts
     static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
-    static_assert(kStages8 >= 3 && kStages16 <= kMaxStages16, "ring depths");
+    static_assert(kStages8 >= 3 && kStagesOp <= kMaxStagesOp, "ring depths");
     static_assert(kStage16 % 1024 == 0 && kStage8 % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(kBM * kPartStride * 4 <= kStageBytes, "split-K partial tile must fit the stages");
     static_assert(kWRows % 8 == 0, "weight rows fill whole swizzle atoms");
@@ -136,12 +140,10 @@ struct EpiParams {
 };
 
 struct Ctl {
-    uint64_t tok_full[kTokStages];    // the token TMA landed a stage
-    uint64_t tok_empty[kTokStages];   // the MMA is done with a token stage
+    uint64_t op_full[kMaxStagesOp];   // token TMA landed and the converters filled an operand stage
+    uint64_t op_empty[kMaxStagesOp];  // the MMA is done with an operand stage
     uint64_t w8_full[kMaxStages8];    // the weight TMA landed an int8 stage
     uint64_t w8_empty[kMaxStages8];   // a converter team is done with an int8 stage
-    uint64_t w16_full[kMaxStages16];  // a converter team filled an fp16 weight stage
-    uint64_t w16_empty[kMaxStages16]; // the MMA is done with an fp16 weight stage
     uint64_t acc_full[2];             // fp32 chunk accumulator buffers in TMEM
     uint64_t acc_empty[2];
     uint64_t drained;
@@ -262,16 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const W8A8Params p) {
     using Cfg = FusedCfg<BN, PAIR>;
     constexpr int S8 = Cfg::kStages8;
-    constexpr int S16 = Cfg::kStages16;
-    constexpr int ST = kTokStages;
+    constexpr int SO = Cfg::kStagesOp;
     constexpr int kHalf = BN / 2;  // columns per epilogue warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + Cfg::kStageBytes);
     int32_t* part = reinterpret_cast<int32_t*>(smem);  // split-K partial tile (after the main loop)
-    const uint32_t tok_base = smem_u32(smem);
-    const uint32_t w16_base = tok_base + Cfg::kW16Off;
-    const uint32_t w8_base = tok_base + Cfg::kW8Off;
+    // operand stage s: tokens at op_base + s * kOpStage, fp16 weights
+    // kTokStage bytes after them
+    const uint32_t op_base = smem_u32(smem);
+    const uint32_t w8_base = op_base + Cfg::kW8Off;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -298,17 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto leader_addr = [&](uint64_t* bar) -> uint32_t { return PAIR ? mapa(smem_u32(bar), 0) : smem_u32(bar); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < ST; ++s) {
-            mbar_init(&ctl->tok_full[s], kArrivers);
-            mbar_init(&ctl->tok_empty[s], 1);
+        for (int s = 0; s < SO; ++s) {
+            // per CTA of the pair: the token producer's arrive-with-bytes and
+            // one arrive per converter warp of the team
+            mbar_init(&ctl->op_full[s], kArrivers * (1 + kTeamWarps));
+            mbar_init(&ctl->op_empty[s], 1);
         }
         for (int s = 0; s < S8; ++s) {
             mbar_init(&ctl->w8_full[s], 1);
             mbar_init(&ctl->w8_empty[s], kTeamWarps);
-        }
-        for (int s = 0; s < S16; ++s) {
-            mbar_init(&ctl->w16_full[s], kArrivers * kTeamWarps);
-            mbar_init(&ctl->w16_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->acc_full[b], 1);
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t wgt_row = (int32_t)(p.swap ? ta * kBM : tb * BN + prank * Cfg::kWRows);
                     for (int kb = kb_lo; kb < kb_hi; ++kb, ++kg) {
                         const int s8 = (int)(kg % S8);
-                        const int st = (int)(kg % ST);
+                        const int so = (int)(kg % SO);
                         if (!mbar_wait_inline(&ctl->w8_empty[s8], (uint32_t)(((kg / S8) & 1) ^ 1), abort, p.err)) {
                             alive = false;
                             break;
@@ -437,20 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_expect_tx(&ctl->w8_full[s8], (uint32_t)Cfg::kStage8);
                         tma_load_2d(w8_base + (uint32_t)(s8 * Cfg::kStage8), &map_wgt, kb * kBK, wgt_row,
                                     &ctl->w8_full[s8]);
-                        if (!mbar_wait_inline(&ctl->tok_empty[st], (uint32_t)(((kg / ST) & 1) ^ 1), abort, p.err)) {
+                        if (!mbar_wait_inline(&ctl->op_empty[so], (uint32_t)(((kg / SO) & 1) ^ 1), abort, p.err)) {
                             alive = false;
                             break;
                         }
                         if constexpr (PAIR) {
                             // both halves of the token tile complete on the leader's barrier
-                            const uint32_t bar = leader_addr(&ctl->tok_full[st]);
+                            const uint32_t bar = leader_addr(&ctl->op_full[so]);
                             mbar_expect_tx_cluster(bar, (uint32_t)Cfg::kTokStage);
-                            tma_load_2d_pair(tok_base + (uint32_t)(st * Cfg::kTokStage), &map_tok, kb * kBK, tok_row,
+                            tma_load_2d_pair(op_base + (uint32_t)(so * Cfg::kOpStage), &map_tok, kb * kBK, tok_row,
                                              bar);
                         } else {
-                            mbar_expect_tx(&ctl->tok_full[st], (uint32_t)Cfg::kTokStage);
-                            tma_load_2d(tok_base + (uint32_t)(st * Cfg::kTokStage), &map_tok, kb * kBK, tok_row,
-                                        &ctl->tok_full[st]);
+                            mbar_expect_tx(&ctl->op_full[so], (uint32_t)Cfg::kTokStage);
+                            tma_load_2d(op_base + (uint32_t)(so * Cfg::kOpStage), &map_tok, kb * kBK, tok_row,
+                                        &ctl->op_full[so]);
                         }
                     }
                 }
@@ -483,16 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kb_first = kb_lo + c * kChunkKB;
                         const int kb_end = min(kb_hi, kb_first + kChunkKB);
                         for (int kb = kb_first; kb < kb_end; ++kb, ++kg) {
-                            const int st = (int)(kg % ST);
-                            const int s16 = (int)(kg % S16);
-                            if (!wait(&ctl->tok_full[st], (uint32_t)((kg / ST) & 1)) ||
-                                !wait(&ctl->w16_full[s16], (uint32_t)((kg / S16) & 1))) {
+                            const int so = (int)(kg % SO);
+                            if (!wait(&ctl->op_full[so], (uint32_t)((kg / SO) & 1))) {
                                 alive = false;
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t tok_st = tok_base + (uint32_t)(st * Cfg::kTokStage);
-                            const uint32_t wgt_st = w16_base + (uint32_t)(s16 * Cfg::kStage16);
+                            const uint32_t tok_st = op_base + (uint32_t)(so * Cfg::kOpStage);
+                            const uint32_t wgt_st = tok_st + Cfg::kTokStage;
                             const uint32_t a_st = p.swap ? wgt_st : tok_st;
                             const uint32_t b_st = p.swap ? tok_st : wgt_st;
 #pragma unroll
@@ -505,8 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 else
                                     mma_f16(d, ad, bd, idesc, acc);
                             }
-                            commit(&ctl->tok_empty[st]);
-                            commit(&ctl->w16_empty[s16]);
+                            commit(&ctl->op_empty[so]);
                         }
                         if (alive) commit(&ctl->acc_full[b]);
                     }
@@ -541,19 +538,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r_in = lane >> 2;
             const int j = lane & 3;
             const uint32_t src0 = w8_base + (uint32_t)(r_in * kBK + j * 16);
-            const uint32_t dst0 = w16_base + (uint32_t)(r_in * (kBK * 2));
+            const uint32_t dst0 = op_base + Cfg::kTokStage + (uint32_t)(r_in * (kBK * 2));
             const uint32_t c0 = (uint32_t)(((2 * j) ^ r_in) << 4);  // swizzled chunk offsets (row mod 8 = r_in)
             const uint32_t c1 = (uint32_t)(((2 * j + 1) ^ r_in) << 4);
             const int64_t per_tile = kb_hi - kb_lo;
             const int64_t total = (tiles > unit0 ? (tiles - unit0 + unit_step - 1) / unit_step : 0) * per_tile;
             for (int64_t kg = team; kg < total; kg += 2) {
                 const int s8 = (int)(kg % S8);
-                const int s16 = (int)(kg % S16);
+                const int so = (int)(kg % SO);
                 if (!warp_wait<true>(&ctl->w8_full[s8], (uint32_t)((kg / S8) & 1), abort, p.err) ||
-                    !warp_wait<true>(&ctl->w16_empty[s16], (uint32_t)(((kg / S16) & 1) ^ 1), abort, p.err))
+                    !warp_wait<true>(&ctl->op_empty[so], (uint32_t)(((kg / SO) & 1) ^ 1), abort, p.err))
                     break;
                 const uint32_t src = src0 + (uint32_t)(s8 * Cfg::kStage8);
-                const uint32_t dst = dst0 + (uint32_t)(s16 * Cfg::kStage16);
+                const uint32_t dst = dst0 + (uint32_t)(so * Cfg::kOpStage);
                 uint4 v[GPW];
 #pragma unroll
                 for (int i = 0; i < GPW; ++i) {
@@ -578,9 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (PAIR)
-                        mbar_arrive_cluster(leader_addr(&ctl->w16_full[s16]));
+                        mbar_arrive_cluster(leader_addr(&ctl->op_full[so]));
                     else
-                        mbar_arrive(&ctl->w16_full[s16]);
+                        mbar_arrive(&ctl->op_full[so]);
                     mbar_arrive(&ctl->w8_empty[s8]);
                 }
             }
