@@ -663,7 +663,7 @@ bool make_map_f16(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t 
 // The tile widths the kernel is built for (single CTAs), and those of CTA
 // pairs.
 constexpr int kTileWidths[] = {256, 224, 192, 160, 128};
-constexpr int kPairWidths[] = {256, 192, 128};
+constexpr int kPairWidths[] = {256, 224, 192, 160, 128};
 // A pair moves a 256 x BN tile through two SMs with half the shared-memory
 // operand traffic and conversion work per SM of a single-CTA 128 x BN tile;
 // its k-blocks are costed at this fraction of the single-CTA ones.
@@ -677,7 +677,9 @@ auto with_cfg(int bn, bool pair, F&& f) {
     if (pair) {
         switch (bn) {
             case 256: return f(integral_constant<int, 256>{}, integral_constant<bool, true>{});
+            case 224: return f(integral_constant<int, 224>{}, integral_constant<bool, true>{});
             case 192: return f(integral_constant<int, 192>{}, integral_constant<bool, true>{});
+            case 160: return f(integral_constant<int, 160>{}, integral_constant<bool, true>{});
             default: return f(integral_constant<int, 128>{}, integral_constant<bool, true>{});
         }
     }
