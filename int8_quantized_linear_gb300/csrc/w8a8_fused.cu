@@ -254,6 +254,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -523,24 +529,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
             // ---------------------------------------------------------- converters
             // Two teams of three warps take alternate k-blocks, so one team's
-            // waits and fences overlap the other team's conversions.  Lane l
-            // of a warp handles 16 int8 codes (k = 16j .. 16j+15, j = l % 4)
-            // of weight row 8g + l / 4 of 8-row group g; a warp issues all its
-            // loads before its conversions.  Reads are contiguous; the two
-            // 16-byte fp16 writes land in 16-byte chunks 2j and 2j+1 of the
-            // row, XOR-swizzled by the row index mod 8 (128-byte swizzle),
-            // which spreads every quarter-warp over all 32 banks.
+            // waits and fences overlap the other team's conversions; a warp
+            // issues all its loads before its conversions.
             constexpr int G = Cfg::kGroups;
-            constexpr int GPW = Cfg::kGroupsPerWarp;
             const int cw = warp - kConvWarp0;
             const int team = cw / kTeamWarps;
             const int tw = cw % kTeamWarps;
-            const int r_in = lane >> 2;
-            const int j = lane & 3;
-            const uint32_t src0 = w8_base + (uint32_t)(r_in * kBK + j * 16);
+            // A unit is 4 weight rows x 64 k: lane l converts the 8 codes
+            // k = 8c .. 8c+7 (c = l % 8) of row 4u + l / 8.  Each 8-lane group
+            // then stores one whole 128-byte row of the 128-byte swizzle (the
+            // 8 chunks land at c ^ (row % 8)) and reads 64 contiguous bytes,
+            // so neither access has bank conflicts.
+            constexpr int U = 2 * G;                                  // units per stage
+            constexpr int UPW = (U + kTeamWarps - 1) / kTeamWarps;  // per warp
+            const int r_in = lane >> 3;
+            const int c = lane & 7;
+            const uint32_t src0 = w8_base + (uint32_t)(r_in * kBK + c * 8);
             const uint32_t dst0 = op_base + Cfg::kTokStage + (uint32_t)(r_in * (kBK * 2));
-            const uint32_t c0 = (uint32_t)(((2 * j) ^ r_in) << 4);  // swizzled chunk offsets (row mod 8 = r_in)
-            const uint32_t c1 = (uint32_t)(((2 * j + 1) ^ r_in) << 4);
             const int64_t per_tile = kb_hi - kb_lo;
             const int64_t total = (tiles > unit0 ? (tiles - unit0 + unit_step - 1) / unit_step : 0) * per_tile;
             for (int64_t kg = team; kg < total; kg += 2) {
@@ -551,24 +556,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 const uint32_t src = src0 + (uint32_t)(s8 * Cfg::kStage8);
                 const uint32_t dst = dst0 + (uint32_t)(so * Cfg::kOpStage);
-                uint4 v[GPW];
+                uint2 v[UPW];
 #pragma unroll
-                for (int i = 0; i < GPW; ++i) {
-                    const int g = tw + i * kTeamWarps;
-                    if (g < G) v[i] = lds128(src + (uint32_t)(g * 8 * kBK));
+                for (int i = 0; i < UPW; ++i) {
+                    const int u = tw + i * kTeamWarps;
+                    if (u < U) v[i] = lds64(src + (uint32_t)(u * 4 * kBK));
                 }
 #pragma unroll
-                for (int i = 0; i < GPW; ++i) {
-                    const int g = tw + i * kTeamWarps;
-                    if (g < G) {
-                        uint32_t h[8];
+                for (int i = 0; i < UPW; ++i) {
+                    const int u = tw + i * kTeamWarps;
+                    if (u < U) {
+                        uint32_t h[4];
                         i8x4_to_f16(v[i].x, h[0], h[1]);
                         i8x4_to_f16(v[i].y, h[2], h[3]);
-                        i8x4_to_f16(v[i].z, h[4], h[5]);
-                        i8x4_to_f16(v[i].w, h[6], h[7]);
-                        const uint32_t rbase = dst + (uint32_t)(g * 8 * (kBK * 2));
-                        sts128(rbase + c0, h[0], h[1], h[2], h[3]);
-                        sts128(rbase + c1, h[4], h[5], h[6], h[7]);
+                        const int row7 = (4 * u + r_in) & 7;
+                        sts128(dst + (uint32_t)(u * 4 * (kBK * 2)) + (uint32_t)((c ^ row7) << 4), h[0], h[1], h[2],
+                               h[3]);
                     }
                 }
                 fence_proxy_async_smem();  // the tensor core reads these stores
