@@ -13,8 +13,9 @@ One step = one pass of the whole hot path over one batch of synthetic input:
     * the grouped W8A16 GEMM over 66 experts (64 routed, top-6, + 2 shared)
       for T = 8 decode tokens, gate_up [2816, 2048] then down [2048, 1408].
   prefill (--workload prefill; Qwen3-4B W8A8 prefill, bias on):
-    * for M in {128, 512, 2048, 4096} and each projection: activation
-      quantization and the W8A8 GEMM.
+    * for M in {128, 512, 2048, 4096} and each projection: the W8A8 linear
+      layer from bf16 activations (w8a8_linear: per-token activation
+      quantization fused with the W8A8 GEMM, two kernels per call).
 
 Every GEMM launch of a step reads its own copy of the int8 weights, and a
 step touches more than 1 GB, so no launch finds its weights in the 129 MB L2
@@ -88,7 +89,7 @@ def workload_name(kind):
                 "DeepSeek-MoE-16B grouped W8A16 (66 experts, top-6 + 2 shared, T=8; "
                 "gate_up 2816x2048, down 2048x1408)")
     return ("Qwen3-4B prefill W8A8 (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, down 9728->2560; "
-            "M in {128,512,2048,4096}; act quant + W8A8, bias on)")
+            "M in {128,512,2048,4096}; W8A8 linear from bf16 activations (per-token act quant fused), bias on)")
 
 
 def load_peaks():
@@ -105,7 +106,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "decode": {"w8a8": ["decode_gemm.cu"], "w8a16": ["decode_gemm.cu"], "grouped": ["decode_gemm.cu"],
                "quant_w": ["quant.cu"], "quant_x": ["quant.cu"]},
-    "prefill": {"w8a8": ["w8a8.cu", "w8a8_fused.cu", "tc_common.cuh"], "quant_x": ["quant.cu"]},
+    "prefill": {"w8a8": ["w8a8.cu", "w8a8_fused.cu", "tc_common.cuh", "quant.cu"]},
 }
 
 
@@ -175,17 +176,25 @@ class Workload:
             for mi, m in enumerate(ms):
                 x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=dev)
                 self.h2d.append((torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x), x))
-                qx = torch.empty((m, k), dtype=torch.int8, device=dev)
-                sx = torch.empty((m,), dtype=torch.float32, device=dev)
-                self.launches.append(Launch(
-                    "quant_x", lambda x=x, qx=qx, sx=sx: capi.quantize_act_per_token_int8(x, q=qx, scale=sx),
-                    bytes_quant(m, k), 0, f"quant_x {name} M={m}"))
                 y8 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
                 q8 = qs[mi * len(kinds)]
-                self.launches.append(Launch(
-                    "w8a8", lambda qx=qx, sx=sx, q=q8, s=s, b=bias, y=y8: capi.w8a8_gemm(qx, sx, q, s, bias=b, y=y),
-                    bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k, f"w8a8 {name} M={m}",
-                    gpu_kernels=1 if m <= W8A8_DECODE_MAX_M else 2))
+                if kind == "decode":
+                    qx = torch.empty((m, k), dtype=torch.int8, device=dev)
+                    sx = torch.empty((m,), dtype=torch.float32, device=dev)
+                    self.launches.append(Launch(
+                        "quant_x", lambda x=x, qx=qx, sx=sx: capi.quantize_act_per_token_int8(x, q=qx, scale=sx),
+                        bytes_quant(m, k), 0, f"quant_x {name} M={m}"))
+                    self.launches.append(Launch(
+                        "w8a8", lambda qx=qx, sx=sx, q=q8, s=s, b=bias, y=y8: capi.w8a8_gemm(qx, sx, q, s, bias=b, y=y),
+                        bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k, f"w8a8 {name} M={m}",
+                        gpu_kernels=1 if m <= W8A8_DECODE_MAX_M else 2))
+                else:
+                    # prefill: the linear layer from bf16 activations, with the
+                    # per-token quantization fused into the call
+                    self.launches.append(Launch(
+                        "w8a8", lambda x=x, q=q8, s=s, b=bias, y=y8: capi.w8a8_linear(x, q, s, bias=b, y=y),
+                        bytes_quant(m, k) + bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k,
+                        f"w8a8_linear {name} M={m}", gpu_kernels=2))
                 self.d2h.append((y8, torch.empty(y8.shape, dtype=y8.dtype, pin_memory=True)))
                 if kind == "decode":
                     y16 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)

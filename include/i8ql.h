@@ -106,6 +106,30 @@ i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const
                       int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * W8A8 linear layer from bf16 activations: per-token activation
+ * quantization fused into the W8A8 GEMM.
+ *
+ * Source: "feat(quantization): support compressed-tensors W8A8 and mixed
+ * modules", Design and Supported Execution Scheme (activations quantized per
+ * token, dynamically, at run time, feeding the int8 GEMM with the static
+ * per-channel weights) and "Day 6 -- Quantize It Yourself", The mechanism,
+ * block 5 (the per-forward activation quantization of W8A8).
+ *
+ * Computes exactly what quantize_act_per_token_int8(x) followed by w8a8_gemm
+ * computes (same codes, scales, accumulators and outputs), in fewer passes
+ * over memory: for M > 64 the quantization pass writes the codes in the form
+ * the tensor-core GEMM reads, so the GEMM needs no separate conversion pass.
+ * Inputs: x bf16 [M, K], qw int8 [N, K], sw fp32 [N], bias bf16 [N] or NULL.
+ * Outputs: y bf16 [M, N]; qx int8 [M, K] and sx fp32 [M] receive the token
+ * codes and scales when given (each may be NULL); acc_debug int32 [M, N] or
+ * NULL.  Takes a temporary stream-ordered workspace (at most 2*M*K + 4*M
+ * bytes).  Errors and argument rules as w8a8_gemm, with x checked like y.
+ */
+i8ql_status w8a8_linear(const i8ql_bf16* x, const int8_t* qw, const float* sw, const i8ql_bf16* bias,
+                        i8ql_bf16* y, int8_t* qx, float* sx, int32_t* acc_debug,
+                        int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * Weight-only W8A16 GEMM / GEMV (decode).
  *
  * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 5 (int8

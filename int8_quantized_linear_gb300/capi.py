@@ -36,6 +36,7 @@ SIGNATURES = {
     "quantize_act_per_token_int8": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "w8a8_gemm": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w8a8_gemm_noalloc": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w8a8_linear": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w8a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "grouped_w8a16_gemm": (_S, [_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P]),
     "i8ql_w8a8_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
@@ -128,6 +129,32 @@ def quantize_weight_per_channel_int8(w: torch.Tensor, q=None, scale=None, stream
 def quantize_act_per_token_int8(x: torch.Tensor, q=None, scale=None, stream=None):
     """int8 codes [M, K] and fp32 per-token scales [M] of bf16 x."""
     return _quant("quantize_act_per_token_int8", x, q, scale, stream)
+
+
+def w8a8_linear(x, qw, sw, bias=None, y=None, qx=None, sx=None, acc_debug=None, stream=None):
+    """bf16 y [M, N] = w8a8_gemm(quantize_act_per_token_int8(x), qw, sw, bias),
+    with the quantization fused into the call; qx / sx, when given, receive
+    the token codes and scales."""
+    m, k = x.shape
+    n = qw.shape[0]
+    _need(x, torch.bfloat16, (m, k), "x")
+    _need(qw, torch.int8, (n, k), "qw")
+    _need(sw, torch.float32, (n,), "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (n,), "bias")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=qw.device)
+    _need(y, torch.bfloat16, (m, n), "y")
+    if qx is not None:
+        _need(qx, torch.int8, (m, k), "qx")
+    if sx is not None:
+        _need(sx, torch.float32, (m,), "sx")
+    if acc_debug is not None:
+        _need(acc_debug, torch.int32, (m, n), "acc_debug")
+    st = lib().w8a8_linear(_ptr(x), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y), _ptr(qx), _ptr(sx),
+                           _ptr(acc_debug), m, n, k, _stream(stream))
+    _check(st, "w8a8_linear")
+    return y
 
 
 def w8a8_gemm(qx, sx, qw, sw, bias=None, y=None, acc_debug=None, stream=None):

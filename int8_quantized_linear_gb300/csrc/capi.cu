@@ -122,7 +122,7 @@ i8ql_status quantize_weight_per_channel_int8(const i8ql_bf16* w, int64_t N, int6
     LaunchEnv env;
     i8ql_status s;
     if (!launch_env(stream, &env, &s)) return s;
-    return from_cuda(launch_quant_rows(w, N, K, q, scale, env));
+    return from_cuda(launch_quant_rows(w, N, K, q, nullptr, scale, env));
 }
 
 i8ql_status quantize_act_per_token_int8(const i8ql_bf16* x, int64_t M, int64_t K, int8_t* q,
@@ -136,7 +136,7 @@ i8ql_status quantize_act_per_token_int8(const i8ql_bf16* x, int64_t M, int64_t K
     LaunchEnv env;
     i8ql_status s;
     if (!launch_env(stream, &env, &s)) return s;
-    return from_cuda(launch_quant_rows(x, M, K, q, scale, env));
+    return from_cuda(launch_quant_rows(x, M, K, q, nullptr, scale, env));
 }
 
 i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
@@ -158,6 +158,28 @@ i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const
     i8ql_status s;
     if (!launch_env(stream, &env, &s)) return s;
     return from_cuda(launch_w8a8(qx, sx, qw, sw, bias, y, acc_debug, M, N, K, env));
+}
+
+i8ql_status w8a8_linear(const i8ql_bf16* x, const int8_t* qw, const float* sw, const i8ql_bf16* bias,
+                        i8ql_bf16* y, int8_t* qx, float* sx, int32_t* acc_debug, int64_t M, int64_t N, int64_t K,
+                        void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_matrix(x, M));
+    I8QL_TRY(check_matrix(qw, N));
+    I8QL_TRY(check_vec(sw, N, 4));
+    if (bias != nullptr && !aligned(bias, 2)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_matrix(y, M));
+    if (qx != nullptr) I8QL_TRY(check_matrix(qx, M));
+    if (sx != nullptr && !aligned(sx, 4)) return I8QL_ERR_INVALID_ARG;
+    if (acc_debug != nullptr && !aligned(acc_debug, 16)) return I8QL_ERR_INVALID_ARG;
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_w8a8_linear(x, qw, sw, bias, y, qx, sx, acc_debug, M, N, K, env));
 }
 
 i8ql_status w8a16_gemm(const i8ql_bf16* x, const int8_t* qw, const float* sw, i8ql_bf16* y,

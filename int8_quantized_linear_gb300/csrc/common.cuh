@@ -89,7 +89,9 @@ bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status);
 // W8A8 up to this many tokens runs on the decode kernel (int8 mma.sync,
 // weight streaming); larger M runs on the tcgen05 kernel.
 constexpr int64_t kW8A8DecodeMaxM = 64;
-cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
+// Per-row quantization; the codes go to q (int8) and/or qh (fp16), either
+// nullable.
+cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
                               const LaunchEnv& env);
 cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw,
                          const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
@@ -112,6 +114,15 @@ cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, 
 cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t* qw, const float* sw,
                               const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
                               const LaunchEnv& env);
+// Activation quantization fused into W8A8 (see w8a8_linear): workspace
+// bytes, and the launch with a given workspace or with a stream-ordered one.
+size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K, bool have_qx, bool have_sx);
+cudaError_t launch_w8a8_linear_ws(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
+                                  uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                                  void* ws, const LaunchEnv& env);
+cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias, uint16_t* y,
+                               int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                               const LaunchEnv& env);
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                         const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                         int64_t K, const LaunchEnv& env);

@@ -86,6 +86,24 @@ __device__ __forceinline__ uint2 codes8(const uint4& v, const RowScale& rs) {
                       __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410));
 }
 
+// Eight int8 codes (two words) -> eight fp16 codes (four words), exact: the
+// biased byte u = q + 128 becomes the low mantissa byte of fp16 1024, and
+// 1152 is subtracted.
+__device__ __forceinline__ uint4 codes_to_f16(const uint2& c) {
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t u = (i == 0 ? c.x : c.y) ^ 0x80808080u;
+        uint32_t lo = __byte_perm(u, 0x64646464u, 0x5150);
+        uint32_t hi = __byte_perm(u, 0x64646464u, 0x5352);
+        asm("sub.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+        asm("sub.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+        h[2 * i] = lo;
+        h[2 * i + 1] = hi;
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
 __device__ __forceinline__ uint4 load_nc(const uint4* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -95,11 +113,13 @@ __device__ __forceinline__ uint4 load_nc(const uint4* p) {
 }
 
 // TPR threads own one row; VPT > 0 keeps up to VPT 8-element vectors per
-// thread in registers, VPT == 0 streams the row twice.
+// thread in registers, VPT == 0 streams the row twice.  The codes go to q
+// (int8) and/or qh (the same codes as fp16, for the tensor-core GEMM); either
+// may be null.
 template <int TPR, int VPT>
 __global__ void __launch_bounds__(kQuantThreads)
 quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
-                  int8_t* __restrict__ q, float* __restrict__ scale, int one_wave) {
+                  int8_t* __restrict__ q, uint16_t* __restrict__ qh, float* __restrict__ scale, int one_wave) {
     pdl_wait();
     if (one_wave) pdl_launch_dependents();
     constexpr int kRowsPerCta = kQuantThreads / TPR;
@@ -153,41 +173,46 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
     rs.r = __frcp_rn(s);
     rs.fast = isfinite(rs.r);
 
-    uint2* qp = reinterpret_cast<uint2*>(q + row * K);
+    uint2* qp = q ? reinterpret_cast<uint2*>(q + row * K) : nullptr;
+    uint4* hp = qh ? reinterpret_cast<uint4*>(qh + row * K) : nullptr;
+    auto put = [&](int64_t idx, const uint2& c) {
+        if (qp) qp[idx] = c;
+        if (hp) hp[idx] = codes_to_f16(c);
+    };
     if constexpr (VPT > 0) {
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t idx = lt + (int64_t)i * TPR;
-            if (idx < nvec) qp[idx] = codes8(v[i], rs);
+            if (idx < nvec) put(idx, codes8(v[i], rs));
         }
     } else {
         for (int64_t idx = lt; idx < nvec; idx += TPR) {
             const uint4 u = rp[idx];
-            qp[idx] = codes8(u, rs);
+            put(idx, codes8(u, rs));
         }
     }
 }
 
 template <int TPR, int VPT>
-cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
+cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
                        const LaunchEnv& env) {
     constexpr int kRowsPerCta = kQuantThreads / TPR;
     const int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
     // one wave: every CTA resident at once (at least 2 per SM fit, 256 threads each)
     const int one_wave = blocks <= 2LL * env.sm_count ? 1 : 0;
     return launch_kernel(quant_rows_kernel<TPR, VPT>, dim3((unsigned)blocks), dim3(kQuantThreads), 0, env.stream, kNoCluster,
-                         src, rows, K, q, s, one_wave);
+                         src, rows, K, q, qh, s, one_wave);
 }
 
 }  // namespace
 
-cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, float* s,
+cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
                               const LaunchEnv& env) {
     const int64_t nvec = K / 8;
-    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, s, env);
-    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, s, env);
-    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, s, env);
-    return launch_cfg<256, 0>(src, rows, K, q, s, env);
+    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, qh, s, env);
+    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, qh, s, env);
+    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, qh, s, env);
+    return launch_cfg<256, 0>(src, rows, K, q, qh, s, env);
 }
 
 }  // namespace i8ql

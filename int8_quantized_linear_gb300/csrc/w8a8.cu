@@ -1,7 +1,8 @@
 // W8A8 GEMM entry: routes a problem to the decode kernel (M <= 64, int8
 // mma.sync weight streaming, decode_gemm.cu) or, for larger M, to the
 // tcgen05 tensor-core kernel (w8a8_fused.cu) after one small pass that turns
-// the token codes into fp16 codes.
+// the token codes into fp16 codes.  The fused linear layer (w8a8_linear)
+// lets the activation quantization pass write those fp16 codes itself.
 //
 // Sources: "feat(quantization): support compressed-tensors W8A8 and mixed
 // modules", Design and Supported Execution Scheme, and "Day 6 -- Quantize It
@@ -71,6 +72,47 @@ cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, con
     e = launch_w8a8_ws(qx, sx, qw, sw, bias, y, acc, M, N, K, static_cast<uint16_t*>(ws), env);
     const cudaError_t f = cudaFreeAsync(ws, env.stream);
     return e != cudaSuccess ? e : f;
+}
+
+size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K, bool have_qx, bool have_sx) {
+    const size_t codes = M > kW8A8DecodeMaxM ? (size_t)M * (size_t)K * 2 : (have_qx ? 0 : (size_t)M * (size_t)K);
+    const size_t codes_padded = (codes + 255) / 256 * 256;
+    return codes_padded + (have_sx ? 0 : (size_t)M * 4);
+}
+
+cudaError_t launch_w8a8_linear_ws(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
+                                  uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                                  void* ws, const LaunchEnv& env) {
+    const size_t codes = M > kW8A8DecodeMaxM ? (size_t)M * (size_t)K * 2 : (qx ? 0 : (size_t)M * (size_t)K);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* s = sx ? sx : reinterpret_cast<float*>(w + (codes + 255) / 256 * 256);
+    cudaError_t e;
+    if (M <= kW8A8DecodeMaxM) {
+        // int8 codes for the decode kernel
+        int8_t* q8 = qx ? qx : reinterpret_cast<int8_t*>(w);
+        if ((e = launch_quant_rows(x, M, K, q8, nullptr, s, env)) != cudaSuccess) return e;
+        return launch_w8a8_decode(q8, s, qw, sw, bias, y, acc, M, N, K, env);
+    }
+    // fp16 codes for the tensor-core kernel, written by the quantization pass
+    // itself (and the int8 codes only if the caller asked for them)
+    uint16_t* x16 = reinterpret_cast<uint16_t*>(w);
+    if ((e = launch_quant_rows(x, M, K, qx, x16, s, env)) != cudaSuccess) return e;
+    return launch_w8a8_fused(x16, s, qw, sw, bias, y, acc, M, N, K, env);
+}
+
+cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias, uint16_t* y,
+                               int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                               const LaunchEnv& env) {
+    const size_t bytes = w8a8_linear_workspace_bytes(M, K, qx != nullptr, sx != nullptr);
+    void* ws = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (bytes > 0 && (e = cudaMallocAsync(&ws, bytes, env.stream)) != cudaSuccess) return e;
+    e = launch_w8a8_linear_ws(x, qw, sw, bias, y, qx, sx, acc, M, N, K, ws, env);
+    if (ws != nullptr) {
+        const cudaError_t f = cudaFreeAsync(ws, env.stream);
+        if (e == cudaSuccess) e = f;
+    }
+    return e;
 }
 
 }  // namespace i8ql

@@ -151,3 +151,20 @@ def test_w8a8_plan_argument_errors(lib):
     assert f(256, 16, 64, ra, rb, None) == capi.I8QL_ERR_INVALID_ARG
     if not torch.cuda.is_available():
         assert f(256, 16, 64, ra, rb, rc) == capi.I8QL_ERR_NO_DEVICE
+
+
+def test_w8a8_linear_argument_errors(lib):
+    f = lib.w8a8_linear
+    ok = (A, B, C, None, D, None, None, None, 8, 16, 64, None)
+    args = list(ok); args[10] = 40
+    assert f(*args) == capi.I8QL_ERR_UNSUPPORTED          # K % 16
+    args = list(ok); args[0] = None
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG          # x
+    args = list(ok); args[5] = A + 8
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG          # qx misaligned
+    args = list(ok); args[6] = A + 2
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG          # sx misaligned
+    args = list(ok); args[8] = 0
+    assert f(*args) == capi.I8QL_OK                        # M = 0: nothing to do
+    if not torch.cuda.is_available():
+        assert f(*ok) == capi.I8QL_ERR_NO_DEVICE

@@ -266,6 +266,38 @@ def test_w8a8_plan_shapes_sampled(m, n, k):
     assert np.array_equal(acc[rows, cols].astype(np.int64), ref_block)
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 256, 1024), (7, 300, 2064), (64, 513, 1040), (65, 640, 2560),
+                                   (128, 2560, 2560), (300, 1000, 4160), (2048, 2560, 2560)])
+def test_w8a8_linear_matches_quantize_then_gemm(m, n, k):
+    """The fused layer gives the two-call result bit for bit, and the oracle's
+    codes, scales, accumulators and outputs."""
+    x = synthetic.activations(m, k, m + k)
+    w = synthetic.weight(n, k, n + k)
+    qw_ref, sw_ref = oracle.quant_rows(util.bits(w))
+    qw, sw = dev(torch.from_numpy(qw_ref)), dev(torch.from_numpy(sw_ref))
+    bias_bits = util.bits(synthetic.bias(n, n)) if m % 2 else None
+    bias = None if bias_bits is None else util.from_bits(bias_bits, "cuda")
+    xd = dev(x)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    qx = torch.empty((m, k), dtype=torch.int8, device="cuda")
+    sx = torch.empty((m,), dtype=torch.float32, device="cuda")
+    acc = torch.empty((m, n), dtype=torch.int32, device="cuda")
+    capi.w8a8_linear(xd, qw, sw, bias=bias, y=y, qx=qx, sx=sx, acc_debug=acc)
+    y_only = capi.w8a8_linear(xd, qw, sw, bias=bias)  # no optional outputs
+    qx2, sx2 = capi.quantize_act_per_token_int8(xd)
+    y2 = capi.w8a8_gemm(qx2, sx2, qw, sw, bias=bias)
+    torch.cuda.synchronize()
+    assert torch.equal(qx, qx2) and torch.equal(sx, sx2)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y_only.view(torch.int16), y2.view(torch.int16))
+    qx_ref, sx_ref = oracle.quant_rows(util.bits(x))
+    assert np.array_equal(qx.cpu().numpy(), qx_ref) and np.array_equal(sx.cpu().numpy(), sx_ref)
+    pm, pn = _points(m, n, 3000, m * 7 + n)
+    ref_acc, _, ref_y = oracle.w8a8_points(qx_ref, sx_ref, qw_ref, sw_ref, bias_bits, pm, pn)
+    assert np.array_equal(acc.cpu().numpy()[pm, pn].astype(np.int64), ref_acc)
+    assert util.max_ulp_diff(util.bits(y)[pm, pn], ref_y) <= 1
+
+
 # ------------------------------------------------------------------ W8A16
 
 def gpu_w8a16(x_bf16, qw, sw):
