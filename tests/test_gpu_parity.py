@@ -231,6 +231,56 @@ def test_w8a8_qwen3_4b_prefill_sampled(shape, m):
     assert util.max_ulp_diff(y[pm, pn], ref_y) <= 1
 
 
+def gpu_w8a8_points(qx, sx, qw, sw, bias_bits, pm, pn):
+    """W8A8 on the GPU, returning only the sampled accumulators and outputs
+    (gathered on the device, so full-size outputs never cross to the host)."""
+    m, k = qx.shape
+    n = qw.shape[0]
+    y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty((m, n), dtype=torch.int32, device="cuda")
+    bias = None if bias_bits is None else util.from_bits(bias_bits, "cuda")
+    capi.w8a8_gemm(dev(torch.from_numpy(qx)), dev(torch.from_numpy(sx)), dev(torch.from_numpy(qw)),
+                   dev(torch.from_numpy(sw)), bias=bias, y=y, acc_debug=acc)
+    im, jn = dev(torch.from_numpy(pm)), dev(torch.from_numpy(pn))
+    a, yy = acc[im, jn].cpu().numpy(), util.bits(y[im, jn])
+    del y, acc
+    return a, yy
+
+
+@pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
+def test_w8a8_qwen3_4b_decode_full_size(shape):
+    """Qwen3-4B decode linears, M in {1, 4, 8}, bias off: the int8 mma.sync
+    decode kernel at full size, sampled against the oracle."""
+    n, k = synthetic.QWEN3_4B_SHAPES[shape]
+    qw, sw = oracle.quant_rows(util.bits(synthetic.weight(n, k, 1)))
+    for m in (1, 4, 8):
+        qx, sx = oracle.quant_rows(util.bits(synthetic.activations(m, k, 20 + m)))
+        pm, pn = _points(m, n, 3000, m * n)
+        acc, y = gpu_w8a8_points(qx, sx, qw, sw, None, pm, pn)
+        ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, None, pm, pn)
+        assert np.array_equal(acc.astype(np.int64), ref_acc)
+        assert util.max_ulp_diff(y, ref_y) <= 1
+
+
+QWEN3_8B_W8A8_CASES = [("qkv", 128), ("qkv", 2048), ("o", 2), ("o", 512), ("gate_up", 1), ("gate_up", 64),
+                       ("gate_up", 8192), ("down", 32), ("down", 8192)]
+
+
+@pytest.mark.parametrize("shape,m", QWEN3_8B_W8A8_CASES)
+def test_w8a8_qwen3_8b_sweep_sampled(shape, m):
+    """The Qwen3-8B sweep (K up to 12,288, M up to 8,192), bias on for even M:
+    sampled outputs and exact accumulators against the oracle."""
+    n, k = synthetic.QWEN3_8B_SHAPES[shape]
+    qw, sw = oracle.quant_rows(util.bits(synthetic.weight(n, k, 4)))
+    qx, sx = oracle.quant_rows(util.bits(synthetic.activations(m, k, 4)))
+    bias = util.bits(synthetic.bias(n, 4)) if m % 2 == 0 else None
+    pm, pn = _points(m, n, 3000, m + n)
+    acc, y = gpu_w8a8_points(qx, sx, qw, sw, bias, pm, pn)
+    ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, bias, pm, pn)
+    assert np.array_equal(acc.astype(np.int64), ref_acc)
+    assert util.max_ulp_diff(y, ref_y) <= 1
+
+
 # Shapes that drive the tensor-core kernel through every tile width and
 # through split-K clusters (deep K, few tiles), swapped and not, with ragged
 # M, N and K edges.
