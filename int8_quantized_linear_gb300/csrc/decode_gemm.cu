@@ -307,18 +307,34 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
 
         {
             // main loop: full k-steps through a kStages-deep register ring
+            // of weights.  For W8A8 with up to 16 tokens the token operand
+            // (an L1/L2 hit that still queues behind the weight stream) is
+            // loaded one k-step ahead (measured: W8A16, whose ring already
+            // fills the register budget, and wider token tiles lose by it).
+            constexpr bool kXAhead = OP == Op::kW8A8 && NT <= 2;
             WeightRegs<MT> ring[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s)
                 if (s < main_count) load_w(ring[s], s);
+            uint32_t xb[NT][kXW];
+            if constexpr (kXAhead) load_x(xb, 0, main_count > 0);
             for (int i0 = 0; i0 < main_count; i0 += kStages) {
 #pragma unroll
                 for (int s = 0; s < kStages; ++s) {
                     const int i = i0 + s;
                     if (i < main_count) {
-                        uint32_t xb[NT][kXW];
-                        load_x(xb, i, true);
-                        mma_step(ring[s], xb);
+                        if constexpr (kXAhead) {
+                            uint32_t xn[NT][kXW];
+                            load_x(xn, i + 1, i + 1 < main_count);
+                            mma_step(ring[s], xb);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                                for (int q = 0; q < kXW; ++q) xb[nt][q] = xn[nt][q];
+                        } else {
+                            load_x(xb, i, true);
+                            mma_step(ring[s], xb);
+                        }
                         if (i + kStages < main_count) load_w(ring[s], i + kStages);
                     }
                 }
@@ -360,14 +376,31 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
             part[0][i] = s;
         }
         // Publish to the cluster, then each rank finishes a slice of the tile.
-        cluster.sync();
+        // (A one-CTA cluster needs only a CTA barrier: the release semantics
+        // of a cluster barrier would also wait for earlier global stores.)
+        if (S == 1)
+            __syncthreads();
+        else
+            cluster.sync();
         const int total = nt_active * 8 * kRows;
         const int per = (total + S - 1) / S;
         const int i_begin = rank * per;
         const int i_end = min(total, i_begin + per);
         for (int i = i_begin + (int)threadIdx.x; i < i_end; i += kThreads) {
-            Acc s = Acc(0);
-            for (int r = 0; r < S; ++r) s += cluster.map_shared_rank(&part[0][0], r)[i];
+            Acc s;
+            if (S == 1) {
+                s = part[0][i];
+            } else {
+                // all peers' loads in flight before the rank-ordered sum
+                Acc v[kMaxClusterSplit];
+#pragma unroll
+                for (int r = 0; r < kMaxClusterSplit; ++r)
+                    v[r] = r < S ? cluster.map_shared_rank(&part[0][0], r)[i] : Acc(0);
+                s = v[0];
+#pragma unroll
+                for (int r = 1; r < kMaxClusterSplit; ++r)
+                    if (r < S) s += v[r];
+            }
             const int row = i % kRows;
             const int tok = i / kRows;
             const int64_t n = n0 + row;
@@ -383,7 +416,13 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
                 }
             }
         }
-        cluster.sync();  // peers are done reading this CTA's shared memory
+        // Peers are done reading this CTA's shared memory (their loads have
+        // returned: the values are summed).  A relaxed arrive does not wait
+        // for this thread's output stores to drain.
+        if (S == 1)
+            __syncthreads();
+        else
+            asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
     }
 }
 
