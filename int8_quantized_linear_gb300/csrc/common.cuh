@@ -44,6 +44,14 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // wave, so early dependents never take SM slots this grid still needs.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Warms L2 with `bytes` bytes at p (multiple of 16, 16-byte aligned).  Safe
+// before pdl_wait() even if the previous grid writes those bytes: L2 is the
+// point of coherence, so a line written later is updated there, and the
+// loads after pdl_wait() read through it.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // cudaLaunchKernelEx with programmatic stream serialization and, when
 // cluster.x > 0, thread-block clusters of the given shape.
 template <typename... KArgs, typename... Args>

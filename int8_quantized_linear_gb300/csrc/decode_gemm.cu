@@ -138,27 +138,33 @@ struct WeightRegs {
     uint4 r[MT][2];  // rows g and g+8 of each 16-row m-tile
 };
 
-// Depth of the per-lane register ring of weight loads: while one k-step is
-// converted and multiplied, the next stages - 1 are in flight (measured best:
-// 3 for W8A16, whose conversion needs more registers, 4 for W8A8).
-template <Op OP>
-struct RingStages {
-    static constexpr int value = OP == Op::kW8A16 ? 3 : 4;
+// Per-configuration tuning (each choice measured on the decode shapes):
+//  kStages  depth of the per-lane register ring of weight loads (while one
+//           k-step is converted and multiplied, the next kStages - 1 are in
+//           flight);
+//  kMinCtas CTAs per SM the register budget is sized for;
+//  kXAhead  the token operand (an L1/L2 hit that still queues behind the
+//           weight stream) is loaded one k-step ahead.
+// W8A8 streams without conversion and keeps a deep ring.  W8A16 with one
+// token tile trades ring depth for the token prefetch; its grouped form
+// (many short expert GEMMs) does better with more CTAs per SM instead.
+// Wider token tiles have no registers to spare for the prefetch.
+template <Op OP, int NT, bool GROUPED>
+struct Tuning {
+    static constexpr bool kW8A16One = OP == Op::kW8A16 && NT == 1;
+    static constexpr int kStages = OP == Op::kW8A8 ? 4 : (NT == 1 ? 2 : 3);
+    static constexpr int kMinCtas = (kW8A16One && GROUPED) ? 6 : (NT <= 2 ? 4 : (NT <= 4 ? 3 : 2));
+    static constexpr bool kXAhead = OP == Op::kW8A8 ? NT <= 2 : (kW8A16One && !GROUPED);
 };
-
-// Warms L2 with `bytes` bytes at p (multiple of 16, 16-byte aligned).
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // MT 16-row m-tiles per warp, NT 8-token n-tiles per pass.
 template <Op OP, int MT, int NT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
+__global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
     decode_gemm_kernel(const DecodeParams p) {
     using Acc = std::conditional_t<OP == Op::kW8A8, int32_t, float>;
     constexpr int kRows = 16 * MT;
     constexpr int kToks = 8 * NT;
-    constexpr int kStages = RingStages<OP>::value;
+    constexpr int kStages = Tuning<OP, NT, GROUPED>::kStages;
     __shared__ Acc part[kWarps][kToks * kRows];
 
     // Before waiting for the previous kernel, start streaming this CTA's
@@ -307,11 +313,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 4 : (NT <= 4 ? 3 : 2))
 
         {
             // main loop: full k-steps through a kStages-deep register ring
-            // of weights.  For W8A8 with up to 16 tokens the token operand
-            // (an L1/L2 hit that still queues behind the weight stream) is
-            // loaded one k-step ahead (measured: W8A16, whose ring already
-            // fills the register budget, and wider token tiles lose by it).
-            constexpr bool kXAhead = OP == Op::kW8A8 && NT <= 2;
+            // of weights (the token operand one k-step ahead if kXAhead)
+            constexpr bool kXAhead = Tuning<OP, NT, GROUPED>::kXAhead;
             WeightRegs<MT> ring[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s)

@@ -120,8 +120,6 @@ template <int TPR, int VPT>
 __global__ void __launch_bounds__(kQuantThreads)
 quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
                   int8_t* __restrict__ q, uint16_t* __restrict__ qh, float* __restrict__ scale, int one_wave) {
-    pdl_wait();
-    if (one_wave) pdl_launch_dependents();
     constexpr int kRowsPerCta = kQuantThreads / TPR;
     constexpr int kWarpsPerRow = TPR / 32;
     __shared__ float warp_max[kQuantThreads / 32];
@@ -131,6 +129,12 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
     const int lt = tid % TPR;
     const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + rloc;
     const bool valid = row < rows;
+    // A one-wave grid may start while the previous kernel still runs: pull
+    // the row into L2 meanwhile (the entry points bound K, so 2 * K fits the
+    // 32-bit size).
+    if (one_wave && valid && lt == 0) prefetch_l2(src + row * K, (uint32_t)(K * 2));
+    pdl_wait();
+    if (one_wave) pdl_launch_dependents();
     const int64_t nvec = K / 8;
     const uint4* rp = reinterpret_cast<const uint4*>(src) + (valid ? row : 0) * nvec;
 
@@ -208,9 +212,15 @@ cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, 
 
 cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
                               const LaunchEnv& env) {
+    // Threads per row and vectors per thread (measured on weight and
+    // activation shapes): many rows of moderate length go two warps to a
+    // row (more CTAs resident, no CTA barrier per row pair); long rows keep
+    // at most five vectors per thread, so that more CTAs fit on an SM.
     const int64_t nvec = K / 8;
     if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, qh, s, env);
+    if (nvec <= 64 * 6 && rows >= 4096) return launch_cfg<64, 6>(src, rows, K, q, qh, s, env);
     if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, qh, s, env);
+    if (nvec <= 256 * 5) return launch_cfg<256, 5>(src, rows, K, q, qh, s, env);
     if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, qh, s, env);
     return launch_cfg<256, 0>(src, rows, K, q, qh, s, env);
 }

@@ -95,7 +95,8 @@ def _adversarial_rows(rows, k, seed):
 
 
 @pytest.mark.parametrize("rows,k", [(1, 16), (3, 48), (33, 1040), (129, 4096), (7, 12288),
-                                    (5, 16384), (4, 16400), (2, 20000), (300, 256), (1000, 2560)])
+                                    (5, 16384), (4, 16400), (2, 20000), (300, 256), (1000, 2560),
+                                    (4100, 2992), (4096, 3072), (40, 9744), (5, 10240)])
 def test_quant_shapes(rows, k):
     check_quant(_adversarial_rows(rows, k, rows * 7 + k), True)
     check_quant(_adversarial_rows(rows, k, rows * 11 + k), False)
