@@ -207,11 +207,22 @@ i8ql_status w8a8_gemm_noalloc(const int8_t* qx, const float* sx, const int8_t* q
  * a 128-wide side), *split_k the number of CTAs of a thread-block cluster
  * that share one tile's k range (1: no split), and *cta_pair 1 when pairs of
  * CTAs on two SMs share 256-row tiles through one two-SM MMA (0: one CTA per
- * 128-row tile).  Same argument rules as w8a8_gemm; the outputs are HOST
- * pointers.
+ * 128-row tile), 2 when such pairs also run stream-K: every pair takes an
+ * equal share of all (tile, k-block) steps, and a tile cut between pairs is
+ * finished by the pair holding its first k-block, which adds the others'
+ * exact int32 partial sums (w8a8_gemm and w8a8_linear only: the stream-K
+ * workspace is part of their temporary allocation).  Same argument rules as
+ * w8a8_gemm; the outputs are HOST pointers.
  */
 i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k,
                            int32_t* cta_pair);
+
+/*
+ * The same report for w8a8_gemm_noalloc, which never runs stream-K (its
+ * fixed array holds only the token codes): *cta_pair is 0 or 1.
+ */
+i8ql_status i8ql_w8a8_noalloc_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k,
+                                   int32_t* cta_pair);
 
 /*
  * Waits for `stream`, then reads and clears the current device's sticky

@@ -40,6 +40,7 @@ SIGNATURES = {
     "w8a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "grouped_w8a16_gemm": (_S, [_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P]),
     "i8ql_w8a8_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
+    "i8ql_w8a8_noalloc_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
     "i8ql_get_device_error": (_S, [_P]),
     "i8ql_status_string": (ctypes.c_char_p, [_S]),
     "i8ql_version": (_S, []),
@@ -238,14 +239,23 @@ def grouped_w8a16_gemm(x, offsets, qw, sw, y=None, stream=None):
     return y
 
 
-def i8ql_w8a8_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
-    """(tile width, split-K factor, CTA-pair flag) w8a8_gemm uses for an
-    M x N x K problem on the current device; (0, 0, 0) in the decode range
-    (M <= 64)."""
+def _plan(fn_name: str, m: int, n: int, k: int) -> tuple[int, int, int]:
     tile_n, split_k, pair = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
-    _check(lib().i8ql_w8a8_plan(m, n, k, ctypes.byref(tile_n), ctypes.byref(split_k), ctypes.byref(pair)),
-           "i8ql_w8a8_plan")
+    _check(getattr(lib(), fn_name)(m, n, k, ctypes.byref(tile_n), ctypes.byref(split_k), ctypes.byref(pair)),
+           fn_name)
     return tile_n.value, split_k.value, pair.value
+
+
+def i8ql_w8a8_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
+    """(tile width, split-K factor, CTA-pair mode: 0 single CTAs, 1 pairs,
+    2 pairs with stream-K) w8a8_gemm uses for an M x N x K problem on the
+    current device; (0, 0, 0) in the decode range (M <= 64)."""
+    return _plan("i8ql_w8a8_plan", m, n, k)
+
+
+def i8ql_w8a8_noalloc_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
+    """The same for w8a8_gemm_noalloc (never stream-K)."""
+    return _plan("i8ql_w8a8_noalloc_plan", m, n, k)
 
 
 def i8ql_get_device_error(stream=None) -> int:

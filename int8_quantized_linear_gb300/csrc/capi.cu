@@ -238,7 +238,10 @@ i8ql_status i8ql_get_device_error(void* stream) {
     return I8QL_OK;
 }
 
-i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k, int32_t* cta_pair) {
+namespace {
+
+i8ql_status plan_query(int64_t M, int64_t N, int64_t K, bool allow_sk, int32_t* tile_n, int32_t* split_k,
+                       int32_t* cta_pair) {
     I8QL_TRY(check_rows(M));
     I8QL_TRY(check_k(K));
     if (N <= 0) return I8QL_ERR_INVALID_ARG;
@@ -248,11 +251,22 @@ i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int
     i8ql_status s;
     if (!launch_env(nullptr, &env, &s)) return s;
     int bn = 0, split = 0, pair = 0;
-    I8QL_TRY(from_cuda(w8a8_plan(M, N, K, env.sm_count, &bn, &split, &pair)));
+    I8QL_TRY(from_cuda(w8a8_plan(M, N, K, env.sm_count, allow_sk, &bn, &split, &pair)));
     *tile_n = bn;
     *split_k = split;
     *cta_pair = pair;
     return I8QL_OK;
+}
+
+}  // namespace
+
+i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k, int32_t* cta_pair) {
+    return plan_query(M, N, K, true, tile_n, split_k, cta_pair);
+}
+
+i8ql_status i8ql_w8a8_noalloc_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k,
+                                   int32_t* cta_pair) {
+    return plan_query(M, N, K, false, tile_n, split_k, cta_pair);
 }
 
 const char* i8ql_status_string(i8ql_status status) {
@@ -265,7 +279,7 @@ const char* i8ql_status_string(i8ql_status status) {
         case I8QL_ERR_BAD_OFFSETS: return "grouped offsets are not 0..T_total and non-decreasing";
         case I8QL_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
         case I8QL_ERR_WORKSPACE_LIMIT:
-            return "problem too large for the fixed workspace of w8a8_gemm_noalloc ((M + N) * K > 16 Mi for M > 64)";
+            return "problem too large for the fixed workspace of w8a8_gemm_noalloc (M * K > 16 Mi for M > 64)";
         default: return "unknown status";
     }
 }

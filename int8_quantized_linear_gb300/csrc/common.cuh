@@ -98,36 +98,40 @@ bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status);
 // weight streaming); larger M runs on the tcgen05 kernel.
 constexpr int64_t kW8A8DecodeMaxM = 64;
 // Per-row quantization; the codes go to q (int8) and/or qh (fp16), either
-// nullable.
+// nullable.  The kernel also sets the `nzero` words at `zero` to 0 (the
+// stream-K flags of the GEMM launched after it; nullable).
 cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
-                              const LaunchEnv& env);
+                              const LaunchEnv& env, unsigned* zero = nullptr, int nzero = 0);
 cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw,
                          const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
                          const LaunchEnv& env);
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                                int64_t K, const LaunchEnv& env);
-// Tile width (N side of the output tile), split-K factor and CTA-pair flag
-// the tcgen05 kernel uses for a W8A8 problem; all 0 when M is in the decode
-// range.
-cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k, int* pair);
-// Bytes of workspace launch_w8a8_ws needs (the fp16 token codes, M * K * 2,
-// when M exceeds the decode range; 0 otherwise).
+// Tile width (N side of the output tile), split-K factor and CTA-pair mode
+// (0 single CTAs, 1 pairs, 2 pairs with stream-K) the tcgen05 kernel uses
+// for a W8A8 problem, with or without a stream-K workspace; all 0 when M is
+// in the decode range.
+cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, bool allow_sk, int* tile_n, int* split_k, int* pair);
+// Bytes of the token workspace launch_w8a8_ws needs (the fp16 token codes,
+// M * K * 2, when M exceeds the decode range; 0 otherwise).
 size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// Stream-K workspace of the tensor-core kernel: its bytes (0 when the plan
+// does not use stream-K) and the number of 32-bit flags at its start that
+// must read zero when the kernel starts.
+cudaError_t w8a8_sk_workspace(int64_t M, int64_t N, int64_t K, int sms, size_t* bytes, int* flags);
+// W8A8 with a given token workspace `ws` and an optional stream-K workspace
+// (sk_ws, sk_bytes; null or too small: no stream-K).
 cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                            const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
-                           uint16_t* ws, const LaunchEnv& env);
+                           uint16_t* ws, void* sk_ws, size_t sk_bytes, const LaunchEnv& env);
 // tcgen05 W8A8 for M > 64: the token codes as fp16 (x16, [M, K]), the weight
-// codes as int8 (converted inside the kernel).
+// codes as int8 (converted inside the kernel).  Stream-K runs when the plan
+// wants it and sk_ws holds sk_bytes >= what w8a8_sk_workspace reports, its
+// flags zeroed by an earlier kernel of the stream.
 cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t* qw, const float* sw,
                               const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
-                              const LaunchEnv& env);
-// Activation quantization fused into W8A8 (see w8a8_linear): workspace
-// bytes, and the launch with a given workspace or with a stream-ordered one.
-size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K, bool have_qx, bool have_sx);
-cudaError_t launch_w8a8_linear_ws(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
-                                  uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
-                                  void* ws, const LaunchEnv& env);
+                              void* sk_ws, size_t sk_bytes, const LaunchEnv& env);
 cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias, uint16_t* y,
                                int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                const LaunchEnv& env);

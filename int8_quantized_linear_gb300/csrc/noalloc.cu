@@ -89,6 +89,7 @@ extern "C" i8ql_status w8a8_gemm_noalloc(const int8_t* qx, const float* sx, cons
     }
     uint16_t* scratch = nullptr;
     if ((s = scratch_address(dev, &scratch)) != I8QL_OK) return s;
-    const cudaError_t e = launch_w8a8_ws(qx, sx, qw, sw, bias, y, acc_debug, M, N, K, scratch, env);
+    // no stream-K: its workspace would not fit a fixed array
+    const cudaError_t e = launch_w8a8_ws(qx, sx, qw, sw, bias, y, acc_debug, M, N, K, scratch, nullptr, 0, env);
     return e == cudaSuccess ? I8QL_OK : I8QL_ERR_CUDA;
 }

@@ -119,7 +119,8 @@ __device__ __forceinline__ uint4 load_nc(const uint4* p) {
 template <int TPR, int VPT>
 __global__ void __launch_bounds__(kQuantThreads)
 quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
-                  int8_t* __restrict__ q, uint16_t* __restrict__ qh, float* __restrict__ scale, int one_wave) {
+                  int8_t* __restrict__ q, uint16_t* __restrict__ qh, float* __restrict__ scale, int one_wave,
+                  unsigned* __restrict__ zero, int nzero) {
     constexpr int kRowsPerCta = kQuantThreads / TPR;
     constexpr int kWarpsPerRow = TPR / 32;
     __shared__ float warp_max[kQuantThreads / 32];
@@ -135,6 +136,8 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
     if (one_wave && valid && lt == 0) prefetch_l2(src + row * K, (uint32_t)(K * 2));
     pdl_wait();
     if (one_wave) pdl_launch_dependents();
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += kQuantThreads) zero[i] = 0u;
     const int64_t nvec = K / 8;
     const uint4* rp = reinterpret_cast<const uint4*>(src) + (valid ? row : 0) * nvec;
 
@@ -199,30 +202,30 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
 
 template <int TPR, int VPT>
 cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
-                       const LaunchEnv& env) {
+                       const LaunchEnv& env, unsigned* zero, int nzero) {
     constexpr int kRowsPerCta = kQuantThreads / TPR;
     const int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
     // one wave: every CTA resident at once (at least 2 per SM fit, 256 threads each)
     const int one_wave = blocks <= 2LL * env.sm_count ? 1 : 0;
     return launch_kernel(quant_rows_kernel<TPR, VPT>, dim3((unsigned)blocks), dim3(kQuantThreads), 0, env.stream, kNoCluster,
-                         src, rows, K, q, qh, s, one_wave);
+                         src, rows, K, q, qh, s, one_wave, zero, nzero);
 }
 
 }  // namespace
 
 cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
-                              const LaunchEnv& env) {
+                              const LaunchEnv& env, unsigned* zero, int nzero) {
     // Threads per row and vectors per thread (measured on weight and
     // activation shapes): many rows of moderate length go two warps to a
     // row (more CTAs resident, no CTA barrier per row pair); long rows keep
     // at most five vectors per thread, so that more CTAs fit on an SM.
     const int64_t nvec = K / 8;
-    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, qh, s, env);
-    if (nvec <= 64 * 6 && rows >= 4096) return launch_cfg<64, 6>(src, rows, K, q, qh, s, env);
-    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, qh, s, env);
-    if (nvec <= 256 * 5) return launch_cfg<256, 5>(src, rows, K, q, qh, s, env);
-    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, qh, s, env);
-    return launch_cfg<256, 0>(src, rows, K, q, qh, s, env);
+    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 64 * 6 && rows >= 4096) return launch_cfg<64, 6>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 256 * 5) return launch_cfg<256, 5>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, qh, s, env, zero, nzero);
+    return launch_cfg<256, 0>(src, rows, K, q, qh, s, env, zero, nzero);
 }
 
 }  // namespace i8ql

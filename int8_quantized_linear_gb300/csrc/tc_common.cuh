@@ -35,6 +35,15 @@ struct W8A8Params {
     int split;  // CTAs of a cluster sharing one tile's k range (1: persistent, no split)
     uint32_t tmem_cols;
     unsigned* err;
+    // Stream-K (CTA pairs only): sk_units pairs share the tiles * nkb
+    // k-block iterations evenly; a pair whose range starts inside a tile
+    // parks that partial tile (int32, this CTA's 128 rows) in its slot of
+    // sk_part and counts it done in sk_flags (zeroed before the launch);
+    // the pair holding the tile's first k-block adds the parked partials.
+    int sk;
+    int64_t sk_units;
+    int32_t* sk_part;   // [sk_units][2][128 * bn] int32
+    unsigned* sk_flags; // [sk_units][2]
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -24,10 +24,15 @@
 namespace i8ql {
 namespace {
 
-// int8 codes -> fp16 codes (exact), grid-stride over 16-byte vectors.
+// int8 codes -> fp16 codes (exact), grid-stride over 16-byte vectors.  CTA
+// 0 also sets the `nzero` words at `zero` to 0 (the stream-K flags of the
+// GEMM launched next; nullable).
 __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ src, int64_t vecs,
-                                                        uint16_t* __restrict__ dst) {
+                                                        uint16_t* __restrict__ dst, unsigned* __restrict__ zero,
+                                                        int nzero) {
     pdl_wait();
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0u;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vecs; i += (int64_t)gridDim.x * blockDim.x) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
         uint32_t h[8];
@@ -41,6 +46,8 @@ __global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict
     }
 }
 
+size_t pad256(size_t n) { return (n + 255) / 256 * 256; }
+
 }  // namespace
 
 size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -51,63 +58,91 @@ size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                            const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
-                           uint16_t* ws, const LaunchEnv& env) {
+                           uint16_t* ws, void* sk_ws, size_t sk_bytes, const LaunchEnv& env) {
     if (M <= kW8A8DecodeMaxM) return launch_w8a8_decode(qx, sx, qw, sw, bias, y, acc, M, N, K, env);
+    size_t need = 0;
+    int flags = 0;
+    cudaError_t e = sk_ws ? w8a8_sk_workspace(M, N, K, env.sm_count, &need, &flags) : cudaSuccess;
+    if (e != cudaSuccess) return e;
+    if (need == 0 || sk_bytes < need) {
+        sk_ws = nullptr;
+        flags = 0;
+    }
     const int64_t vecs = M * K / 16;  // K is a multiple of 16
     const int64_t blocks = std::min<int64_t>((vecs + 255) / 256, (int64_t)env.sm_count * 8);
-    cudaError_t e = launch_kernel(i8_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, env.stream, kNoCluster, qx,
-                                  vecs, ws);
+    e = launch_kernel(i8_to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, env.stream, kNoCluster, qx, vecs, ws,
+                      static_cast<unsigned*>(sk_ws), flags);
     if (e != cudaSuccess) return e;
-    return launch_w8a8_fused(ws, sx, qw, sw, bias, y, acc, M, N, K, env);
+    return launch_w8a8_fused(ws, sx, qw, sw, bias, y, acc, M, N, K, sk_ws, sk_ws ? sk_bytes : 0, env);
 }
 
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw, const uint16_t* bias,
                         uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K, const LaunchEnv& env) {
     if (M <= kW8A8DecodeMaxM) return launch_w8a8_decode(qx, sx, qw, sw, bias, y, acc, M, N, K, env);
-    // Stream-ordered workspace for the fp16 token codes (from the device's
-    // default memory pool, returned when the stream reaches the free).
-    void* ws = nullptr;
-    cudaError_t e = cudaMallocAsync(&ws, w8a8_workspace_bytes(M, N, K), env.stream);
+    // One stream-ordered allocation (from the device's default memory pool,
+    // returned when the stream reaches the free): the fp16 token codes, then
+    // the stream-K workspace.
+    size_t sk = 0;
+    int flags = 0;
+    cudaError_t e = w8a8_sk_workspace(M, N, K, env.sm_count, &sk, &flags);
     if (e != cudaSuccess) return e;
-    e = launch_w8a8_ws(qx, sx, qw, sw, bias, y, acc, M, N, K, static_cast<uint16_t*>(ws), env);
+    const size_t tok = pad256(w8a8_workspace_bytes(M, N, K));
+    void* ws = nullptr;
+    if ((e = cudaMallocAsync(&ws, tok + sk, env.stream)) != cudaSuccess) return e;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    e = launch_w8a8_ws(qx, sx, qw, sw, bias, y, acc, M, N, K, reinterpret_cast<uint16_t*>(w), sk ? w + tok : nullptr,
+                       sk, env);
     const cudaError_t f = cudaFreeAsync(ws, env.stream);
     return e != cudaSuccess ? e : f;
 }
 
-size_t w8a8_linear_workspace_bytes(int64_t M, int64_t K, bool have_qx, bool have_sx) {
+namespace {
+
+// Workspace of the fused linear layer: the token codes (int8 for the decode
+// kernel unless the caller keeps them, fp16 for the tensor-core kernel), the
+// scales unless the caller keeps them, then the stream-K workspace.
+struct LinearLayout {
+    size_t codes, scales, sk;
+    int flags;
+    size_t total() const { return codes + scales + sk; }
+};
+
+cudaError_t linear_layout(int64_t M, int64_t N, int64_t K, bool have_qx, bool have_sx, int sms, LinearLayout* l) {
     const size_t codes = M > kW8A8DecodeMaxM ? (size_t)M * (size_t)K * 2 : (have_qx ? 0 : (size_t)M * (size_t)K);
-    const size_t codes_padded = (codes + 255) / 256 * 256;
-    return codes_padded + (have_sx ? 0 : (size_t)M * 4);
+    l->codes = pad256(codes);
+    l->scales = have_sx ? 0 : pad256((size_t)M * 4);
+    l->sk = 0;
+    l->flags = 0;
+    if (M <= kW8A8DecodeMaxM) return cudaSuccess;
+    return w8a8_sk_workspace(M, N, K, sms, &l->sk, &l->flags);
 }
 
-cudaError_t launch_w8a8_linear_ws(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
-                                  uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
-                                  void* ws, const LaunchEnv& env) {
-    const size_t codes = M > kW8A8DecodeMaxM ? (size_t)M * (size_t)K * 2 : (qx ? 0 : (size_t)M * (size_t)K);
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    float* s = sx ? sx : reinterpret_cast<float*>(w + (codes + 255) / 256 * 256);
-    cudaError_t e;
-    if (M <= kW8A8DecodeMaxM) {
-        // int8 codes for the decode kernel
-        int8_t* q8 = qx ? qx : reinterpret_cast<int8_t*>(w);
-        if ((e = launch_quant_rows(x, M, K, q8, nullptr, s, env)) != cudaSuccess) return e;
-        return launch_w8a8_decode(q8, s, qw, sw, bias, y, acc, M, N, K, env);
-    }
-    // fp16 codes for the tensor-core kernel, written by the quantization pass
-    // itself (and the int8 codes only if the caller asked for them)
-    uint16_t* x16 = reinterpret_cast<uint16_t*>(w);
-    if ((e = launch_quant_rows(x, M, K, qx, x16, s, env)) != cudaSuccess) return e;
-    return launch_w8a8_fused(x16, s, qw, sw, bias, y, acc, M, N, K, env);
-}
+}  // namespace
 
 cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias, uint16_t* y,
                                int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                const LaunchEnv& env) {
-    const size_t bytes = w8a8_linear_workspace_bytes(M, K, qx != nullptr, sx != nullptr);
+    LinearLayout l;
+    cudaError_t e = linear_layout(M, N, K, qx != nullptr, sx != nullptr, env.sm_count, &l);
+    if (e != cudaSuccess) return e;
     void* ws = nullptr;
-    cudaError_t e = cudaSuccess;
-    if (bytes > 0 && (e = cudaMallocAsync(&ws, bytes, env.stream)) != cudaSuccess) return e;
-    e = launch_w8a8_linear_ws(x, qw, sw, bias, y, qx, sx, acc, M, N, K, ws, env);
+    if (l.total() > 0 && (e = cudaMallocAsync(&ws, l.total(), env.stream)) != cudaSuccess) return e;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* s = sx ? sx : reinterpret_cast<float*>(w + l.codes);
+    if (M <= kW8A8DecodeMaxM) {
+        // int8 codes for the decode kernel
+        int8_t* q8 = qx ? qx : reinterpret_cast<int8_t*>(w);
+        e = launch_quant_rows(x, M, K, q8, nullptr, s, env);
+        if (e == cudaSuccess) e = launch_w8a8_decode(q8, s, qw, sw, bias, y, acc, M, N, K, env);
+    } else {
+        // fp16 codes for the tensor-core kernel, written by the quantization
+        // pass itself (and the int8 codes only if the caller asked for
+        // them); the same pass zeroes the stream-K flags
+        uint16_t* x16 = reinterpret_cast<uint16_t*>(w);
+        void* sk = l.sk ? w + l.codes + l.scales : nullptr;
+        e = launch_quant_rows(x, M, K, qx, x16, s, env, static_cast<unsigned*>(sk), l.flags);
+        if (e == cudaSuccess) e = launch_w8a8_fused(x16, s, qw, sw, bias, y, acc, M, N, K, sk, l.sk, env);
+    }
     if (ws != nullptr) {
         const cudaError_t f = cudaFreeAsync(ws, env.stream);
         if (e == cudaSuccess) e = f;

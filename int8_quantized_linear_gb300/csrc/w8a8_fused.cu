@@ -264,6 +264,74 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// The work of one unit (a CTA, a split-K cluster or a CTA pair) as a
+// sequence of segments, each a tile and a range of its k-blocks.
+// Persistent: tiles unit, unit + step, ... each over the unit's split-K
+// range [kb_lo, kb_hi).  Stream-K: the iterations [total * u / U,
+// total * (u + 1) / U) of the tile-major order (total = tiles * nkb), cut
+// at tile boundaries.  Every role walks the same sequence.
+struct Work {
+    int64_t cur, end, step;
+    int kb_lo, kb_hi, nkb;
+    bool sk;
+
+    __device__ __forceinline__ bool next(int64_t& tile, int& lo, int& hi) {
+        if (cur >= end) return false;
+        if (!sk) {
+            tile = cur;
+            lo = kb_lo;
+            hi = kb_hi;
+            cur += step;
+            return true;
+        }
+        tile = cur / nkb;
+        lo = (int)(cur - tile * nkb);
+        hi = (int)min((int64_t)nkb, end - tile * nkb);
+        cur = tile * nkb + hi;
+        return true;
+    }
+    // k-blocks of the whole sequence
+    __device__ __forceinline__ int64_t kblocks() const {
+        if (sk) return end > cur ? end - cur : 0;
+        return (end > cur ? (end - cur + step - 1) / step : 0) * (kb_hi - kb_lo);
+    }
+};
+
+// First stream-K iteration of unit u.
+__device__ __forceinline__ int64_t sk_first(int64_t total, int64_t u, int64_t units) { return total * u / units; }
+
+// (Stream-K runs on CTA pairs only; SK = false compiles it out.)
+template <bool SK>
+__device__ __forceinline__ Work make_work(const W8A8Params& p, int64_t unit0, int64_t unit_step, int kb_lo, int kb_hi,
+                                          int nkb) {
+    Work w;
+    w.nkb = nkb;
+    w.kb_lo = kb_lo;
+    w.kb_hi = kb_hi;
+    w.sk = SK && p.sk != 0;
+    w.step = unit_step;
+    const int64_t tiles = p.tiles_a * p.tiles_b;
+    if (w.sk) {
+        const int64_t total = tiles * nkb;
+        w.cur = sk_first(total, unit0, p.sk_units);
+        w.end = sk_first(total, unit0 + 1, p.sk_units);
+    } else {
+        w.cur = unit0;
+        w.end = tiles;
+    }
+    return w;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     w8a8_fused_kernel(const __grid_constant__ CUtensorMap map_tok, const __grid_constant__ CUtensorMap map_wgt,
@@ -295,7 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = prank == 0;
     const int kb_lo = (int)((int64_t)nkb * krank / S);
     const int kb_hi = (int)((int64_t)nkb * (krank + 1) / S);
-    const int nchunks = (kb_hi - kb_lo + kChunkKB - 1) / kChunkKB;
     const int64_t tiles = p.tiles_a * p.tiles_b;
     const int64_t unit0 = blockIdx.x / csize;
     const int64_t unit_step = gridDim.x / csize;
@@ -356,7 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t cg = 0;
         int64_t lt = 0;  // tiles of this CTA so far
         bool alive = true;
-        for (int64_t tile = unit0; tile < tiles && alive; tile += unit_step, ++lt) {
+        Work work = make_work<PAIR>(p, unit0, unit_step, kb_lo, kb_hi, nkb);
+        int64_t tile;
+        int seg_lo, seg_hi;
+        for (; alive && work.next(tile, seg_lo, seg_hi); ++lt) {
+            const int nch = (seg_hi - seg_lo + kChunkKB - 1) / kChunkKB;
             int64_t ta, tb;
             tile_coords(p, tile, ta, tb);
             // Stage this tile's scales and bias in parameter set lt % 2 once
@@ -372,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->epi_ready[eb]);
             if (!warp_wait<true>(&ctl->epi_ready[eb], eu, abort, p.err)) break;
-            for (int c = 0; c < nchunks; ++c, ++cg) {
+            for (int c = 0; c < nch; ++c, ++cg) {
                 const int b = (int)(cg & 1);
                 if (!warp_wait<true>(&ctl->acc_full[b], (uint32_t)((cg >> 1) & 1), abort, p.err)) {
                     alive = false;
@@ -411,6 +482,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[q] = make_int4(run[4 * q], run[4 * q + 1], run[4 * q + 2], run[4 * q + 3]);
                 continue;
             }
+            if (PAIR && p.sk && seg_lo > 0) {
+                // Stream-K, a later part of the tile: park it for the tile's
+                // owner (coalesced: consecutive lanes, consecutive rows) and
+                // count this thread's stores done with a release.
+                int4* slot = reinterpret_cast<int4*>(p.sk_part + (unit0 * 2 + prank) * (int64_t)(kBM * BN));
+#pragma unroll
+                for (int q = 0; q < kHalf / 4; ++q)
+                    __stcg(slot + (q * 2 + half) * kBM + row,
+                           make_int4(run[4 * q], run[4 * q + 1], run[4 * q + 2], run[4 * q + 3]));
+                red_release_gpu_add(p.sk_flags + unit0 * 2 + prank, 1u);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->epi_free[eb]);
+                continue;
+            }
+            if (PAIR && p.sk && seg_hi < nkb) {
+                // Stream-K, the tile's owner (it holds k-block 0): add the
+                // parts parked by the units after this one, in unit order.
+                // Those units run their part first, so this wait is short.
+                const int64_t total = tiles * nkb;
+                const int64_t tile_end = (tile + 1) * nkb;
+                for (int64_t q = unit0 + 1; q < p.sk_units && sk_first(total, q, p.sk_units) < tile_end; ++q) {
+                    const unsigned* f = p.sk_flags + q * 2 + prank;
+                    const uint64_t t0 = global_ns();
+                    while (true) {
+                        const bool seen = ld_acquire_gpu(f) >= (unsigned)(kEpiWarps * 32);
+                        if (__all_sync(0xffffffffu, seen)) break;
+                        const bool give_up =
+                            *reinterpret_cast<volatile int*>(abort) != 0 || global_ns() - t0 > kWaitLimitNs;
+                        if (__any_sync(0xffffffffu, give_up)) {
+                            alive = false;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                    if (!alive) {
+                        if (lane == 0) {
+                            record_fault(p.err, kErrBitTimeout);
+                            *reinterpret_cast<volatile int*>(abort) = 1;
+                        }
+                        break;
+                    }
+                    const int4* slot = reinterpret_cast<const int4*>(p.sk_part + (q * 2 + prank) * (int64_t)(kBM * BN));
+#pragma unroll
+                    for (int v = 0; v < kHalf / 4; ++v) {
+                        const int4 t = __ldcg(slot + (v * 2 + half) * kBM + row);
+                        run[4 * v] += t.x;
+                        run[4 * v + 1] += t.y;
+                        run[4 * v + 2] += t.z;
+                        run[4 * v + 3] += t.w;
+                    }
+                }
+                if (!alive) break;
+            }
 #pragma unroll
             for (int q = 0; q < kHalf / 8; ++q)
                 store_out<8>(p, ep, row_base, col_base, row, half * kHalf + 8 * q, run + 8 * q);
@@ -428,12 +552,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 int64_t kg = 0;  // k-blocks issued by this CTA
                 bool alive = true;
-                for (int64_t tile = unit0; tile < tiles && alive; tile += unit_step) {
+                Work work = make_work<PAIR>(p, unit0, unit_step, kb_lo, kb_hi, nkb);
+                int64_t tile;
+                int seg_lo, seg_hi;
+                while (alive && work.next(tile, seg_lo, seg_hi)) {
                     int64_t ta, tb;
                     tile_coords(p, tile, ta, tb);
                     const int32_t tok_row = (int32_t)(p.swap ? tb * kBM : ta * Cfg::kTileM + prank * kBM);
                     const int32_t wgt_row = (int32_t)(p.swap ? ta * kBM : tb * BN + prank * Cfg::kWRows);
-                    for (int kb = kb_lo; kb < kb_hi; ++kb, ++kg) {
+                    for (int kb = seg_lo; kb < seg_hi; ++kb, ++kg) {
                         const int s8 = (int)(kg % S8);
                         const int so = (int)(kg % SO);
                         if (!mbar_wait_inline(&ctl->w8_empty[s8], (uint32_t)(((kg / S8) & 1) ^ 1), abort, p.err)) {
@@ -476,8 +603,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int64_t kg = 0;  // k-blocks consumed
                 int64_t cg = 0;  // chunks accumulated
                 bool alive = true;
-                for (int64_t tile = unit0; tile < tiles && alive; tile += unit_step) {
-                    for (int c = 0; c < nchunks && alive; ++c, ++cg) {
+                Work work = make_work<PAIR>(p, unit0, unit_step, kb_lo, kb_hi, nkb);
+                int64_t tile;
+                int seg_lo, seg_hi;
+                while (alive && work.next(tile, seg_lo, seg_hi)) {
+                    const int nch = (seg_hi - seg_lo + kChunkKB - 1) / kChunkKB;
+                    for (int c = 0; c < nch && alive; ++c, ++cg) {
                         const int b = (int)(cg & 1);
                         // the epilogue must have drained this buffer's previous chunk
                         if (!wait(&ctl->acc_empty[b], (uint32_t)(((cg >> 1) & 1) ^ 1))) {
@@ -486,8 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t d = tmem + (uint32_t)(b * BN);
-                        const int kb_first = kb_lo + c * kChunkKB;
-                        const int kb_end = min(kb_hi, kb_first + kChunkKB);
+                        const int kb_first = seg_lo + c * kChunkKB;
+                        const int kb_end = min(seg_hi, kb_first + kChunkKB);
                         for (int kb = kb_first; kb < kb_end; ++kb, ++kg) {
                             const int so = (int)(kg % SO);
                             if (!wait(&ctl->op_full[so], (uint32_t)((kg / SO) & 1))) {
@@ -546,8 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c = lane & 7;
             const uint32_t src0 = w8_base + (uint32_t)(r_in * kBK + c * 8);
             const uint32_t dst0 = op_base + Cfg::kTokStage + (uint32_t)(r_in * (kBK * 2));
-            const int64_t per_tile = kb_hi - kb_lo;
-            const int64_t total = (tiles > unit0 ? (tiles - unit0 + unit_step - 1) / unit_step : 0) * per_tile;
+            const int64_t total = make_work<PAIR>(p, unit0, unit_step, kb_lo, kb_hi, nkb).kblocks();
             for (int64_t kg = team; kg < total; kg += 2) {
                 const int s8 = (int)(kg % S8);
                 const int so = (int)(kg % SO);
@@ -764,13 +894,27 @@ struct Plan {
     bool pair;
     int64_t units;  // CTAs (or clusters) the persistent grid runs
     int64_t tiles_a, tiles_b;
+    bool sk = false;  // stream-K over `units` pairs
 };
 
-// Tile width, CTA pairs or single CTAs, and split-K factor.  A k-block of a
-// 128 x BN tile is costed BN + 96 (MMA work plus the fixed A-side work); a
-// persistent launch costs its number of waves of tiles, a split launch one
-// wave of clusters plus a fixed allowance for the cross-CTA reduction.
-Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap) {
+// Stream-K fix-up (parking partial tiles, owners adding them, the extra
+// segment ends), as measured: about this many pair k-blocks per launch.
+constexpr int64_t kSkFixupKb = 40;
+
+// Bytes of the stream-K workspace of a plan: the flags (2 per pair, padded
+// to 256 bytes), then one int32 partial tile half (128 x BN) per CTA.
+size_t sk_flag_count(const Plan& plan) { return plan.sk ? (size_t)plan.units * 2 : 0; }
+size_t sk_bytes(const Plan& plan) {
+    if (!plan.sk) return 0;
+    return (sk_flag_count(plan) * 4 + 255) / 256 * 256 + (size_t)plan.units * 2 * kBM * plan.bn * 4;
+}
+
+// Tile width, CTA pairs or single CTAs, split-K factor, and stream-K.  A
+// k-block of a 128 x BN tile is costed BN + 96 (MMA work plus the fixed
+// A-side work); a persistent launch costs its number of waves of tiles, a
+// split launch one wave of clusters plus a fixed allowance for the cross-CTA
+// reduction, a stream-K launch its even share of k-blocks plus the fix-up.
+Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap, bool allow_sk) {
     const int64_t nkb = (K + kBK - 1) / kBK;
     Plan best{128, 1, false, 1, 1, 1};
     double best_cost = 1e300;
@@ -814,6 +958,28 @@ Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap) {
             }
         }
     }
+    if (!swap && allow_sk) {
+        // Stream-K on 256-wide pair tiles, for tiles that outnumber the
+        // pairs.  Measured with every SM busy, a pair k-block costs about
+        // the same at any tile width, so the alternative costs its fewest
+        // waves of whole tiles times nkb; stream-K costs an even share of
+        // all k-blocks plus the fix-up.
+        constexpr int bn = 256;
+        const int64_t pairs = active_clusters(dev, bn, true, 2);
+        const int64_t ta = (M + 2 * kBM - 1) / (2 * kBM);
+        const int64_t tiles = ta * ((N + bn - 1) / bn);
+        if (pairs >= 2 && tiles > pairs) {
+            int64_t whole = INT64_MAX;
+            for (int w : kPairWidths) {
+                const int64_t pw = active_clusters(dev, w, true, 2);
+                if (pw == 0) continue;
+                const int64_t tw = ta * ((N + w - 1) / w);
+                whole = std::min(whole, (tw + pw - 1) / pw * nkb);
+            }
+            const int64_t total = tiles * nkb;
+            if ((total + pairs - 1) / pairs + kSkFixupKb < whole) best = Plan{bn, 1, true, pairs, ta, tiles / ta, true};
+        }
+    }
     return best;
 }
 
@@ -844,7 +1010,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace tc
 
-cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k, int* pair) {
+cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, bool allow_sk, int* tile_n, int* split_k, int* pair) {
     if (M <= kW8A8DecodeMaxM) {
         *tile_n = 0;
         *split_k = 0;
@@ -855,16 +1021,30 @@ cudaError_t w8a8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = prepare_device(dev)) != cudaSuccess) return e;
-    const Plan plan = choose_plan(dev, M, N, K, sms, M <= kBM);
+    const Plan plan = choose_plan(dev, M, N, K, sms, M <= kBM, allow_sk);
     *tile_n = plan.bn;
     *split_k = plan.split;
-    *pair = plan.pair ? 1 : 0;
+    *pair = plan.sk ? 2 : (plan.pair ? 1 : 0);
+    return cudaSuccess;
+}
+
+cudaError_t w8a8_sk_workspace(int64_t M, int64_t N, int64_t K, int sms, size_t* bytes, int* flags) {
+    *bytes = 0;
+    *flags = 0;
+    if (M <= kBM) return cudaSuccess;  // swapped operands: no pairs, no stream-K
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare_device(dev)) != cudaSuccess) return e;
+    const Plan plan = choose_plan(dev, M, N, K, sms, false, true);
+    *bytes = sk_bytes(plan);
+    *flags = (int)sk_flag_count(plan);
     return cudaSuccess;
 }
 
 cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t* qw, const float* sw,
                               const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
-                              const LaunchEnv& env) {
+                              void* sk_ws, size_t sk_ws_bytes, const LaunchEnv& env) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -882,7 +1062,8 @@ cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t
     // For M <= 128, "swap AB": weights fill the 128-row MMA operand and the
     // tokens the N side (a 128-row box; the tensor map reads zeros past M).
     p.swap = M <= kBM ? 1 : 0;
-    const Plan plan = choose_plan(dev, M, N, K, env.sm_count, p.swap != 0);
+    Plan plan = choose_plan(dev, M, N, K, env.sm_count, p.swap != 0, sk_ws != nullptr);
+    if (plan.sk && sk_ws_bytes < sk_bytes(plan)) plan = choose_plan(dev, M, N, K, env.sm_count, p.swap != 0, false);
     p.bn = plan.bn;
     p.split = plan.split;
     p.tiles_a = plan.tiles_a;
@@ -890,6 +1071,14 @@ cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t
     p.rows_a = p.swap ? N : M;
     p.rows_b = p.swap ? M : N;
     p.tmem_cols = pow2_cols(2 * p.bn);  // two fp32 chunk buffers
+    if (plan.sk) {
+        // flags first (zeroed by the launch before this one), then the
+        // partial tiles
+        p.sk = 1;
+        p.sk_units = plan.units;
+        p.sk_flags = static_cast<unsigned*>(sk_ws);
+        p.sk_part = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(sk_ws) + (sk_flag_count(plan) * 4 + 255) / 256 * 256);
+    }
     const int wgt_box = p.swap ? kBM : (plan.pair ? p.bn / 2 : p.bn);
     CUtensorMap map_tok, map_wgt;
     if (!make_map_f16(&map_tok, x16, M, K) || !make_map_i8(&map_wgt, qw, N, K, wgt_box)) return cudaErrorInvalidValue;

@@ -139,11 +139,12 @@ def test_valid_call_without_device_reports_no_device(lib):
     assert lib.w8a16_gemm(A, B, C, D, 4, 16, 64, None) == capi.I8QL_ERR_NO_DEVICE
 
 
-def test_w8a8_plan_argument_errors(lib):
+@pytest.mark.parametrize("fn", ["i8ql_w8a8_plan", "i8ql_w8a8_noalloc_plan"])
+def test_w8a8_plan_argument_errors(lib, fn):
     import ctypes
     a, b, c = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
     ra, rb, rc = ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)
-    f = lib.i8ql_w8a8_plan
+    f = getattr(lib, fn)
     assert f(256, 512, 40, ra, rb, rc) == capi.I8QL_ERR_UNSUPPORTED
     assert f(256, 0, 64, ra, rb, rc) == capi.I8QL_ERR_INVALID_ARG
     assert f(-1, 16, 64, ra, rb, rc) == capi.I8QL_ERR_INVALID_ARG

@@ -147,14 +147,17 @@ def _codes(rows, k, seed, extreme=False):
     return g.integers(-127, 128, size=(rows, k)).astype(np.int8)
 
 
-def gpu_w8a8(qx, sx, qw, sw, bias_bits=None):
+def gpu_w8a8(qx, sx, qw, sw, bias_bits=None, noalloc=False):
     m, k = qx.shape
     n = qw.shape[0]
     ybuf, y = util.guarded((m, n), torch.int16, "cuda", 0x7F7F)
     abuf, acc = util.guarded((m, n), torch.int32, "cuda", -5)
     bias = None if bias_bits is None else util.from_bits(bias_bits, "cuda")
-    capi.w8a8_gemm(dev(torch.from_numpy(qx)), dev(torch.from_numpy(sx)), dev(torch.from_numpy(qw)),
-                   dev(torch.from_numpy(sw)), bias=bias, y=y.view(torch.bfloat16), acc_debug=acc)
+    args = (dev(torch.from_numpy(qx)), dev(torch.from_numpy(sx)), dev(torch.from_numpy(qw)), dev(torch.from_numpy(sw)))
+    if noalloc:
+        capi.w8a8_gemm_noalloc(*args, y.view(torch.bfloat16), bias=bias, acc_debug=acc)
+    else:
+        capi.w8a8_gemm(*args, bias=bias, y=y.view(torch.bfloat16), acc_debug=acc)
     torch.cuda.synchronize()
     assert util.guard_intact(ybuf, m * n, 0x7F7F) and util.guard_intact(abuf, m * n, -5)
     return acc.cpu().numpy(), y.cpu().numpy().view(np.uint16)
@@ -291,21 +294,40 @@ PLAN_SHAPES = [(65, 640, 9728), (100, 2560, 2560), (128, 200, 12288), (129, 2560
                (512, 2560, 2560), (512, 2560, 9728), (128, 19456, 2560)]
 
 
+# Shapes whose 256-wide pair tiles outnumber the pairs without filling whole
+# waves, deep enough in K for w8a8_gemm to run stream-K: tiles cut between
+# pairs at the k-block offsets the even split gives, with ragged M, N and K
+# edges.
+STREAM_K_SHAPES = [(2048, 2560, 9728), (4096, 2560, 9728), (2000, 2600, 9744), (1800, 2600, 6160)]
+
+
 def test_w8a8_plans_cover_tile_widths_and_split_k():
-    plans = {capi.i8ql_w8a8_plan(m, n, k) for m, n, k in PLAN_SHAPES}
+    # without a stream-K workspace (the fixed-array entry point)
+    plans = {capi.i8ql_w8a8_noalloc_plan(m, n, k) for m, n, k in PLAN_SHAPES}
     assert {bn for bn, _, pair in plans if not pair} >= {128, 160, 192, 256}, plans
     assert {bn for bn, _, pair in plans if pair} >= {160, 192, 224, 256}, plans
     assert any(s > 1 for _, s, _ in plans) and any(s == 1 and not pair for _, s, pair in plans), plans
-    assert all(s == 1 for _, s, pair in plans if pair), plans
+    assert all(s == 1 for _, s, pair in plans if pair) and all(pair in (0, 1) for _, _, pair in plans), plans
+    # with one: stream-K takes the shapes whose 256-wide pair tiles leave a
+    # wave of pairs partly idle, and runs 256-wide pair tiles only
+    plans = {capi.i8ql_w8a8_plan(m, n, k) for m, n, k in PLAN_SHAPES + STREAM_K_SHAPES}
+    assert any(pair == 2 for _, _, pair in plans) and any(pair == 1 for _, _, pair in plans), plans
+    assert all(bn == 256 and s == 1 for bn, s, pair in plans if pair == 2), plans
+    for m, n, k in STREAM_K_SHAPES:
+        assert capi.i8ql_w8a8_plan(m, n, k)[2] == 2, (m, n, k)
+    for m, n, k in PLAN_SHAPES:
+        if m <= 128:
+            assert capi.i8ql_w8a8_plan(m, n, k) == capi.i8ql_w8a8_noalloc_plan(m, n, k)
     assert capi.i8ql_w8a8_plan(64, 4096, 4096) == (0, 0, 0)
 
 
+@pytest.mark.parametrize("entry", ["gemm", "noalloc"])
 @pytest.mark.parametrize("m,n,k", PLAN_SHAPES)
-def test_w8a8_plan_shapes_sampled(m, n, k):
+def test_w8a8_plan_shapes_sampled(m, n, k, entry):
     qx, qw = _codes(m, k, m + 7 * k), _codes(n, k, n + 11 * k)
     sx, sw = _scales(m, m + 3, 0.01, 1.0), _scales(n, n + 4)
     bias = util.bits(synthetic.bias(n, n + 1)) if m % 2 else None
-    acc, y = gpu_w8a8(qx, sx, qw, sw, bias)
+    acc, y = gpu_w8a8(qx, sx, qw, sw, bias, noalloc=entry == "noalloc")
     pm, pn = _points(m, n, 4000, m * n + k)
     ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, bias, pm, pn)
     assert np.array_equal(acc[pm, pn].astype(np.int64), ref_acc)
@@ -315,6 +337,28 @@ def test_w8a8_plan_shapes_sampled(m, n, k):
     cols = slice(0, min(n, 300))
     ref_block = qx[rows].astype(np.int64) @ qw[cols].astype(np.int64).T
     assert np.array_equal(acc[rows, cols].astype(np.int64), ref_block)
+
+
+@pytest.mark.parametrize("m,n,k", STREAM_K_SHAPES)
+def test_w8a8_stream_k_exact(m, n, k):
+    """Stream-K: every accumulator equals the exact integer product (host
+    float64 matmul of the codes, exact below 2^53), whichever pair computed
+    each part of its tile; outputs match the oracle at sampled points and
+    the fixed-workspace entry point (no stream-K) bit for bit."""
+    qx, qw = _codes(m, k, 3 * m + k), _codes(n, k, 5 * n + k)
+    sx, sw = _scales(m, m + 9, 0.01, 1.0), _scales(n, n + 8)
+    bias = util.bits(synthetic.bias(n, n + 2)) if m % 2 else None
+    acc, y = gpu_w8a8(qx, sx, qw, sw, bias)
+    exact = qx.astype(np.float64) @ qw.astype(np.float64).T
+    assert np.array_equal(acc.astype(np.float64), exact), \
+        f"acc differs at {np.argwhere(acc.astype(np.float64) != exact)[:3].tolist()}"
+    pm, pn = _points(m, n, 3000, m + n + k)
+    ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, bias, pm, pn)
+    assert np.array_equal(acc[pm, pn].astype(np.int64), ref_acc)
+    assert util.max_ulp_diff(y[pm, pn], ref_y) <= 1
+    if m * k <= capi.I8QL_NOALLOC_MAX_ELEMENTS:
+        acc2, y2 = gpu_w8a8(qx, sx, qw, sw, bias, noalloc=True)
+        assert np.array_equal(acc2, acc) and np.array_equal(y2, y)
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 256, 1024), (7, 300, 2064), (64, 513, 1040), (65, 640, 2560),
