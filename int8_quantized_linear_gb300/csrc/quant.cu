@@ -29,16 +29,17 @@ constexpr int kQuantThreads = 256;
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Packed |a| max of two bf16 pairs: the magnitude of each half is the larger
+// magnitude (exact; the sign bit, an xor of the inputs', is ignored).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 __device__ __forceinline__ float absmax8(const uint4& v, float a) {
-    a = fmaxf(a, fabsf(lo_bf16(v.x)));
-    a = fmaxf(a, fabsf(hi_bf16(v.x)));
-    a = fmaxf(a, fabsf(lo_bf16(v.y)));
-    a = fmaxf(a, fabsf(hi_bf16(v.y)));
-    a = fmaxf(a, fabsf(lo_bf16(v.z)));
-    a = fmaxf(a, fabsf(hi_bf16(v.z)));
-    a = fmaxf(a, fabsf(lo_bf16(v.w)));
-    a = fmaxf(a, fabsf(hi_bf16(v.w)));
-    return a;
+    const uint32_t m = absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w));
+    return fmaxf(a, fmaxf(fabsf(lo_bf16(m)), fabsf(hi_bf16(m))));
 }
 
 // The code of v is rint(fl32(v / s)).  Fast path: t = fl32(v * r) with
@@ -58,9 +59,11 @@ constexpr float kNearTie = 3.0517578125e-05f;  // 2^-15
 constexpr float kRoundMagic = 12582912.0f;     // 1.5 * 2^23
 
 struct RowScale {
-    float s;     // the scale
-    float r;     // fl32(1 / s)
-    bool fast;   // r is finite
+    float s;      // the scale
+    float r;      // fl32(1 / s)
+    bool fast;    // r is finite
+    uint64_t r2;  // (r, r) and the rounding constant, packed for f32x2 arithmetic
+    uint64_t magic2;
 };
 
 // Codes of 8 values (two words of bf16 pairs) packed into two words.
@@ -70,12 +73,21 @@ __device__ __forceinline__ uint2 codes8(const uint4& v, const RowScale& rs) {
     uint32_t b[8];
     float worst = 0.0f;  // largest |t - round(t)| over the 8 values
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float t = __fmul_rn(x[i], rs.r);
-        const float m = __fadd_rn(t, kRoundMagic);
-        const float c = __fsub_rn(m, kRoundMagic);
-        worst = fmaxf(worst, fabsf(__fsub_rn(t, c)));
-        b[i] = __float_as_uint(m);
+    for (int i = 0; i < 8; i += 2) {
+        // per value, two at a time with the same IEEE single roundings:
+        // t = x * r, m = t + magic, c = m - magic, d = t - c
+        float d0, d1;
+        asm("{\n\t.reg .b64 x, t, m, c, d;\n\t"
+            "mov.b64 x, {%4, %5};\n\t"
+            "mul.rn.f32x2 t, x, %6;\n\t"
+            "add.rn.f32x2 m, t, %7;\n\t"
+            "sub.rn.f32x2 c, m, %7;\n\t"
+            "sub.rn.f32x2 d, t, c;\n\t"
+            "mov.b64 {%0, %1}, m;\n\t"
+            "mov.b64 {%2, %3}, d;\n\t}"
+            : "=r"(b[i]), "=r"(b[i + 1]), "=f"(d0), "=f"(d1)
+            : "f"(x[i]), "f"(x[i + 1]), "l"(rs.r2), "l"(rs.magic2));
+        worst = fmaxf(worst, fmaxf(fabsf(d0), fabsf(d1)));
     }
     if (!rs.fast || worst > 0.5f - kNearTie) {
         // rare: some value lies next to a half-integer; take the division
@@ -179,6 +191,8 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
     rs.s = s;
     rs.r = __frcp_rn(s);
     rs.fast = isfinite(rs.r);
+    asm("mov.b64 %0, {%1, %1};" : "=l"(rs.r2) : "f"(rs.r));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(rs.magic2) : "f"(kRoundMagic));
 
     uint2* qp = q ? reinterpret_cast<uint2*>(q + row * K) : nullptr;
     uint4* hp = qh ? reinterpret_cast<uint4*>(qh + row * K) : nullptr;
