@@ -116,7 +116,12 @@ struct FusedCfg {
     static constexpr int kFree = kSmemOptin - 1024 /*alignment slack*/ - kCtlBytes - kFixed;
     static constexpr int kStages8 = kFree / kStage8 < kMaxStages8 ? kFree / kStage8 : kMaxStages8;
     static constexpr int kW8Off = kFixed;
-    static constexpr int kStageBytes = kFixed + kStages8 * kStage8;
+    // Output staging (2 KB per epilogue warp: 32 rows x 32 bf16 columns),
+    // only where it fits beside full rings.
+    static constexpr int kOutBytes = kEpiWarps * 32 * 64;
+    static constexpr bool kStageOut = kFree - kStages8 * kStage8 >= kOutBytes;
+    static constexpr int kOutOff = kFixed + kStages8 * kStage8;
+    static constexpr int kStageBytes = kFixed + kStages8 * kStage8 + (kStageOut ? kOutBytes : 0);
     static constexpr int kSmemBytes = kStageBytes + 1024 + kCtlBytes;
     static constexpr int kGroups = kWRows / 8;  // 8-row groups of weights per stage
     static constexpr int kGroupsPerWarp = (kGroups + kTeamWarps - 1) / kTeamWarps;
@@ -246,6 +251,57 @@ __device__ __forceinline__ void store_out(const W8A8Params& p, const EpiParams& 
             }
         }
     }
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d);
+__device__ __forceinline__ uint4 lds128(uint32_t addr);
+
+// The same epilogue as store_out for a non-swapped tile, KH columns of one
+// warp's 32 rows, written through the warp's staging buffer: each whole
+// block of 32 columns goes to shared memory row by row (16-byte units
+// XOR-swizzled by row pair, no bank conflicts), then out as 8 rows x 64
+// contiguous bytes per store instruction instead of 32 rows x 16 bytes; the
+// KH % 32 columns left over go out directly.  Needs N % 8 == 0.
+template <int KH>
+__device__ __forceinline__ void store_staged(const W8A8Params& p, const EpiParams& e, int64_t row_base,
+                                             int64_t col_base, int quarter, int half, int lane, uint32_t stage,
+                                             const int32_t* run) {
+    const int row = quarter * 32 + lane;
+    const float rs = e.row_scale[row];
+    const int swz = (lane >> 1) & 3;
+#pragma unroll
+    for (int blk = 0; blk < KH / 32; ++blk) {
+        const int c0 = half * KH + blk * 32;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                const int c = c0 + 8 * u + j;
+                float f0 = __fmul_rn(__fmul_rn(__int2float_rn(run[blk * 32 + 8 * u + j]), rs), e.col_scale[c]);
+                float f1 = __fmul_rn(__fmul_rn(__int2float_rn(run[blk * 32 + 8 * u + j + 1]), rs), e.col_scale[c + 1]);
+                if (p.bias) {
+                    f0 = __fadd_rn(f0, bf16_to_f32(e.col_bias[c]));
+                    f1 = __fadd_rn(f1, bf16_to_f32(e.col_bias[c + 1]));
+                }
+                w[j / 2] = (uint32_t)f32_to_bf16_rn(f0) | ((uint32_t)f32_to_bf16_rn(f1) << 16);
+            }
+            sts128(stage + (uint32_t)(lane * 64 + ((u ^ swz) << 4)), w[0], w[1], w[2], w[3]);
+        }
+        __syncwarp();
+#pragma unroll 1  // (unrolled, it pushed the epilogue past its registers)
+        for (int r = 0; r < 4; ++r) {
+            const int lr = 8 * r + (lane >> 2);
+            const int u = lane & 3;
+            const uint4 v = lds128(stage + (uint32_t)(lr * 64 + ((u ^ ((lr >> 1) & 3)) << 4)));
+            const int64_t m = row_base + quarter * 32 + lr;
+            const int64_t n = col_base + c0 + 8 * u;
+            if (m < p.M && n < p.N) *reinterpret_cast<uint4*>(p.y + m * p.N + n) = v;
+        }
+        __syncwarp();
+    }
+#pragma unroll
+    for (int q = (KH / 32) * 4; q < KH / 8; ++q) store_out<8>(p, e, row_base, col_base, row, half * KH + 8 * q, run + 8 * q);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -535,9 +591,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!alive) break;
             }
+            if (Cfg::kStageOut && !p.swap && p.acc == nullptr && (p.N % 8) == 0) {
+                store_staged<kHalf>(p, ep, row_base, col_base, quarter, half, lane,
+                                    op_base + (uint32_t)(Cfg::kOutOff + warp * 2048), run);
+            } else {
 #pragma unroll
-            for (int q = 0; q < kHalf / 8; ++q)
-                store_out<8>(p, ep, row_base, col_base, row, half * kHalf + 8 * q, run + 8 * q);
+                for (int q = 0; q < kHalf / 8; ++q)
+                    store_out<8>(p, ep, row_base, col_base, row, half * kHalf + 8 * q, run + 8 * q);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->epi_free[eb]);
         }
@@ -748,13 +809,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row = p.swap ? r0 + i % nrows : r0 + i / kVecs;
                 const int c = (p.swap ? i / nrows : i % kVecs) * 4;
                 const uint32_t off = part_addr + (uint32_t)(row * Cfg::kPartStride + c) * 4u;
+                // every rank's partial in flight before the rank-ordered sum
+                // (a load after each add would wait out each load in turn)
+                int4 t[kMaxSplit];
+#pragma unroll
+                for (int q = 0; q < kMaxSplit; ++q)
+                    if (q < S) t[q] = ld_dsmem_v4(off, (uint32_t)q);
                 int32_t v[4] = {0, 0, 0, 0};
-                for (int q = 0; q < S; ++q) {
-                    const int4 t = ld_dsmem_v4(off, (uint32_t)q);
-                    v[0] += t.x;
-                    v[1] += t.y;
-                    v[2] += t.z;
-                    v[3] += t.w;
+#pragma unroll
+                for (int q = 0; q < kMaxSplit; ++q) {
+                    if (q < S) {
+                        v[0] += t[q].x;
+                        v[1] += t[q].y;
+                        v[2] += t[q].z;
+                        v[3] += t[q].w;
+                    }
                 }
                 store_out<4>(p, ep, row_base, col_base, row, c, v);
             }

@@ -147,19 +147,24 @@ def _codes(rows, k, seed, extreme=False):
     return g.integers(-127, 128, size=(rows, k)).astype(np.int8)
 
 
-def gpu_w8a8(qx, sx, qw, sw, bias_bits=None, noalloc=False):
+def gpu_w8a8(qx, sx, qw, sw, bias_bits=None, noalloc=False, with_acc=True):
+    """W8A8 on the GPU into guarded buffers: (acc, y bits), or y bits alone
+    with with_acc=False (no accumulator output: the epilogue's plain form)."""
     m, k = qx.shape
     n = qw.shape[0]
     ybuf, y = util.guarded((m, n), torch.int16, "cuda", 0x7F7F)
     abuf, acc = util.guarded((m, n), torch.int32, "cuda", -5)
+    a = acc if with_acc else None
     bias = None if bias_bits is None else util.from_bits(bias_bits, "cuda")
     args = (dev(torch.from_numpy(qx)), dev(torch.from_numpy(sx)), dev(torch.from_numpy(qw)), dev(torch.from_numpy(sw)))
     if noalloc:
-        capi.w8a8_gemm_noalloc(*args, y.view(torch.bfloat16), bias=bias, acc_debug=acc)
+        capi.w8a8_gemm_noalloc(*args, y.view(torch.bfloat16), bias=bias, acc_debug=a)
     else:
-        capi.w8a8_gemm(*args, bias=bias, y=y.view(torch.bfloat16), acc_debug=acc)
+        capi.w8a8_gemm(*args, bias=bias, y=y.view(torch.bfloat16), acc_debug=a)
     torch.cuda.synchronize()
     assert util.guard_intact(ybuf, m * n, 0x7F7F) and util.guard_intact(abuf, m * n, -5)
+    if not with_acc:
+        return y.cpu().numpy().view(np.uint16)
     return acc.cpu().numpy(), y.cpu().numpy().view(np.uint16)
 
 
@@ -291,7 +296,7 @@ def test_w8a8_qwen3_8b_sweep_sampled(shape, m):
 PLAN_SHAPES = [(65, 640, 9728), (100, 2560, 2560), (128, 200, 12288), (129, 2560, 9728), (256, 512, 4096),
                (300, 1000, 4160), (512, 6144, 2560), (1024, 2560, 2560), (2048, 6144, 2560),
                (2048, 19456, 2560), (4096, 2560, 2560), (777, 3000, 1040), (512, 4096, 4096),
-               (512, 2560, 2560), (512, 2560, 9728), (128, 19456, 2560)]
+               (512, 2560, 2560), (512, 2560, 9728), (128, 19456, 2560), (300, 1004, 1040)]
 
 
 # Shapes whose 256-wide pair tiles outnumber the pairs without filling whole
@@ -328,6 +333,8 @@ def test_w8a8_plan_shapes_sampled(m, n, k, entry):
     sx, sw = _scales(m, m + 3, 0.01, 1.0), _scales(n, n + 4)
     bias = util.bits(synthetic.bias(n, n + 1)) if m % 2 else None
     acc, y = gpu_w8a8(qx, sx, qw, sw, bias, noalloc=entry == "noalloc")
+    # without the accumulator output the outputs are the same, bit for bit
+    assert np.array_equal(gpu_w8a8(qx, sx, qw, sw, bias, noalloc=entry == "noalloc", with_acc=False), y)
     pm, pn = _points(m, n, 4000, m * n + k)
     ref_acc, _, ref_y = oracle.w8a8_points(qx, sx, qw, sw, bias, pm, pn)
     assert np.array_equal(acc[pm, pn].astype(np.int64), ref_acc)
@@ -349,6 +356,7 @@ def test_w8a8_stream_k_exact(m, n, k):
     sx, sw = _scales(m, m + 9, 0.01, 1.0), _scales(n, n + 8)
     bias = util.bits(synthetic.bias(n, n + 2)) if m % 2 else None
     acc, y = gpu_w8a8(qx, sx, qw, sw, bias)
+    assert np.array_equal(gpu_w8a8(qx, sx, qw, sw, bias, with_acc=False), y)
     exact = qx.astype(np.float64) @ qw.astype(np.float64).T
     assert np.array_equal(acc.astype(np.float64), exact), \
         f"acc differs at {np.argwhere(acc.astype(np.float64) != exact)[:3].tolist()}"
