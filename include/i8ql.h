@@ -99,7 +99,11 @@ i8ql_status quantize_act_per_token_int8(const i8ql_bf16* x, int64_t M, int64_t K
  * sw fp32 [N], bias bf16 [N] or NULL.  Outputs: y bf16 [M, N]; acc_debug
  * int32 [M, N] or NULL (when given, receives the exact accumulator).
  * The epilogue may fuse multiply-adds: y is within one bf16 ulp of the
- * value above.
+ * value above.  For M > 64 the call takes a temporary stream-ordered
+ * workspace (cudaMallocAsync / cudaFreeAsync on `stream`): the fp16 codes of
+ * the tokens, 2*M*K bytes, plus, when the plan runs stream-K (see
+ * i8ql_w8a8_plan), one int32 partial tile of 128 x 256 per CTA pair half
+ * (128 KiB per CTA, about 19 MiB on 152 SMs) and a flag per CTA.
  */
 i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                       const i8ql_bf16* bias, i8ql_bf16* y, int32_t* acc_debug,
@@ -123,7 +127,8 @@ i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const
  * Outputs: y bf16 [M, N]; qx int8 [M, K] and sx fp32 [M] receive the token
  * codes and scales when given (each may be NULL); acc_debug int32 [M, N] or
  * NULL.  Takes a temporary stream-ordered workspace (at most 2*M*K + 4*M
- * bytes).  Errors and argument rules as w8a8_gemm, with x checked like y.
+ * bytes, plus the stream-K workspace of w8a8_gemm when the plan runs
+ * stream-K).  Errors and argument rules as w8a8_gemm, with x checked like y.
  */
 i8ql_status w8a8_linear(const i8ql_bf16* x, const int8_t* qw, const float* sw, const i8ql_bf16* bias,
                         i8ql_bf16* y, int8_t* qx, float* sx, int32_t* acc_debug,
@@ -176,7 +181,9 @@ i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64
  * exactly what w8a8_gemm computes, with the same arguments, layouts and
  * errors, but where w8a8_gemm takes a temporary workspace from the
  * stream-ordered allocator (for M > 64: the fp16 codes of the tokens,
- * 2 * M * K bytes), this one uses a fixed array compiled into the
+ * 2 * M * K bytes, and a stream-K workspace when its plan uses one), this
+ * one never runs stream-K (i8ql_w8a8_noalloc_plan) and uses a fixed array
+ * compiled into the
  * library: I8QL_NOALLOC_MAX_ELEMENTS 16-bit elements (32 MiB), held by every
  * GPU that loads the library until the process exits.
  *
