@@ -1,38 +1,48 @@
 #!/usr/bin/env python
 """Benchmark of the int8 quantized linear layer on GB300.
 
-One step = one pass of the whole hot path over one batch of synthetic input:
+The default run (``--workload all``) measures the whole metric, "int8 GEMM
+TOPS (prefill) & weight GB/s (decode)", in three parts, each captured as a
+CUDA graph of one step and timed on its own, and prints ONE JSON line:
 
-  decode (default; Qwen3-4B-shaped decode linears plus the DeepSeek-MoE-16B
-  grouped experts):
+  decode (top-level value, GB/s): the Qwen3-4B decode linears plus the
+  DeepSeek-MoE-16B grouped experts, one pass of every row of the path:
     * per-channel weight quantization of the four bf16 projection weights
       (fused QKV [6144, 2560], o [2560, 2560], fused gate_up [19456, 2560],
       down [2560, 9728]);
     * for M in {1, 4, 8} and each projection: per-token activation
       quantization, the W8A8 GEMM and the W8A16 GEMM;
     * the grouped W8A16 GEMM over 66 experts (64 routed, top-6, + 2 shared)
-      for T = 8 decode tokens, gate_up [2816, 2048] then down [2048, 1408].
-  prefill (--workload prefill; Qwen3-4B W8A8 prefill, bias on):
-    * for M in {128, 512, 2048, 4096} and each projection: the W8A8 linear
-      layer from bf16 activations (w8a8_linear: per-token activation
-      quantization fused with the W8A8 GEMM, two kernels per call).
+      for T in {1, 8, 64} decode tokens, gate_up [2816, 2048] then down
+      [2048, 1408].
+  prefill (block "prefill", TOPS): Qwen3-4B W8A8 prefill, bias on: for M in
+    {128, 512, 2048, 4096} and each projection, the W8A8 linear layer from
+    bf16 activations (w8a8_linear: per-token quantization fused into the
+    call).
+  Qwen3-8B sweep (block "qwen3_8b_sweep"): fused QKV [6144, 4096],
+    o [4096, 4096], fused gate_up [24576, 4096], down [4096, 12288]; W8A16
+    for M in {1, 2, 4, 8, 16, 32, 64} and the W8A8 linear layer for M in
+    {1, 2, 4, 8, 16, 32, 64, 128, 512, 2048, 8192}.
 
-Every GEMM launch of a step reads its own copy of the int8 weights, and a
-step touches more than 1 GB, so no launch finds its weights in the 129 MB L2
-(between timed steps nothing is reused either).  The step is captured once as
-a CUDA graph; the timed region replays K steps back to back.  Launches of
-one kernel run back to back (programmatic dependent launch overlaps their
-prologues), and an external CUDA event pair around each kernel's batch times
+Every GEMM launch of a step reads its own copy of the int8 weights, and each
+part touches more than the 129 MB L2 per step, so no launch finds its
+weights in L2 (between timed steps nothing is reused either).  The timed
+region replays K steps of the part's graph back to back.  Launches of one
+kernel class run back to back (programmatic dependent launch overlaps their
+prologues), and an external CUDA event pair around each class's batch times
 it live: average launch duration = batch time / launches.
 
 value (decode) = algorithmic HBM bytes of all launches / step time (GB/s);
-value (prefill) = 2*M*N*K summed over the W8A8 launches / step time (TOPS).
+prefill TOPS = 2*M*N*K summed over the W8A8 launches / step time.
 Algorithmic bytes per launch: quantization 3*R*K + 4*R; W8A8
-M*K + N*K + 4*(M+N) + 2*M*N; W8A16 N*K + 4*N + 2*M*K + 2*M*N; grouped
-sum over experts with rows of (N*K + 4*N) + 2*rows*(K+N).
+M*K + N*K + 4*(M+N) + 2*M*N (+2*N bias); the W8A8 linear layer adds the
+quantization pass of its activations; W8A16 N*K + 4*N + 2*M*K + 2*M*N;
+grouped sum over experts with rows of (N*K + 4*N) + 2*rows*(K+N).
 
---impl reference times the CPU oracle (the only reference implementation:
-the pages ship no code) on a bounded sample of the same workload.
+cpu_baseline times the CPU oracle (the only reference implementation: the
+pages ship no code) on the host cores, with one thread and with every core,
+on a bounded sample of the same workload; --impl reference times it with
+every core.
 """
 
 from __future__ import annotations
@@ -57,10 +67,20 @@ if ROOT not in sys.path:
 METRIC = "int8 GEMM TOPS (prefill) & weight GB/s (decode) vs GB300 roofline"
 DECODE_MS = (1, 4, 8)
 PREFILL_MS = (128, 512, 2048, 4096)
-MOE_TOKENS = 8
-W8A8_DECODE_MAX_M = 64  # above it a W8A8 call is two kernels: token codes to fp16, then the tensor-core GEMM
-KERNEL_ORDER = ("quant_w", "quant_x", "w8a8", "w8a16", "grouped")
+MOE_TOKENS = (1, 8, 64)
+SWEEP_W8A16_MS = (1, 2, 4, 8, 16, 32, 64)
+SWEEP_W8A8_MS = (1, 2, 4, 8, 16, 32, 64, 128, 512, 2048, 8192)
+W8A8_DECODE_MAX_M = 64  # above it a W8A8 call runs on the tensor-core kernel
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Kernel classes of each part, in launch order; "tensor" classes are
+# contractions on the tensor-core kernel (TOPS against the bf16-pipe peak),
+# the others stream weights (GB/s against HBM).
+PART_CLASSES = {
+    "decode": ("quant_w", "quant_x", "w8a8", "w8a16", "grouped"),
+    "prefill": ("w8a8",),
+    "sweep8b": ("w8a16", "w8a8_decode", "w8a8_prefill"),
+}
+TENSOR_CLASSES = {("prefill", "w8a8"), ("sweep8b", "w8a8_prefill")}
 
 
 # ---------------------------------------------------------------- accounting
@@ -82,14 +102,18 @@ def bytes_grouped(counts, n, k):
     return len(active) * (n * k + 4 * n) + 2 * sum(active) * (k + n)
 
 
-def workload_name(kind):
-    if kind == "decode":
+def workload_name(part):
+    if part == "decode":
         return ("Qwen3-4B decode linears (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, "
                 "down 9728->2560; M in {1,4,8}; weight quant + act quant + W8A8 + W8A16) + "
-                "DeepSeek-MoE-16B grouped W8A16 (66 experts, top-6 + 2 shared, T=8; "
+                "DeepSeek-MoE-16B grouped W8A16 (66 experts, top-6 + 2 shared, T in {1,8,64}; "
                 "gate_up 2816x2048, down 2048x1408)")
-    return ("Qwen3-4B prefill W8A8 (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, down 9728->2560; "
-            "M in {128,512,2048,4096}; W8A8 linear from bf16 activations (per-token act quant fused), bias on)")
+    if part == "prefill":
+        return ("Qwen3-4B prefill W8A8 (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, down 9728->2560; "
+                "M in {128,512,2048,4096}; W8A8 linear from bf16 activations (per-token act quant fused), bias on)")
+    return ("Qwen3-8B sweep (QKV 6144x4096, o 4096x4096, gate_up 24576x4096, down 12288->4096; "
+            "W8A16 for M in {1,2,4,8,16,32,64}; W8A8 linear from bf16 activations for "
+            "M in {1,2,4,8,16,32,64,128,512,2048,8192})")
 
 
 def load_peaks():
@@ -101,24 +125,26 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# CUDA sources each kernel class of a workload runs (W8A8 in the decode range
-# runs on the decode kernel; above it on the tensor-core kernel).
+# CUDA sources each kernel class runs (W8A8 in the decode range runs on the
+# decode kernel; above it on the tensor-core kernel).
 KERNEL_SOURCES = {
     "decode": {"w8a8": ["decode_gemm.cu"], "w8a16": ["decode_gemm.cu"], "grouped": ["decode_gemm.cu"],
                "quant_w": ["quant.cu"], "quant_x": ["quant.cu"]},
     "prefill": {"w8a8": ["w8a8.cu", "w8a8_fused.cu", "tc_common.cuh", "quant.cu"]},
+    "sweep8b": {"w8a16": ["decode_gemm.cu"], "w8a8_decode": ["decode_gemm.cu", "quant.cu"],
+                "w8a8_prefill": ["w8a8.cu", "w8a8_fused.cu", "tc_common.cuh", "quant.cu"]},
 }
 
 
-def kernel_source_hash(kernel, workload):
+def kernel_source_hash(kernel, part):
     h = hashlib.sha256()
-    for src in KERNEL_SOURCES[workload][kernel]:
+    for src in KERNEL_SOURCES[part][kernel]:
         with open(os.path.join(ROOT, "int8_quantized_linear_gb300", "csrc", src), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel, workload):
+def ncu_traffic(kernel, part):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current source of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -126,8 +152,8 @@ def ncu_traffic(kernel, workload):
         return None
     with open(path) as fh:
         table = json.load(fh)
-    entry = table.get(workload, {}).get(kernel)
-    if not entry or entry.get("source_sha256_16") != kernel_source_hash(kernel, workload):
+    entry = table.get(part, {}).get(kernel)
+    if not entry or entry.get("source_sha256_16") != kernel_source_hash(kernel, part):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -143,96 +169,25 @@ class Launch:
 
 
 class Workload:
-    """Device buffers and the ordered launch list of one step."""
+    """Device buffers and the ordered launch list of one step of a part."""
 
-    def __init__(self, kind, device, seed=1):
-        from int8_quantized_linear_gb300 import capi, synthetic
-        self.kind = kind
+    def __init__(self, part, device, seed=1):
+        self.part = part
         self.device = device
         self.launches: list[Launch] = []
         self.h2d: list[tuple[torch.Tensor, torch.Tensor]] = []  # (pinned host, device) inputs
         self.d2h: list[tuple[torch.Tensor, torch.Tensor]] = []  # (device, pinned host) results
-        self.cpu_inputs = {}
-        shapes = synthetic.QWEN3_4B_SHAPES
-        ms = DECODE_MS if kind == "decode" else PREFILL_MS
-        dev = device
-        kinds = ("w8a8", "w8a16") if kind == "decode" else ("w8a8",)
-        copies = len(ms) * len(kinds)
-
-        for si, (name, (n, k)) in enumerate(shapes.items()):
-            w = synthetic.weight(n, k, seed + si, device=dev)
-            qs = [torch.empty((n, k), dtype=torch.int8, device=dev) for _ in range(copies)]
-            s = torch.empty((n,), dtype=torch.float32, device=dev)
-            capi.quantize_weight_per_channel_int8(w, q=qs[0], scale=s)
-            for c in range(1, copies):
-                qs[c].copy_(qs[0])
-            bias = synthetic.bias(n, seed + si, device=dev) if kind == "prefill" else None
-            self.cpu_inputs[name] = {"w": w}
-            if kind == "decode":
-                self.launches.append(Launch(
-                    "quant_w", lambda w=w, q=qs[0], s=s: capi.quantize_weight_per_channel_int8(w, q=q, scale=s),
-                    bytes_quant(n, k), 0, f"quant_w {name} {n}x{k}"))
-                self.h2d.append((torch.empty(w.shape, dtype=w.dtype, pin_memory=True).copy_(w), w))
-            for mi, m in enumerate(ms):
-                x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=dev)
-                self.h2d.append((torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x), x))
-                y8 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-                q8 = qs[mi * len(kinds)]
-                if kind == "decode":
-                    qx = torch.empty((m, k), dtype=torch.int8, device=dev)
-                    sx = torch.empty((m,), dtype=torch.float32, device=dev)
-                    self.launches.append(Launch(
-                        "quant_x", lambda x=x, qx=qx, sx=sx: capi.quantize_act_per_token_int8(x, q=qx, scale=sx),
-                        bytes_quant(m, k), 0, f"quant_x {name} M={m}"))
-                    self.launches.append(Launch(
-                        "w8a8", lambda qx=qx, sx=sx, q=q8, s=s, b=bias, y=y8: capi.w8a8_gemm(qx, sx, q, s, bias=b, y=y),
-                        bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k, f"w8a8 {name} M={m}",
-                        gpu_kernels=1 if m <= W8A8_DECODE_MAX_M else 2))
-                else:
-                    # prefill: the linear layer from bf16 activations, with the
-                    # per-token quantization fused into the call
-                    self.launches.append(Launch(
-                        "w8a8", lambda x=x, q=q8, s=s, b=bias, y=y8: capi.w8a8_linear(x, q, s, bias=b, y=y),
-                        bytes_quant(m, k) + bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k,
-                        f"w8a8_linear {name} M={m}", gpu_kernels=2))
-                self.d2h.append((y8, torch.empty(y8.shape, dtype=y8.dtype, pin_memory=True)))
-                if kind == "decode":
-                    y16 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-                    q16 = qs[mi * len(kinds) + 1]
-                    self.launches.append(Launch(
-                        "w8a16", lambda x=x, q=q16, s=s, y=y16: capi.w8a16_gemm(x, q, s, y=y),
-                        bytes_w8a16(m, n, k), 2 * m * n * k, f"w8a16 {name} M={m}"))
-                    self.d2h.append((y16, torch.empty(y16.shape, dtype=y16.dtype, pin_memory=True)))
-                self.cpu_inputs[name][m] = x
-            self.cpu_inputs[name]["s"] = s
-            del w
-
-        if kind == "decode":
-            route = synthetic.moe_routing(MOE_TOKENS, seed=3)
-            counts = np.diff(route.offsets)
-            off = torch.from_numpy(route.offsets).to(dev)
-            self.h2d.append((torch.from_numpy(route.offsets).pin_memory(), off))
-            self.moe = {"route": route}
-            for pi, (proj, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
-                e_count = route.experts
-                q = torch.empty((e_count, n, k), dtype=torch.int8, device=dev)
-                s = torch.empty((e_count, n), dtype=torch.float32, device=dev)
-                for e in range(e_count):
-                    we = synthetic.weight(n, k, 1000 + 100 * pi + e, device=dev)
-                    capi.quantize_weight_per_channel_int8(we, q=q[e], scale=s[e])
-                x_tok = synthetic.activations(MOE_TOKENS, k, 900 + pi, device=dev)
-                x = x_tok[torch.from_numpy(route.rows).to(dev)].contiguous()
-                self.h2d.append((torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x), x))
-                y = torch.empty((x.shape[0], n), dtype=torch.bfloat16, device=dev)
-                self.launches.append(Launch(
-                    "grouped", lambda x=x, off=off, q=q, s=s, y=y: capi.grouped_w8a16_gemm(x, off, q, s, y=y),
-                    bytes_grouped(counts, n, k), 2 * int(counts.sum()) * n * k, f"grouped {proj} T={MOE_TOKENS}"))
-                self.d2h.append((y, torch.empty(y.shape, dtype=y.dtype, pin_memory=True)))
-                self.moe[proj] = (q, s, x)
-        # Launches of one kernel run back to back (stable order otherwise), so
-        # that consecutive launches can overlap through programmatic
-        # dependent launch and a pair of events brackets each kernel's batch.
-        order = {k: i for i, k in enumerate(KERNEL_ORDER)}
+        if part == "decode":
+            self._decode(seed)
+        elif part == "prefill":
+            self._prefill(seed)
+        else:
+            self._sweep8b(seed)
+        # Launches of one kernel class run back to back (stable order
+        # otherwise), so that consecutive launches can overlap through
+        # programmatic dependent launch and a pair of events brackets each
+        # class's batch.
+        order = {k: i for i, k in enumerate(PART_CLASSES[part])}
         self.launches.sort(key=lambda l: order[l.kernel])
         self.batches = []
         for l in self.launches:
@@ -240,6 +195,118 @@ class Workload:
                 self.batches.append((l.kernel, []))
             self.batches[-1][1].append(l)
         torch.cuda.synchronize()
+
+    def _pin_in(self, t):
+        self.h2d.append((torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t), t))
+
+    def _pin_out(self, t):
+        self.d2h.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
+
+    def _weight_copies(self, n, k, seed, copies):
+        from int8_quantized_linear_gb300 import capi, synthetic
+        w = synthetic.weight(n, k, seed, device=self.device)
+        qs = [torch.empty((n, k), dtype=torch.int8, device=self.device) for _ in range(copies)]
+        s = torch.empty((n,), dtype=torch.float32, device=self.device)
+        capi.quantize_weight_per_channel_int8(w, q=qs[0], scale=s)
+        for c in range(1, copies):
+            qs[c].copy_(qs[0])
+        return w, qs, s
+
+    def _linear(self, kernel, x, q, s, bias, label):
+        """The W8A8 linear layer from bf16 activations (quantization fused)."""
+        from int8_quantized_linear_gb300 import capi
+        m, k = x.shape
+        n = q.shape[0]
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=self.device)
+        self.launches.append(Launch(
+            kernel, lambda x=x, q=q, s=s, b=bias, y=y: capi.w8a8_linear(x, q, s, bias=b, y=y),
+            bytes_quant(m, k) + bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k, f"{label} M={m}",
+            gpu_kernels=2))
+        self._pin_out(y)
+
+    def _w8a16(self, kernel, x, q, s, label):
+        from int8_quantized_linear_gb300 import capi
+        m, k = x.shape
+        n = q.shape[0]
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=self.device)
+        self.launches.append(Launch(kernel, lambda x=x, q=q, s=s, y=y: capi.w8a16_gemm(x, q, s, y=y),
+                                    bytes_w8a16(m, n, k), 2 * m * n * k, f"{label} M={m}"))
+        self._pin_out(y)
+
+    def _decode(self, seed):
+        from int8_quantized_linear_gb300 import capi, synthetic
+        dev = self.device
+        for si, (name, (n, k)) in enumerate(synthetic.QWEN3_4B_SHAPES.items()):
+            w, qs, s = self._weight_copies(n, k, seed + si, 2 * len(DECODE_MS))
+            self.launches.append(Launch(
+                "quant_w", lambda w=w, q=qs[0], s=s: capi.quantize_weight_per_channel_int8(w, q=q, scale=s),
+                bytes_quant(n, k), 0, f"quant_w {name} {n}x{k}"))
+            self._pin_in(w)
+            for mi, m in enumerate(DECODE_MS):
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=dev)
+                self._pin_in(x)
+                qx = torch.empty((m, k), dtype=torch.int8, device=dev)
+                sx = torch.empty((m,), dtype=torch.float32, device=dev)
+                self.launches.append(Launch(
+                    "quant_x", lambda x=x, qx=qx, sx=sx: capi.quantize_act_per_token_int8(x, q=qx, scale=sx),
+                    bytes_quant(m, k), 0, f"quant_x {name} M={m}"))
+                y8 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                self.launches.append(Launch(
+                    "w8a8", lambda qx=qx, sx=sx, q=qs[2 * mi], s=s, y=y8: capi.w8a8_gemm(qx, sx, q, s, y=y),
+                    bytes_w8a8(m, n, k, False), 2 * m * n * k, f"w8a8 {name} M={m}"))
+                self._pin_out(y8)
+                self._w8a16("w8a16", x, qs[2 * mi + 1], s, f"w8a16 {name}")
+        # DeepSeek-MoE grouped experts: one weight set per token count
+        for ti, tokens in enumerate(MOE_TOKENS):
+            route = synthetic.moe_routing(tokens, seed=3 + ti)
+            counts = np.diff(route.offsets)
+            off = torch.from_numpy(route.offsets).to(dev)
+            self._pin_in(off)
+            for pi, (proj, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
+                e_count = route.experts
+                q = torch.empty((e_count, n, k), dtype=torch.int8, device=dev)
+                s = torch.empty((e_count, n), dtype=torch.float32, device=dev)
+                for e in range(e_count):
+                    we = synthetic.weight(n, k, 1000 + 100 * pi + e, device=dev)
+                    capi.quantize_weight_per_channel_int8(we, q=q[e], scale=s[e])
+                x_tok = synthetic.activations(tokens, k, 900 + 10 * ti + pi, device=dev)
+                x = x_tok[torch.from_numpy(route.rows).to(dev)].contiguous()
+                self._pin_in(x)
+                y = torch.empty((x.shape[0], n), dtype=torch.bfloat16, device=dev)
+                self.launches.append(Launch(
+                    "grouped", lambda x=x, off=off, q=q, s=s, y=y: capi.grouped_w8a16_gemm(x, off, q, s, y=y),
+                    bytes_grouped(counts, n, k), 2 * int(counts.sum()) * n * k, f"grouped {proj} T={tokens}"))
+                self._pin_out(y)
+
+    def _prefill(self, seed):
+        from int8_quantized_linear_gb300 import synthetic
+        for si, (name, (n, k)) in enumerate(synthetic.QWEN3_4B_SHAPES.items()):
+            w, qs, s = self._weight_copies(n, k, seed + si, len(PREFILL_MS))
+            del w
+            bias = synthetic.bias(n, seed + si, device=self.device)
+            for mi, m in enumerate(PREFILL_MS):
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=self.device)
+                self._pin_in(x)
+                self._linear("w8a8", x, qs[mi], s, bias, f"w8a8_linear {name}")
+
+    def _sweep8b(self, seed):
+        from int8_quantized_linear_gb300 import synthetic
+        seed += 40
+        for si, (name, (n, k)) in enumerate(synthetic.QWEN3_8B_SHAPES.items()):
+            w, qs, s = self._weight_copies(n, k, seed + si, len(SWEEP_W8A16_MS) + len(SWEEP_W8A8_MS))
+            del w
+            c = 0
+            for m in SWEEP_W8A16_MS:
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + m, device=self.device)
+                self._pin_in(x)
+                self._w8a16("w8a16", x, qs[c], s, f"w8a16 {name}")
+                c += 1
+            for m in SWEEP_W8A8_MS:
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + m + 1, device=self.device)
+                self._pin_in(x)
+                kind = "w8a8_decode" if m <= W8A8_DECODE_MAX_M else "w8a8_prefill"
+                self._linear(kind, x, qs[c], s, None, f"w8a8_linear {name}")
+                c += 1
 
     def run(self, events=None):
         """One step; events[b] = (start, end) brackets batch b."""
@@ -255,9 +322,8 @@ class Workload:
     def step_bytes(self):
         return sum(l.bytes for l in self.launches)
 
-    @property
-    def step_flops(self):
-        return sum(l.flops for l in self.launches if l.kernel == "w8a8")
+    def step_flops(self, classes):
+        return sum(l.flops for l in self.launches if l.kernel in classes)
 
 
 def _event(external):
@@ -317,8 +383,8 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle (CPU) arm
 
-def oracle_step(sample, threads_note=False):
-    """Time the CPU oracle over a row sample of the workload; returns
+def oracle_step(sample):
+    """Time the CPU oracle over a row sample of a workload; returns
     (algorithmic bytes, GEMM ops 2*M*N*K, seconds)."""
     import oracle
     total_b, total_ops, total_s = 0, 0, 0.0
@@ -330,11 +396,11 @@ def oracle_step(sample, threads_note=False):
             oracle.quant_rows(src)
             total_b += bytes_quant(*src.shape)
         elif kind == "w8a8":
-            _, xb, qw, sw = item
+            _, xb, qw, sw, bias = item
             qx, sx = oracle.quant_rows(xb)
-            oracle.w8a8(qx, sx, qw, sw)
+            oracle.w8a8(qx, sx, qw, sw, bias)
             m, k = xb.shape
-            total_b += bytes_quant(m, k) + bytes_w8a8(m, qw.shape[0], k, False)
+            total_b += bytes_quant(m, k) + bytes_w8a8(m, qw.shape[0], k, bias is not None)
             total_ops += 2 * m * qw.shape[0] * k
         elif kind == "w8a16":
             _, xb, qw, sw = item
@@ -350,46 +416,79 @@ def oracle_step(sample, threads_note=False):
     return total_b, total_ops, total_s
 
 
-def oracle_rate(workload, nbytes, ops, seconds):
-    """The oracle's rate in the workload's metric unit: GB/s for decode,
-    TOPS (2*M*N*K of the W8A8 GEMMs) for prefill."""
-    if workload == "decode":
+def oracle_rate(part, nbytes, ops, seconds):
+    """The oracle's rate in the part's unit: GB/s for decode, TOPS (2*M*N*K
+    of the W8A8 GEMMs) for prefill."""
+    if part == "decode":
         return nbytes / seconds / 1e9, "GB/s"
     return ops / seconds / 1e12, "TOPS"
 
 
-def build_oracle_sample(kind, row_frac, seed=1):
-    """The workload with every weight cut to a fraction of its output rows
-    (and the grouped experts to a fraction of their rows), drawn on the CPU
-    from the same generators."""
+def build_oracle_sample(part, row_frac, seed=1):
+    """The part's workload with every weight cut to a fraction of its output
+    rows (prefill: every M too; grouped experts: a fraction of their rows),
+    drawn on the CPU from the same generators."""
     import oracle
     from int8_quantized_linear_gb300 import synthetic
     sample = []
-    ms = DECODE_MS if kind == "decode" else PREFILL_MS
+    ms = DECODE_MS if part == "decode" else PREFILL_MS
     for si, (name, (n, k)) in enumerate(synthetic.QWEN3_4B_SHAPES.items()):
         nr = max(16, int(n * row_frac))
         w = synthetic.bf16_bits(synthetic.weight(nr, k, seed + si))
         qw, sw = oracle.quant_rows(w)
-        if kind == "decode":
+        bias = None if part == "decode" else synthetic.bf16_bits(synthetic.bias(nr, seed + si))
+        if part == "decode":
             sample.append(("quant", w))
         for mi, m in enumerate(ms):
-            mr = m if kind == "decode" else max(1, int(m * row_frac))
+            mr = m if part == "decode" else max(1, int(m * row_frac))
             xb = synthetic.bf16_bits(synthetic.activations(mr, k, 100 * seed + 10 * si + mi))
-            sample.append(("w8a8", xb, qw, sw))
-            if kind == "decode":
+            sample.append(("w8a8", xb, qw, sw, bias))
+            if part == "decode":
                 sample.append(("w8a16", xb, qw, sw))
-    if kind == "decode":
-        route = synthetic.moe_routing(MOE_TOKENS, seed=3)
-        for pi, (proj, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
-            nr = max(16, int(n * row_frac))
-            q = np.empty((route.experts, nr, k), np.int8)
-            s = np.empty((route.experts, nr), np.float32)
-            for e in range(route.experts):
-                q[e], s[e] = oracle.quant_rows(synthetic.bf16_bits(synthetic.weight(nr, k, 1000 + 100 * pi + e)))
-            x_tok = synthetic.activations(MOE_TOKENS, k, 900 + pi)
-            xb = synthetic.bf16_bits(x_tok[torch.from_numpy(route.rows)])
-            sample.append(("grouped", xb, route.offsets, q, s))
+    if part == "decode":
+        experts = {}  # the same expert weights serve every token count
+        for ti, tokens in enumerate(MOE_TOKENS):
+            route = synthetic.moe_routing(tokens, seed=3 + ti)
+            for pi, (proj, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
+                nr = max(16, int(n * row_frac))
+                if pi not in experts:
+                    q = np.empty((route.experts, nr, k), np.int8)
+                    s = np.empty((route.experts, nr), np.float32)
+                    for e in range(route.experts):
+                        q[e], s[e] = oracle.quant_rows(
+                            synthetic.bf16_bits(synthetic.weight(nr, k, 1000 + 100 * pi + e)))
+                    experts[pi] = (q, s)
+                q, s = experts[pi]
+                x_tok = synthetic.activations(tokens, k, 900 + 10 * ti + pi)
+                xb = synthetic.bf16_bits(x_tok[torch.from_numpy(route.rows)])
+                sample.append(("grouped", xb, route.offsets, q, s))
     return sample
+
+
+def cpu_baseline(part, row_frac, min_seconds=3.0):
+    """The oracle on a bounded sample of the part, first on one thread, then
+    on every core: {value (all cores), cores, single_thread {...}, ...}."""
+    import oracle
+    sample = build_oracle_sample(part, row_frac)
+    scope = ("the whole workload" if row_frac >= 1 else
+             f"the workload with every weight cut to {row_frac:.4g} of its output rows"
+             + (" and every M to the same fraction" if part == "prefill" else " (grouped experts too)"))
+    out = {}
+    for label, threads in (("single", 1), ("all", os.cpu_count() or 1)):
+        used = oracle.set_threads(threads)
+        b, o, s, passes = 0, 0, 0.0, 0
+        while passes == 0 or (label == "all" and s < min_seconds and passes < 10):
+            bb, oo, ss = oracle_step(sample)
+            b, o, s, passes = b + bb, o + oo, s + ss, passes + 1
+        rate, unit = oracle_rate(part, b, o, s)
+        out[label] = {"value": rate, "unit": unit, "cores": used, "seconds": s, "passes": passes}
+    oracle.set_threads(os.cpu_count() or 1)
+    a, one = out["all"], out["single"]
+    return {"value": a["value"], "unit": a["unit"], "cores": a["cores"], "kind": "oracle",
+            "sample": f"{a['passes']} pass(es) of {scope}; {a['seconds']:.1f} s on {a['cores']} threads",
+            "nproc": os.cpu_count(),
+            "single_thread": {"value": one["value"], "unit": one["unit"], "cores": 1,
+                              "sample": f"{one['passes']} pass(es); {one['seconds']:.1f} s on 1 thread"}}
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -422,11 +521,17 @@ def barrier(world: int):
 # ---------------------------------------------------------------- arms
 
 def run_reference(args, world, rank):
-    """The oracle on the host cores: each step is a bounded row sample."""
+    """The oracle on the host cores (every core): each step is one pass over
+    a bounded row sample of the decode part (the top-level metric)."""
     if rank != 0:
         return 0
+    import oracle
+    part = "decode" if args.workload == "all" else args.workload
+    if part == "sweep8b":
+        part = "decode"
     frac = args.ref_row_frac
-    sample = build_oracle_sample(args.workload, frac)
+    sample = build_oracle_sample(part, frac)
+    cores = oracle.set_threads(os.cpu_count() or 1)
     for _ in range(args.warmup):
         oracle_step(sample)
     b_tot, o_tot, s_tot = 0, 0, 0.0
@@ -435,39 +540,37 @@ def run_reference(args, world, rank):
         b_tot += b
         o_tot += o
         s_tot += s
-    rate, unit = oracle_rate(args.workload, b_tot, o_tot, s_tot)
+    rate, unit = oracle_rate(part, b_tot, o_tot, s_tot)
     desc = (f"every weight cut to {frac:.4g} of its output rows (grouped experts too), "
-            f"{'M in {1,4,8}' if args.workload == 'decode' else 'M scaled by the same fraction'}; "
-            "single-threaded C oracle")
+            f"{'M in {1,4,8}' if part == 'decode' else 'M scaled by the same fraction'}; "
+            f"C oracle on {cores} threads")
     line = {
         "metric": METRIC, "value": rate, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000 * s_tot / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": workload_name(args.workload), "sample": desc},
-        "cpu_baseline": {"value": rate, "unit": unit, "cores": 1, "kind": "oracle", "sample": desc},
+        "config": {"workload": workload_name(part), "sample": desc},
+        "cpu_baseline": {"value": rate, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_ours(args, world, rank, local):
+def time_part(part, args, world, local, stream):
+    """Build, capture and time one part; returns its measurements."""
     from int8_quantized_linear_gb300 import capi
-
-    torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    wl = Workload(args.workload, device)
+    wl = Workload(part, device)
     n_launch = sum(l.gpu_kernels for l in wl.launches)  # library kernels per step
     n_batch = len(wl.batches)
-    stream = torch.cuda.Stream(device)
 
     # eager pass: per-device initialisation happens outside graph capture
     with torch.cuda.stream(stream):
         wl.run()
     torch.cuda.synchronize()
     if capi.i8ql_get_device_error(stream) != capi.I8QL_OK:
-        raise RuntimeError("kernel fault word set after the eager pass")
+        raise RuntimeError(f"{part}: kernel fault word set after the eager pass")
 
     external = _event(True) is not None
     use_graph = not args.no_graph and external
@@ -482,6 +585,7 @@ def run_ours(args, world, rank, local):
             for s in range(steps):
                 wl.run(events[s])
     else:
+        g_warm = None
         events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(n_batch)] for _ in range(steps)]
 
@@ -510,14 +614,12 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world)
-    ms_total = start.elapsed_time(end)
-    ms_total = max_over_ranks(ms_total, world)
-    ms_step = ms_total / steps
+    ms_step = max_over_ranks(start.elapsed_time(end), world) / steps
     fault = capi.i8ql_get_device_error(stream)
     if fault != capi.I8QL_OK:
-        raise RuntimeError(f"kernel fault word set: {capi.status_string(fault)}")
+        raise RuntimeError(f"{part}: kernel fault word set: {capi.status_string(fault)}")
 
-    # per-kernel live timings over the timed region
+    # per-class live timings over the timed region
     per = {}
     for s in range(steps):
         for b, (kernel, launches) in enumerate(wl.batches):
@@ -528,81 +630,119 @@ def run_ours(args, world, rank, local):
             e["bytes"] += sum(l.bytes for l in launches)
             e["flops"] += sum(l.flops for l in launches)
     peaks, peak_src = load_peaks()
-    hbm = peaks["hbm_gbs"]
-    # burst peak: the timed region lasts tens of milliseconds, far from the
-    # seconds-long power-capped loop behind the sustained figure
-    tflops_peak = peaks["bf16_tflops"]
     kernels = {}
     for name, e in per.items():
         gbs = e["bytes"] / (e["ms"] / 1e3) / 1e9
         entry = {"launches": e["launches"], "us_per_launch": 1e3 * e["ms"] / e["launches"],
                  "share": e["ms"] / sum(v["ms"] for v in per.values()),
-                 "GB/s": gbs, "hbm_frac": gbs / hbm}
+                 "GB/s": gbs, "hbm_frac": gbs / peaks["hbm_gbs"]}
         if e["flops"]:
-            entry["TOPS"] = e["flops"] / (e["ms"] / 1e3) / 1e12
+            tops = e["flops"] / (e["ms"] / 1e3) / 1e12
+            entry["TOPS"] = tops
+            if (part, name) in TENSOR_CLASSES:
+                entry["tensor_frac"] = tops / peaks["bf16_tflops"]
         kernels[name] = entry
-    dom = max(per, key=lambda k: per[k]["ms"])
+
+    e2e = run_e2e(args, wl, stream, g_warm, world, part)
+    out = {"wl": wl, "per": per, "kernels": kernels, "ms_step": ms_step, "clocks": clk, "e2e": e2e,
+           "launches": n_launch * steps, "graph": use_graph, "peaks": (peaks, peak_src)}
+    del g_warm
+    if use_graph:
+        del g_timed
+    return out
+
+
+def roofline(part, res, kernel=None):
+    """Roofline of the dominant kernel class of a part (or of `kernel`)."""
+    per = res["per"]
+    peaks, peak_src = res["peaks"]
+    dom = kernel or max(per, key=lambda k: per[k]["ms"])
     d = per[dom]
-    if args.workload == "decode" or dom != "w8a8":
-        achieved = d["bytes"] / d["launches"] / (d["ms"] / d["launches"] / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_source": f"{peak_src} hbm_gbs",
-                "kernel": dom}
-        per_launch_bytes = d["bytes"] / d["launches"]
-    else:
+    per_launch_bytes = d["bytes"] / d["launches"]
+    if (part, dom) in TENSOR_CLASSES:
         achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
-                "frac": achieved / tflops_peak,
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
                 "peak_source": f"{peak_src} bf16_tflops burst (fp16 kind::f16 pipe, nominal ratio 1)",
                 "kernel": dom}
-        per_launch_bytes = d["bytes"] / d["launches"]
-    roof["traffic"] = ncu_traffic(dom, args.workload)
-    roof["algorithmic_bytes_per_launch"] = per_launch_bytes
-
-    if args.workload == "decode":
-        value = world * wl.step_bytes / (ms_step / 1e3) / 1e9
-        unit = "GB/s"
     else:
-        value = world * wl.step_flops / (ms_step / 1e3) / 1e12
-        unit = "TOPS"
+        achieved = per_launch_bytes / (d["ms"] / d["launches"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs", "kernel": dom}
+    roof["traffic"] = ncu_traffic(dom, part)
+    roof["algorithmic_bytes_per_launch"] = per_launch_bytes
+    return roof
 
-    # end to end through the public API: pinned host inputs in, results out
-    e2e = run_e2e(args, wl, stream, g_warm if use_graph else None, world)
 
+def run_ours(args, world, rank, local):
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device)
+    parts = ("decode", "prefill", "sweep8b") if args.workload == "all" else (args.workload,)
+    results = {}
+    for part in parts:
+        results[part] = time_part(part, args, world, local, stream)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    top = parts[0]
+    r = results[top]
+    wl = r["wl"]
+    if top == "prefill":
+        value, unit = world * wl.step_flops({"w8a8"}) / (r["ms_step"] / 1e3) / 1e12, "TOPS"
+    else:
+        value, unit = world * wl.step_bytes / (r["ms_step"] / 1e3) / 1e9, "GB/s"
+    reasons = sorted({x for res in results.values() for x in res["clocks"].get("reasons", [])})
+    clocks = dict(r["clocks"])
+    clocks["reasons"] = reasons
     line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": workload_name(args.workload), "parallelism": f"replicas x{world}",
+        "config": {"workload": " + ".join(workload_name(p) for p in parts), "parallelism": f"replicas x{world}",
+                   "top_level": workload_name(top),
                    "l2": "inputs larger than L2: every GEMM launch reads its own weight copy, "
-                         ">1 GB touched per step",
-                   "graph": use_graph},
-        "roofline": roof,
-        "kernels": kernels,
-        "gpu_launches": n_launch * steps,
-        "clocks": clk,
-        "e2e": e2e,
+                         ">1 GB touched per step of each part",
+                   "graph": r["graph"]},
+        "roofline": roofline(top, r),
+        "kernels": r["kernels"],
+        "gpu_launches": sum(res["launches"] for res in results.values()),
+        "clocks": clocks,
+        "e2e": r["e2e"],
     }
+    if "prefill" in results and top != "prefill":
+        p = results["prefill"]
+        tops = world * p["wl"].step_flops({"w8a8"}) / (p["ms_step"] / 1e3) / 1e12
+        line["prefill"] = {"workload": workload_name("prefill"), "value": tops, "unit": "TOPS",
+                           "ms_per_step": p["ms_step"], "roofline": roofline("prefill", p),
+                           "kernels": p["kernels"], "e2e": p["e2e"], "clocks": p["clocks"],
+                           "gpu_launches": p["launches"]}
+    if "sweep8b" in results:
+        sw = results["sweep8b"]
+        block = {"workload": workload_name("sweep8b"), "ms_per_step": sw["ms_step"], "kernels": sw["kernels"],
+                 "e2e": sw["e2e"], "clocks": sw["clocks"], "gpu_launches": sw["launches"],
+                 "roofline": {k: roofline("sweep8b", sw, k) for k in sw["per"]}}
+        dec = [l for l in sw["wl"].launches if l.kernel != "w8a8_prefill"]
+        pre = [l for l in sw["wl"].launches if l.kernel == "w8a8_prefill"]
+        ms_dec = sum(sw["per"][k]["ms"] for k in ("w8a16", "w8a8_decode")) / args.steps
+        ms_pre = sw["per"]["w8a8_prefill"]["ms"] / args.steps
+        block["decode_GB/s"] = world * sum(l.bytes for l in dec) / (ms_dec / 1e3) / 1e9
+        block["prefill_TOPS"] = world * sum(l.flops for l in pre) / (ms_pre / 1e3) / 1e12
+        if top == "sweep8b":
+            line.update({k: v for k, v in block.items() if k in ("kernels",)})
+        else:
+            line["qwen3_8b_sweep"] = block
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
-        frac = args.cpu_row_frac if args.cpu_row_frac is not None else (1.0 if args.workload == "decode" else 1 / 8)
-        sample = build_oracle_sample(args.workload, frac)
-        b, o, s, passes = 0, 0, 0.0, 0
-        while passes < 3 and (passes == 0 or s < 10.0):
-            bb, oo, ss = oracle_step(sample)
-            b, o, s, passes = b + bb, o + oo, s + ss, passes + 1
-        rate, unit = oracle_rate(args.workload, b, o, s)
-        scope = ("the whole workload" if frac >= 1 else
-                 f"the workload with every weight cut to {frac:.4g} of its output rows"
-                 + (" and every M to the same fraction" if args.workload == "prefill" else ""))
-        line["cpu_baseline"] = {
-            "value": rate, "unit": unit, "cores": 1, "kind": "oracle",
-            "sample": f"{passes} pass(es) of {scope}; {s:.1f} s single-threaded"}
+        frac = args.cpu_row_frac if args.cpu_row_frac is not None else (1 / 2 if top == "decode" else 1 / 8)
+        cpu_part = top if top != "sweep8b" else "decode"
+        line["cpu_baseline"] = cpu_baseline(cpu_part, frac)
+        if "prefill" in line:
+            line["prefill"]["cpu_baseline"] = cpu_baseline("prefill", 1 / 8)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
 
 
-def run_e2e(args, wl, stream, graph, world):
+def run_e2e(args, wl, stream, graph, world, part):
     """Same step through the public API with host buffers: H2D of every input
     from pinned memory, the step, D2H of every result, all inside the timed
     region."""
@@ -626,12 +766,10 @@ def run_e2e(args, wl, stream, graph, world):
         end.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(start.elapsed_time(end), world) / steps
-    if wl.kind == "decode":
-        value = world * wl.step_bytes / (ms / 1e3) / 1e9
-        unit = "GB/s"
+    if part == "prefill":
+        value, unit = world * wl.step_flops({"w8a8"}) / (ms / 1e3) / 1e12, "TOPS"
     else:
-        value = world * wl.step_flops / (ms / 1e3) / 1e12
-        unit = "TOPS"
+        value, unit = world * wl.step_bytes / (ms / 1e3) / 1e9, "GB/s"
     return {"value": value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps}
 
@@ -645,7 +783,7 @@ def run_single(args, local):
     parts = args.single.split(":")
     kind, dims = parts[0], [int(v) for v in parts[1:]]
     l2 = 256 << 20
-    if kind in ("w8a8", "w8a16"):
+    if kind in ("w8a8", "w8a16", "linear"):
         m, n, k = dims
         copies = max(1, -(-l2 // (n * k)))
         w = synthetic.weight(n, k, 1, device=dev)
@@ -658,6 +796,9 @@ def run_single(args, local):
         if kind == "w8a8":
             fns = [lambda q=q: capi.w8a8_gemm(qx, sx, q, s, y=y) for q in qs]
             nbytes, flops = bytes_w8a8(m, n, k, False), 2 * m * n * k
+        elif kind == "linear":
+            fns = [lambda q=q: capi.w8a8_linear(x, q, s, y=y) for q in qs]
+            nbytes, flops = bytes_quant(m, k) + bytes_w8a8(m, n, k, False), 2 * m * n * k
         else:
             fns = [lambda q=q: capi.w8a16_gemm(x, q, s, y=y) for q in qs]
             nbytes, flops = bytes_w8a16(m, n, k), 2 * m * n * k
@@ -696,14 +837,15 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
+    ap.add_argument("--workload", choices=["all", "decode", "prefill", "sweep8b"], default="all")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-row-frac", type=float, default=None,
-                    help="row fraction of the cpu_baseline sample (default: 1 for decode, 1/8 for prefill)")
+                    help="row fraction of the cpu_baseline sample (default: 1/2 for decode, 1/8 for prefill)")
     ap.add_argument("--ref-row-frac", type=float, default=1 / 8)
     ap.add_argument("--single", default=None,
-                    help="time one kernel: w8a8:M:N:K, w8a16:M:N:K or quant:R:K (eager, for profiling)")
+                    help="time one kernel: w8a8:M:N:K, linear:M:N:K, w8a16:M:N:K or quant:R:K "
+                         "(eager, for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

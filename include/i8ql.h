@@ -104,6 +104,13 @@ i8ql_status quantize_act_per_token_int8(const i8ql_bf16* x, int64_t M, int64_t K
  * the tokens, 2*M*K bytes, plus, when the plan runs stream-K (see
  * i8ql_w8a8_plan), one int32 partial tile of 128 x 256 per CTA pair half
  * (128 KiB per CTA, about 19 MiB on 152 SMs) and a flag per CTA.
+ * Stream-K hands partial tiles from lower-numbered CTA pairs to higher ones:
+ * a pair waits only for pairs dispatched before it, which park their part
+ * before they wait for anything.  Its grid is sized to the pairs that fit on
+ * the device at once; it relies on the hardware dispatching a grid's CTAs in
+ * order (a later pair is never resident while an earlier one waits to be
+ * scheduled).  A wait that still runs out (1 s) records I8QL_ERR_TIMEOUT and
+ * leaves the tile unstored.
  */
 i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                       const i8ql_bf16* bias, i8ql_bf16* y, int32_t* acc_debug,
@@ -216,10 +223,10 @@ i8ql_status w8a8_gemm_noalloc(const int8_t* qx, const float* sx, const int8_t* q
  * CTAs on two SMs share 256-row tiles through one two-SM MMA (0: one CTA per
  * 128-row tile), 2 when such pairs also run stream-K: every pair takes an
  * equal share of all (tile, k-block) steps, and a tile cut between pairs is
- * finished by the pair holding its first k-block, which adds the others'
- * exact int32 partial sums (w8a8_gemm and w8a8_linear only: the stream-K
- * workspace is part of their temporary allocation).  Same argument rules as
- * w8a8_gemm; the outputs are HOST pointers.
+ * finished by the pair holding its last k-block, which adds the earlier
+ * pairs' exact int32 partial sums (w8a8_gemm and w8a8_linear only: the
+ * stream-K workspace is part of their temporary allocation).  Same argument
+ * rules as w8a8_gemm; the outputs are HOST pointers.
  */
 i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k,
                            int32_t* cta_pair);
@@ -244,6 +251,18 @@ const char* i8ql_status_string(i8ql_status status);
 
 /* Library version as major * 10000 + minor * 100 + patch. */
 int32_t i8ql_version(void);
+
+/*
+ * Test hook, no counterpart on the pages: exercises the timeout path of the
+ * stream-K hand-over without faulting or hanging anything.  While `on` is
+ * nonzero (process-wide), every stream-K finisher launched by w8a8_gemm or
+ * w8a8_linear waits for a flag value that no CTA ever writes, with a 1 ms
+ * limit instead of 1 s: the wait runs out, the CTA records I8QL_ERR_TIMEOUT
+ * in the sticky word, leaves the tiles it finishes unstored and exits
+ * cleanly (its other work, and every other CTA's, is unaffected).  Only
+ * tests should call it; calls with it off behave exactly as before.
+ */
+void i8ql_debug_stream_k_timeout(int32_t on);
 
 #ifdef __cplusplus
 }

@@ -44,6 +44,7 @@ SIGNATURES = {
     "i8ql_get_device_error": (_S, [_P]),
     "i8ql_status_string": (ctypes.c_char_p, [_S]),
     "i8ql_version": (_S, []),
+    "i8ql_debug_stream_k_timeout": (None, [_S]),
 }
 
 _LIB = None
@@ -265,3 +266,9 @@ def i8ql_get_device_error(stream=None) -> int:
 
 def i8ql_version() -> int:
     return int(lib().i8ql_version())
+
+
+def i8ql_debug_stream_k_timeout(on: bool) -> None:
+    """Test hook: while on, stream-K finishers wait for a flag nothing writes
+    (1 ms limit), so the call records I8QL_ERR_TIMEOUT without hanging."""
+    lib().i8ql_debug_stream_k_timeout(1 if on else 0)

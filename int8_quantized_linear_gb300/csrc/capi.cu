@@ -28,6 +28,7 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
+std::atomic<int> g_debug_sk_timeout{0};
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -64,6 +65,8 @@ i8ql_status check_vec(const void* p, int64_t n, uintptr_t align) {
 i8ql_status from_cuda(cudaError_t e) { return e == cudaSuccess ? I8QL_OK : I8QL_ERR_CUDA; }
 
 }  // namespace
+
+bool debug_sk_timeout() { return g_debug_sk_timeout.load(std::memory_order_relaxed) != 0; }
 
 bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status) {
     int dev = -1;
@@ -284,6 +287,8 @@ const char* i8ql_status_string(i8ql_status status) {
     }
 }
 
-int32_t i8ql_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int32_t i8ql_version(void) { return 1 * 10000 + 1 * 100 + 0; }
+
+void i8ql_debug_stream_k_timeout(int32_t on) { g_debug_sk_timeout.store(on != 0 ? 1 : 0, std::memory_order_relaxed); }
 
 }  // extern "C"

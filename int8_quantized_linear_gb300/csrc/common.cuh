@@ -93,6 +93,10 @@ struct LaunchEnv {
 // on first use.  Returns false (and sets *status) on failure.
 bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status);
 
+// Test hook (i8ql_debug_stream_k_timeout): stream-K finishers wait for a
+// flag value that is never written, with a 1 ms limit.
+bool debug_sk_timeout();
+
 // Kernel launchers.  They assume validated arguments.
 // W8A8 up to this many tokens runs on the decode kernel (int8 mma.sync,
 // weight streaming); larger M runs on the tcgen05 kernel.

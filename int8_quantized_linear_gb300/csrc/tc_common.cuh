@@ -36,14 +36,17 @@ struct W8A8Params {
     uint32_t tmem_cols;
     unsigned* err;
     // Stream-K (CTA pairs only): sk_units pairs share the tiles * nkb
-    // k-block iterations evenly; a pair whose range starts inside a tile
-    // parks that partial tile (int32, this CTA's 128 rows) in its slot of
-    // sk_part and counts it done in sk_flags (zeroed before the launch);
-    // the pair holding the tile's first k-block adds the parked partials.
+    // k-block iterations evenly; a pair whose range ends inside a tile parks
+    // that partial tile (int32, this CTA's 128 rows) in its slot of sk_part
+    // and counts it done in sk_flags (zeroed before the launch); the pair
+    // holding the tile's last k-block adds the parked partials of the
+    // earlier pairs.
     int sk;
     int64_t sk_units;
     int32_t* sk_part;   // [sk_units][2][128 * bn] int32
     unsigned* sk_flags; // [sk_units][2]
+    unsigned sk_flag_target;  // flag value of a parked part (one count per epilogue thread)
+    uint64_t sk_wait_ns;      // limit of a finisher's wait for one parked part
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

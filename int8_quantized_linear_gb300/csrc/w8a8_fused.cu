@@ -89,6 +89,7 @@ constexpr int kSmemOptin = 232448;  // largest dynamic shared memory of one CTA 
 constexpr int kMaxStages8 = 8;
 constexpr int kMaxStagesOp = 4;
 constexpr int kCtlBytes = 5120;  // barriers + two sets of staged epilogue parameters
+constexpr uint64_t kAbortDrainNs = 50000;  // pause of a CTA that gave up, before it releases its resources
 
 // Shared-memory rings of one CTA for tile width BN (all stages 1024-byte
 // aligned), with W = BN weight rows per CTA, or BN / 2 for a CTA pair:
@@ -325,9 +326,13 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 // Persistent: tiles unit, unit + step, ... each over the unit's split-K
 // range [kb_lo, kb_hi).  Stream-K: the iterations [total * u / U,
 // total * (u + 1) / U) of the tile-major order (total = tiles * nkb), cut
-// at tile boundaries.  Every role walks the same sequence.
+// at tile boundaries and walked from the END of the range backwards: the
+// first segment a unit processes is the head of a tile that later units
+// finish (it is parked at once), the last one is the tail of a tile whose
+// head earlier units parked long before.  Every role walks the same
+// sequence.
 struct Work {
-    int64_t cur, end, step;
+    int64_t cur, end, step;  // stream-K: cur is the range start, end moves down
     int kb_lo, kb_hi, nkb;
     bool sk;
 
@@ -340,10 +345,11 @@ struct Work {
             cur += step;
             return true;
         }
-        tile = cur / nkb;
-        lo = (int)(cur - tile * nkb);
-        hi = (int)min((int64_t)nkb, end - tile * nkb);
-        cur = tile * nkb + hi;
+        tile = (end - 1) / nkb;
+        const int64_t t0 = tile * nkb;
+        lo = (int)(max(cur, t0) - t0);
+        hi = (int)(end - t0);
+        end = t0 + lo;
         return true;
     }
     // k-blocks of the whole sequence
@@ -538,10 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[q] = make_int4(run[4 * q], run[4 * q + 1], run[4 * q + 2], run[4 * q + 3]);
                 continue;
             }
-            if (PAIR && p.sk && seg_lo > 0) {
-                // Stream-K, a later part of the tile: park it for the tile's
-                // owner (coalesced: consecutive lanes, consecutive rows) and
-                // count this thread's stores done with a release.
+            if (PAIR && p.sk && seg_hi < nkb) {
+                // Stream-K, a part of a tile finished by a later unit (the
+                // first segment this unit processes): park it for the
+                // finisher (coalesced: consecutive lanes, consecutive rows)
+                // and count this thread's stores done with a release.
                 int4* slot = reinterpret_cast<int4*>(p.sk_part + (unit0 * 2 + prank) * (int64_t)(kBM * BN));
 #pragma unroll
                 for (int q = 0; q < kHalf / 4; ++q)
@@ -552,20 +559,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&ctl->epi_free[eb]);
                 continue;
             }
-            if (PAIR && p.sk && seg_hi < nkb) {
-                // Stream-K, the tile's owner (it holds k-block 0): add the
-                // parts parked by the units after this one, in unit order.
-                // Those units run their part first, so this wait is short.
+            if (PAIR && p.sk && seg_lo > 0) {
+                // Stream-K, the tile's finisher (it holds the last k-block;
+                // this is the last segment it processes): add the parts
+                // parked by the earlier units whose ranges reach into the
+                // tile.  Each parked its part as the first segment it
+                // processed, before waiting for anything itself, and was
+                // dispatched no later than this unit, so the wait is short
+                // and never depends on a unit that is not resident yet.
                 const int64_t total = tiles * nkb;
-                const int64_t tile_end = (tile + 1) * nkb;
-                for (int64_t q = unit0 + 1; q < p.sk_units && sk_first(total, q, p.sk_units) < tile_end; ++q) {
+                const int64_t tile_start = tile * nkb;
+                for (int64_t q = unit0 - 1; q >= 0 && sk_first(total, q + 1, p.sk_units) > tile_start; --q) {
+                    if (sk_first(total, q, p.sk_units) == sk_first(total, q + 1, p.sk_units)) continue;  // no work
                     const unsigned* f = p.sk_flags + q * 2 + prank;
                     const uint64_t t0 = global_ns();
                     while (true) {
-                        const bool seen = ld_acquire_gpu(f) >= (unsigned)(kEpiWarps * 32);
+                        const bool seen = ld_acquire_gpu(f) >= p.sk_flag_target;
                         if (__all_sync(0xffffffffu, seen)) break;
                         const bool give_up =
-                            *reinterpret_cast<volatile int*>(abort) != 0 || global_ns() - t0 > kWaitLimitNs;
+                            *reinterpret_cast<volatile int*>(abort) != 0 || global_ns() - t0 > p.sk_wait_ns;
                         if (__any_sync(0xffffffffu, give_up)) {
                             alive = false;
                             break;
@@ -781,6 +793,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) {
+        // A CTA that gave up may still have bulk copies in flight into its
+        // shared memory (at most one k-block per ring stage, tens of KB);
+        // they land within microseconds, so a fixed pause lets them complete
+        // before the CTA's shared memory and TMEM are released.
+        if (threadIdx.x == 0) {
+            const uint64_t t0 = global_ns();
+            while (global_ns() - t0 < kAbortDrainNs) __nanosleep(1000);
+        }
+        __syncthreads();
+    }
     tc_fence_after();
     if constexpr (PAIR) {
         // Neither CTA leaves (or frees TMEM) while the pair's MMAs, TMA
@@ -1140,6 +1163,14 @@ cudaError_t launch_w8a8_fused(const uint16_t* x16, const float* sx, const int8_t
     p.rows_a = p.swap ? N : M;
     p.rows_b = p.swap ? M : N;
     p.tmem_cols = pow2_cols(2 * p.bn);  // two fp32 chunk buffers
+    p.sk_flag_target = kEpiWarps * 32;
+    p.sk_wait_ns = kWaitLimitNs;
+    if (debug_sk_timeout()) {
+        // test hook: finishers wait for a flag value no unit ever writes,
+        // with a short limit, so that the bounded wait runs out
+        p.sk_flag_target = 0xffffffffu;
+        p.sk_wait_ns = 1000000ull;
+    }
     if (plan.sk) {
         // flags first (zeroed by the launch before this one), then the
         // partial tiles

@@ -36,6 +36,7 @@ def load(path: str):
     lib.oracle_grouped_w8a16.argtypes = [p, p, i64, p, p, i64, i64, i64, p]
     lib.oracle_narrow_bf16.argtypes = [p, i64, p]
     lib.oracle_narrow_bf16.restype = None
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
     return lib
 
 
@@ -169,3 +170,9 @@ def narrow_bf16(f32) -> np.ndarray:
 def widen_bf16(bits) -> np.ndarray:
     """bf16 bits -> float32 (exact)."""
     return (_c(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def set_threads(n: int = 0) -> int:
+    """Threads of the oracle's row loops (n <= 0: keep the current count);
+    returns the count in effect (1 in a build without OpenMP)."""
+    return int(_lib().oracle_set_threads(int(n)))

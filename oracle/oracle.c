@@ -10,7 +10,9 @@
  * precision the pages fix (fp32 for scales, exact integers for codes and
  * accumulators) or in fp64 where they fix none.  Build flags:
  * -O2 -ffp-contract=off -fno-fast-math, so that no multiply-add is fused
- * and no denormal is flushed.
+ * and no denormal is flushed.  With OpenMP the outer loop over output rows
+ * is shared among threads; every output is still computed by one thread in
+ * the same order, so results do not depend on the thread count.
  *
  * Sources, cited by page title and section:
  *  [Q]  "Day 6 -- Quantize It Yourself", The mechanism, block 1: a stored
@@ -41,12 +43,27 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_NONFINITE 1
 #define ORACLE_ERR_ARG 2
 #define ORACLE_ERR_OVERFLOW 3
 #define ORACLE_ERR_OFFSETS 4
+
+/* Threads of the row loops (all cores by default); returns the count in
+ * effect, 1 in a build without OpenMP. */
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* bf16 is the top half of an IEEE binary32; widening is exact. */
 static float widen_bf16(uint16_t b) {
@@ -88,13 +105,14 @@ static float round_half_even(float t) {
 int oracle_quant_rows(const uint16_t* src, int64_t rows, int64_t k,
                       int8_t* q, float* s) {
     if (rows < 0 || k < 0) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < rows * k; ++i)
+        if (!isfinite(widen_bf16(src[i]))) return ORACLE_ERR_NONFINITE;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
         const uint16_t* row = src + r * k;
         float a = 0.0f;
         for (int64_t j = 0; j < k; ++j) {
-            float v = widen_bf16(row[j]);
-            if (!isfinite(v)) return ORACLE_ERR_NONFINITE;
-            float av = fabsf(v);
+            float av = fabsf(widen_bf16(row[j]));
             if (av > a) a = av;
         }
         float scale = (a == 0.0f) ? 1.0f : a / 127.0f;
@@ -114,6 +132,7 @@ int oracle_quant_rows(const uint16_t* src, int64_t rows, int64_t k,
 int oracle_int_acc(const int8_t* qx, const int8_t* qw, int64_t m_rows,
                    int64_t n_rows, int64_t k, int64_t* acc) {
     if (m_rows < 0 || n_rows < 0 || k < 0) return ORACLE_ERR_ARG;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t m = 0; m < m_rows; ++m)
         for (int64_t n = 0; n < n_rows; ++n) {
             int64_t sum = 0;
@@ -142,13 +161,18 @@ static int w8a8_point(int64_t acc, float sx, float sw, const uint16_t* bias,
 int oracle_w8a8_epilogue(const int64_t* acc, const float* sx, const float* sw,
                          const uint16_t* bias, int64_t m_rows, int64_t n_rows,
                          float* f, uint16_t* y) {
+    int err = ORACLE_OK;
+#pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < m_rows; ++m)
         for (int64_t n = 0; n < n_rows; ++n) {
             int64_t i = m * n_rows + n;
             int rc = w8a8_point(acc[i], sx[m], sw[n], bias, n, &f[i], &y[i]);
-            if (rc) return rc;
+            if (rc) {
+#pragma omp atomic write
+                err = rc;
+            }
         }
-    return ORACLE_OK;
+    return err;
 }
 
 /* W8A8 at chosen output points (m = pm[i], n = pn[i]) of a large layer:
@@ -158,17 +182,23 @@ int oracle_w8a8_points(const int8_t* qx, const float* sx, const int8_t* qw,
                        int64_t n_rows, int64_t k, int64_t npts,
                        const int64_t* pm, const int64_t* pn, int64_t* acc,
                        float* f, uint16_t* y) {
+    for (int64_t i = 0; i < npts; ++i)
+        if (pm[i] < 0 || pm[i] >= m_rows || pn[i] < 0 || pn[i] >= n_rows) return ORACLE_ERR_ARG;
+    int err = ORACLE_OK;
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < npts; ++i) {
         int64_t m = pm[i], n = pn[i];
-        if (m < 0 || m >= m_rows || n < 0 || n >= n_rows) return ORACLE_ERR_ARG;
         int64_t sum = 0;
         for (int64_t j = 0; j < k; ++j)
             sum += (int64_t)qx[m * k + j] * (int64_t)qw[n * k + j];
         acc[i] = sum;
         int rc = w8a8_point(sum, sx[m], sw[n], bias, n, &f[i], &y[i]);
-        if (rc) return rc;
+        if (rc) {
+#pragma omp atomic write
+            err = rc;
+        }
     }
-    return ORACLE_OK;
+    return err;
 }
 
 /* Weight-only W8A16 as dequantize-then-matmul in fp64 [W8A16][Q]:
@@ -176,6 +206,7 @@ int oracle_w8a8_points(const int8_t* qx, const float* sx, const int8_t* qw,
 int oracle_w8a16(const uint16_t* x, const int8_t* q, const float* s,
                  int64_t m_rows, int64_t n_rows, int64_t k, double* y) {
     if (m_rows < 0 || n_rows < 0 || k < 0) return ORACLE_ERR_ARG;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t m = 0; m < m_rows; ++m)
         for (int64_t n = 0; n < n_rows; ++n) {
             double sum = 0.0;
@@ -192,9 +223,11 @@ int oracle_w8a16(const uint16_t* x, const int8_t* q, const float* s,
 int oracle_w8a16_points(const uint16_t* x, const int8_t* q, const float* s,
                         int64_t m_rows, int64_t n_rows, int64_t k, int64_t npts,
                         const int64_t* pm, const int64_t* pn, double* y) {
+    for (int64_t i = 0; i < npts; ++i)
+        if (pm[i] < 0 || pm[i] >= m_rows || pn[i] < 0 || pn[i] >= n_rows) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < npts; ++i) {
         int64_t m = pm[i], n = pn[i];
-        if (m < 0 || m >= m_rows || n < 0 || n >= n_rows) return ORACLE_ERR_ARG;
         double sum = 0.0;
         for (int64_t j = 0; j < k; ++j) {
             double w = (double)s[n] * (double)q[n * k + j];
@@ -218,6 +251,7 @@ int oracle_grouped_w8a16(const uint16_t* x, const int32_t* off, int64_t experts,
     for (int64_t e = 0; e < experts; ++e) {
         const int8_t* qe = q + e * n_rows * k;
         const float* se = s + e * n_rows;
+#pragma omp parallel for collapse(2) schedule(static)
         for (int64_t r = off[e]; r < off[e + 1]; ++r)
             for (int64_t n = 0; n < n_rows; ++n) {
                 double sum = 0.0;

@@ -369,6 +369,39 @@ def test_w8a8_stream_k_exact(m, n, k):
         assert np.array_equal(acc2, acc) and np.array_equal(y2, y)
 
 
+def test_w8a8_stream_k_timeout_is_reported_and_recoverable():
+    """The timeout path of the stream-K hand-over, without faulting or
+    hanging anything: with the test hook on, every finisher waits for a flag
+    value no CTA writes, with a 1 ms limit.  The call must record
+    I8QL_ERR_TIMEOUT in the sticky word and return; the parkers' and the
+    whole tiles' outputs are still written; the context stays usable and the
+    next call (hook off) is exact again."""
+    m, n, k = STREAM_K_SHAPES[0]
+    assert capi.i8ql_w8a8_plan(m, n, k)[2] == 2
+    qx, qw = _codes(m, k, 41), _codes(n, k, 42)
+    sx, sw = _scales(m, 43, 0.01, 1.0), _scales(n, 44)
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    args = (dev(torch.from_numpy(qx)), dev(torch.from_numpy(sx)), dev(torch.from_numpy(qw)), dev(torch.from_numpy(sw)))
+    acc = torch.full((m, n), -5, dtype=torch.int32, device="cuda")
+    capi.i8ql_debug_stream_k_timeout(True)
+    try:
+        capi.w8a8_gemm(*args, acc_debug=acc)
+        status = capi.i8ql_get_device_error()
+    finally:
+        capi.i8ql_debug_stream_k_timeout(False)
+    assert status == capi.I8QL_ERR_TIMEOUT
+    # tiles no finisher owns (whole tiles inside one pair's range) are exact
+    exact = qx.astype(np.float64) @ qw.astype(np.float64).T
+    got = acc.cpu().numpy()
+    done = got != -5
+    assert done.any() and not done.all()
+    assert np.array_equal(got[done].astype(np.float64), exact[done])
+    # the context is usable and the next call is exact
+    acc2, _ = gpu_w8a8(qx, sx, qw, sw)
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    assert np.array_equal(acc2.astype(np.float64), exact)
+
+
 @pytest.mark.parametrize("m,n,k", [(1, 256, 1024), (7, 300, 2064), (64, 513, 1040), (65, 640, 2560),
                                    (128, 2560, 2560), (300, 1000, 4160), (2048, 2560, 2560)])
 def test_w8a8_linear_matches_quantize_then_gemm(m, n, k):
@@ -460,18 +493,35 @@ def test_w8a16_qwen3_4b_decode_full(shape):
         check_w8a16(synthetic.activations(m, k, 10 + m), qw, sw)
 
 
-@pytest.mark.parametrize("m", [16, 64])
-def test_w8a16_qwen3_8b_sampled(m):
-    n, k = synthetic.QWEN3_8B_SHAPES["down"]
-    qw, sw = oracle.quant_rows(util.bits(synthetic.weight(n, k, 4)))
-    x = synthetic.activations(m, k, 4)
+_QWEN3_8B_WEIGHTS = {}
+
+
+def _qwen3_8b_weight(shape):
+    """Oracle codes and scales of one Qwen3-8B projection (seed 4), cached."""
+    if shape not in _QWEN3_8B_WEIGHTS:
+        n, k = synthetic.QWEN3_8B_SHAPES[shape]
+        _QWEN3_8B_WEIGHTS[shape] = oracle.quant_rows(util.bits(synthetic.weight(n, k, 4)))
+    return _QWEN3_8B_WEIGHTS[shape]
+
+
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("shape", list(synthetic.QWEN3_8B_SHAPES))
+def test_w8a16_qwen3_8b_full(shape, m):
+    """The W8A16 arm of the Qwen3-8B sweep: every projection at every decode
+    M (each changes the token tile and the split-K / grid choice), the whole
+    output against the fp64 oracle.  The relative Frobenius bar is taken over
+    the whole output, as stated: on a few thousand sampled points the bf16
+    rounding of the exact result alone can exceed 2e-3 (2.008e-3 on one such
+    sample of o at M = 4, against 1.70e-3 over the full output)."""
+    n, k = synthetic.QWEN3_8B_SHAPES[shape]
+    qw, sw = _qwen3_8b_weight(shape)
+    x = synthetic.activations(m, k, 4 + m)
     y = gpu_w8a16(x, qw, sw)
-    pm, pn = _points(m, n, 4000, m)
     xb = util.bits(x)
-    ref = oracle.w8a16_points(xb, qw, sw, pm, pn)
-    assert util.rel_frobenius(y[pm, pn], ref) <= W8A16_FROB
+    ref = oracle.w8a16(xb, qw, sw)
+    assert util.rel_frobenius(y, ref) <= W8A16_FROB
     ax, aq = _abs_inputs(xb, qw)
-    check_elementwise(y[pm, pn], ref, oracle.w8a16_points(ax, aq, sw, pm, pn), k)
+    check_elementwise(y, ref, oracle.w8a16(ax, aq, sw), k)
 
 
 # ------------------------------------------------------------------ grouped W8A16

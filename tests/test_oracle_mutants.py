@@ -33,7 +33,7 @@ MUTANTS = {
     # (The clamp to [-127, 127] is never active: with s = fl32(a / 127) the
     # quotient stays within 127 * (1 + 2^-23), so removing it is an
     # equivalent mutant and is not listed.)
-    "signed_max_not_absmax": ("float av = fabsf(v);", "float av = v;"),
+    "signed_max_not_absmax": ("float av = fabsf(widen_bf16(row[j]));", "float av = widen_bf16(row[j]);"),
     "transposed_weight_operand": (
         "acc[m * n_rows + n] = sum;",
         "acc[n * m_rows + m] = sum;"),
