@@ -44,6 +44,7 @@ __all__ = [
     "outlier_channels",
     "tiny_layer",
     "moe_routing",
+    "gate_logits",
     "MoeRouting",
     "bf16_bits",
 ]
@@ -153,11 +154,18 @@ class MoeRouting:
         return int(self.offsets[-1])
 
 
+def gate_logits(tokens: int, routed: int, seed: int) -> torch.Tensor:
+    """fp32 ``[tokens, routed]`` gate logits ~ N(0, 1), seeded."""
+    g = _gen(seed)
+    return torch.randn((tokens, routed), generator=g, dtype=torch.float32)
+
+
 def moe_routing(tokens: int, seed: int, routed: int = DSMOE_ROUTED,
                 shared: int = DSMOE_SHARED, topk: int = DSMOE_TOPK) -> MoeRouting:
-    """Seeded top-k routing plus shared experts, rows grouped by expert."""
-    g = _gen(seed)
-    logits = torch.randn((tokens, routed), generator=g, dtype=torch.float32).double().numpy()
+    """Seeded top-k routing plus shared experts, rows grouped by expert: the
+    input recipe of the grouped GEMM's benchmark and parity cases (numpy;
+    the oracle's routing of the MoE layer is written independently)."""
+    logits = gate_logits(tokens, routed, seed).double().numpy()
     z = logits - logits.max(axis=1, keepdims=True)
     p = np.exp(z)
     p /= p.sum(axis=1, keepdims=True)

@@ -20,6 +20,7 @@ _ERRORS = {
     2: "bad argument",
     3: "accumulator outside int32",
     4: "bad group offsets",
+    5: "a nonzero group's scale underflows bf16",
 }
 
 
@@ -37,6 +38,25 @@ def load(path: str):
     lib.oracle_narrow_bf16.argtypes = [p, i64, p]
     lib.oracle_narrow_bf16.restype = None
     lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_fp8_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_fp8_decode.restype = ctypes.c_float
+    lib.oracle_fp8_encode.argtypes = [ctypes.c_float]
+    lib.oracle_fp8_encode.restype = ctypes.c_uint8
+    lib.oracle_fp8_encode_array.argtypes = [p, i64, p]
+    lib.oracle_fp8_encode_array.restype = None
+    lib.oracle_fp8_decode_array.argtypes = [p, i64, p]
+    lib.oracle_fp8_decode_array.restype = None
+    lib.oracle_quant_rows_fp8.argtypes = [p, i64, i64, p, p]
+    lib.oracle_w8a8_fp8_points.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, p, p, p]
+    lib.oracle_quant_w4_g128.argtypes = [p, i64, i64, p, p]
+    lib.oracle_w4_unpack.argtypes = [p, i64, i64, p]
+    lib.oracle_w4_unpack.restype = None
+    lib.oracle_w4a16.argtypes = [p, p, p, i64, i64, i64, p]
+    lib.oracle_moe_route.argtypes = [p, i64, i64, i64, i64, p, p, p, p, p]
+    lib.oracle_silu_mul.argtypes = [p, i64, i64, p]
+    lib.oracle_silu_mul.restype = None
+    lib.oracle_moe_combine.argtypes = [p, p, p, i64, i64, i64, p]
+    lib.oracle_moe_combine.restype = None
     return lib
 
 
@@ -176,3 +196,136 @@ def set_threads(n: int = 0) -> int:
     """Threads of the oracle's row loops (n <= 0: keep the current count);
     returns the count in effect (1 in a build without OpenMP)."""
     return int(_lib().oracle_set_threads(int(n)))
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+
+def fp8_encode(v) -> np.ndarray:
+    """E4M3 codes (uint8) of fp32 values: nearest, ties to even, saturating."""
+    f = _c(v, np.float32)
+    out = np.empty(f.shape, np.uint8)
+    _lib().oracle_fp8_encode_array(_ptr(f), f.size, _ptr(out))
+    return out
+
+
+def fp8_decode(c) -> np.ndarray:
+    """fp32 values of E4M3 codes (exact)."""
+    c = _c(c, np.uint8)
+    out = np.empty(c.shape, np.float32)
+    _lib().oracle_fp8_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def quant_rows_fp8(src_bf16):
+    """Per-row E4M3 codes (uint8) and fp32 scales (absmax / 448) of bf16 [R, K]."""
+    src = _c(src_bf16, np.uint16)
+    rows, k = src.shape
+    q = np.empty((rows, k), np.uint8)
+    s = np.empty((rows,), np.float32)
+    _check(_lib().oracle_quant_rows_fp8(_ptr(src), rows, k, _ptr(q), _ptr(s)))
+    return q, s
+
+
+def w8a8_fp8_points(qx, sx, qw, sw, bias_bf16, pm, pn):
+    """FP8 W8A8 at output points: (exact fp64 dot products, fp64 outputs)."""
+    qx, qw = _c(qx, np.uint8), _c(qw, np.uint8)
+    m, k = qx.shape
+    n = qw.shape[0]
+    sx, sw = _c(sx, np.float32), _c(sw, np.float32)
+    b = None if bias_bf16 is None else _c(bias_bf16, np.uint16)
+    pm, pn = _c(pm, np.int64), _c(pn, np.int64)
+    acc = np.empty(pm.shape[0], np.float64)
+    y = np.empty(pm.shape[0], np.float64)
+    _check(_lib().oracle_w8a8_fp8_points(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(b), m, n, k,
+                                         pm.shape[0], _ptr(pm), _ptr(pn), _ptr(acc), _ptr(y)))
+    return acc, y
+
+
+def w8a8_fp8(qx, sx, qw, sw, bias_bf16=None):
+    """FP8 W8A8 over the whole [M, N] output: (exact acc, fp64 y)."""
+    m, n = np.asarray(qx).shape[0], np.asarray(qw).shape[0]
+    pm, pn = np.meshgrid(np.arange(m), np.arange(n), indexing="ij")
+    acc, y = w8a8_fp8_points(qx, sx, qw, sw, bias_bf16, pm.ravel(), pn.ravel())
+    return acc.reshape(m, n), y.reshape(m, n)
+
+
+# ---------------------------------------------------------------- W4A16, group 128
+
+def quant_w4_g128(src_bf16):
+    """Packed int4 codes [R, K/2] (uint8) and bf16 group scales [R, K/128]."""
+    src = _c(src_bf16, np.uint16)
+    rows, k = src.shape
+    packed = np.empty((rows, k // 2), np.uint8)
+    scale = np.empty((rows, k // 128), np.uint16)
+    _check(_lib().oracle_quant_w4_g128(_ptr(src), rows, k, _ptr(packed), _ptr(scale)))
+    return packed, scale
+
+
+def w4_unpack(packed, k):
+    """Signed codes [R, K] of packed int4 storage."""
+    packed = _c(packed, np.uint8)
+    rows = packed.shape[0]
+    codes = np.empty((rows, k), np.int8)
+    _lib().oracle_w4_unpack(_ptr(packed), rows, k, _ptr(codes))
+    return codes
+
+
+def w4a16(x_bf16, packed, scale) -> np.ndarray:
+    """fp64 dequantize-then-matmul of the group-128 int4 weights."""
+    x = _c(x_bf16, np.uint16)
+    packed, scale = _c(packed, np.uint8), _c(scale, np.uint16)
+    m, k = x.shape
+    n = packed.shape[0]
+    y = np.empty((m, n), np.float64)
+    _check(_lib().oracle_w4a16(_ptr(x), _ptr(packed), _ptr(scale), m, n, k, _ptr(y)))
+    return y
+
+
+# ---------------------------------------------------------------- MoE expert MLP
+
+class Route:
+    """Routing of T tokens: sel/prob [T, topk], offsets [E + shared + 1],
+    row_token [rows], token_row [T, topk + shared], row_weight [rows]."""
+
+    def __init__(self, sel, prob, offsets, row_token, token_row, shared):
+        self.sel, self.prob, self.offsets = sel, prob, offsets
+        self.row_token, self.token_row = row_token, token_row
+        t, topk = sel.shape
+        self.slot_weight = np.concatenate([prob, np.ones((t, shared))], axis=1)  # [T, topk + shared]
+        self.row_weight = np.empty(row_token.shape[0], np.float64)
+        self.row_weight[token_row.ravel()] = self.slot_weight.ravel()
+
+
+def moe_route(logits, topk, shared) -> Route:
+    lg = _c(logits, np.float32)
+    t, e = lg.shape
+    s = topk + shared
+    sel = np.empty((t, topk), np.int32)
+    prob = np.empty((t, topk), np.float64)
+    offsets = np.empty(e + shared + 1, np.int32)
+    row_token = np.empty(t * s, np.int32)
+    token_row = np.empty((t, s), np.int32)
+    _check(_lib().oracle_moe_route(_ptr(lg), t, e, topk, shared, _ptr(sel), _ptr(prob), _ptr(offsets),
+                                   _ptr(row_token), _ptr(token_row)))
+    return Route(sel, prob, offsets, row_token, token_row, shared)
+
+
+def silu_mul(gu) -> np.ndarray:
+    """h = silu(gate) * up of a fused [rows, 2I] gate/up output (fp64)."""
+    gu = _c(gu, np.float64)
+    rows, two_i = gu.shape
+    h = np.empty((rows, two_i // 2), np.float64)
+    _lib().oracle_silu_mul(_ptr(gu), rows, two_i // 2, _ptr(h))
+    return h
+
+
+def moe_combine(yd, token_row, slot_weight) -> np.ndarray:
+    """out[t] = sum_s w[t, s] * yd[token_row[t, s]] (fp64)."""
+    yd = _c(yd, np.float64)
+    tr = _c(token_row, np.int32)
+    w = _c(slot_weight, np.float64)
+    t, s = tr.shape
+    h = yd.shape[1]
+    out = np.empty((t, h), np.float64)
+    _lib().oracle_moe_combine(_ptr(yd), _ptr(tr), _ptr(w), t, s, h, _ptr(out))
+    return out
