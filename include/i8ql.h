@@ -5,6 +5,8 @@
  * of LLM serving: per-output-channel weight quantization, per-token
  * activation quantization, the W8A8 GEMM with its scale/bias epilogue, the
  * weight-only W8A16 GEMM/GEMV, and the grouped W8A16 GEMM over MoE experts.
+ * Beside them: the fused W8A8 linear layer, FP8 E4M3 W8A8, and the calls
+ * declared after those.
  *
  * Conventions shared by every call:
  *  - Every pointer is a DEVICE pointer to a buffer the caller owns, allocates
@@ -177,6 +179,64 @@ i8ql_status w8a16_gemm(const i8ql_bf16* x, const int8_t* qw, const float* sw, i8
 i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64_t E,
                                const int8_t* qw, const float* sw, i8ql_bf16* y,
                                int64_t T_total, int64_t N, int64_t K, void* stream);
+
+/*
+ * FP8 E4M3 per-row quantization (weights per output channel, activations per
+ * token; the two entry points run the same arithmetic on different rows).
+ *
+ * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 2 (E4M3: sign,
+ * 4 exponent and 3 mantissa bits, largest value 448), block 1 (q =
+ * clamp(round(w / s)), s = absmax / largest representable value) and block 5
+ * with its FP8_DYNAMIC recipe (per-channel weights, dynamic per-token
+ * activations).
+ *
+ * For every row r of src (bf16 [R, K]):
+ *   a = max_k |src[r,k]|;  scale[r] = a / 448 (fp32 IEEE division), or 1 if a == 0;
+ *   q[r,k] = E4M3 code of (src[r,k] / scale[r]) (one IEEE fp32 division),
+ *            rounded to nearest with ties to the even code, saturated at
+ *            +-448, the sign of a value that rounds to zero kept.
+ * Code layout: bits s eeee mmm, exponent bias 7, no infinities (0x7f and
+ * 0xff are NaN and never produced).  Outputs: q uint8 [R, K], scale fp32 [R].
+ */
+i8ql_status quantize_weight_per_channel_fp8(const i8ql_bf16* w, int64_t N, int64_t K,
+                                            uint8_t* q, float* scale, void* stream);
+i8ql_status quantize_act_per_token_fp8(const i8ql_bf16* x, int64_t M, int64_t K,
+                                       uint8_t* q, float* scale, void* stream);
+
+/*
+ * FP8 E4M3 W8A8 GEMM on the tensor cores.
+ *
+ * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 5 (W8A8 with
+ * fp8 operands runs the GEMM on 8-bit tensor cores) and block 2 (E4M3).
+ *
+ *   acc[m,n] = sum_k e4m3(qx[m,k]) * e4m3(qw[n,k])      (fp32 accumulation)
+ *   y[m,n]   = bf16_rne((acc[m,n] * sx[m]) * sw[n] (+ (float)bias[n]))
+ * Inputs: qx uint8 [M, K] and qw uint8 [N, K] E4M3 codes (K-contiguous),
+ * sx fp32 [M], sw fp32 [N], bias bf16 [N] or NULL.  Output y bf16 [M, N].
+ * Every product of two E4M3 values is exact in fp32; the sum is accumulated
+ * in fp32 by the tensor core, so y differs from the exact value by fp32
+ * accumulation rounding and one bf16 rounding.  No workspace.  Argument
+ * rules and errors as w8a8_gemm.
+ */
+i8ql_status w8a8_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
+                          const i8ql_bf16* bias, i8ql_bf16* y, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * FP8 W8A8 linear layer from bf16 activations: quantize_act_per_token_fp8
+ * then w8a8_fp8_gemm in one call (bit-identical to the two calls).
+ *
+ * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 5 (the
+ * per-token activation quantization of W8A8 at run time).
+ *
+ * Inputs: x bf16 [M, K], qw uint8 [N, K], sw fp32 [N], bias bf16 [N] or NULL.
+ * Outputs: y bf16 [M, N]; qx uint8 [M, K] and sx fp32 [M] receive the token
+ * codes and scales when given (each may be NULL).  Takes a temporary
+ * stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on `stream`) for
+ * the codes and scales the caller does not keep: at most M*K + 4*M bytes.
+ */
+i8ql_status w8a8_fp8_linear(const i8ql_bf16* x, const uint8_t* qw, const float* sw, const i8ql_bf16* bias,
+                            i8ql_bf16* y, uint8_t* qx, float* sx, int64_t M, int64_t N, int64_t K,
+                            void* stream);
 
 /*
  * W8A8 GEMM that allocates nothing.

@@ -45,6 +45,10 @@ SIGNATURES = {
     "i8ql_status_string": (ctypes.c_char_p, [_S]),
     "i8ql_version": (_S, []),
     "i8ql_debug_stream_k_timeout": (None, [_S]),
+    "quantize_weight_per_channel_fp8": (_S, [_P, _I64, _I64, _P, _P, _P]),
+    "quantize_act_per_token_fp8": (_S, [_P, _I64, _I64, _P, _P, _P]),
+    "w8a8_fp8_gemm": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w8a8_fp8_linear": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
 }
 
 _LIB = None
@@ -272,3 +276,69 @@ def i8ql_debug_stream_k_timeout(on: bool) -> None:
     """Test hook: while on, stream-K finishers wait for a flag nothing writes
     (1 ms limit), so the call records I8QL_ERR_TIMEOUT without hanging."""
     lib().i8ql_debug_stream_k_timeout(1 if on else 0)
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+
+def _quant_fp8(fn_name: str, src: torch.Tensor, q, scale, stream):
+    if src.dim() != 2:
+        raise ValueError("input must be 2-D [rows, K]")
+    rows, k = src.shape
+    _need(src, torch.bfloat16, (rows, k), "input")
+    if q is None:
+        q = torch.empty((rows, k), dtype=torch.uint8, device=src.device)
+    if scale is None:
+        scale = torch.empty((rows,), dtype=torch.float32, device=src.device)
+    _need(q, torch.uint8, (rows, k), "q")
+    _need(scale, torch.float32, (rows,), "scale")
+    _check(getattr(lib(), fn_name)(_ptr(src), rows, k, _ptr(q), _ptr(scale), _stream(stream)), fn_name)
+    return q, scale
+
+
+def quantize_weight_per_channel_fp8(w: torch.Tensor, q=None, scale=None, stream=None):
+    """E4M3 codes [N, K] (uint8) and fp32 per-channel scales (absmax / 448)."""
+    return _quant_fp8("quantize_weight_per_channel_fp8", w, q, scale, stream)
+
+
+def quantize_act_per_token_fp8(x: torch.Tensor, q=None, scale=None, stream=None):
+    """E4M3 codes [M, K] (uint8) and fp32 per-token scales (absmax / 448)."""
+    return _quant_fp8("quantize_act_per_token_fp8", x, q, scale, stream)
+
+
+def w8a8_fp8_gemm(qx, sx, qw, sw, bias=None, y=None, stream=None):
+    """bf16 y [M, N] = ((sum_k e4m3(qx) e4m3(qw)) * sx[:, None]) * sw[None, :] (+ bias)."""
+    m, k = qx.shape
+    n = qw.shape[0]
+    _need(qx, torch.uint8, (m, k), "qx")
+    _need(sx, torch.float32, (m,), "sx")
+    _need(qw, torch.uint8, (n, k), "qw")
+    _need(sw, torch.float32, (n,), "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (n,), "bias")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=qw.device)
+    _need(y, torch.bfloat16, (m, n), "y")
+    _check(lib().w8a8_fp8_gemm(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y), m, n, k,
+                               _stream(stream)), "w8a8_fp8_gemm")
+    return y
+
+
+def w8a8_fp8_linear(x, qw, sw, bias=None, y=None, qx=None, sx=None, stream=None):
+    """bf16 y = w8a8_fp8_gemm(quantize_act_per_token_fp8(x), qw, sw, bias) in one call."""
+    m, k = x.shape
+    n = qw.shape[0]
+    _need(x, torch.bfloat16, (m, k), "x")
+    _need(qw, torch.uint8, (n, k), "qw")
+    _need(sw, torch.float32, (n,), "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (n,), "bias")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=qw.device)
+    _need(y, torch.bfloat16, (m, n), "y")
+    if qx is not None:
+        _need(qx, torch.uint8, (m, k), "qx")
+    if sx is not None:
+        _need(sx, torch.float32, (m,), "sx")
+    _check(lib().w8a8_fp8_linear(_ptr(x), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y), _ptr(qx), _ptr(sx), m, n, k,
+                                 _stream(stream)), "w8a8_fp8_linear")
+    return y

@@ -223,6 +223,64 @@ i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64
     return from_cuda(launch_w8a16(x, offsets, E, qw, sw, y, T_total, N, K, env));
 }
 
+i8ql_status quantize_weight_per_channel_fp8(const i8ql_bf16* w, int64_t N, int64_t K, uint8_t* q, float* scale,
+                                            void* stream) {
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_k(K));
+    I8QL_TRY(check_matrix(w, N));
+    I8QL_TRY(check_matrix(q, N));
+    I8QL_TRY(check_vec(scale, N, 4));
+    if (N == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_quant_rows_fp8(w, N, K, q, scale, env));
+}
+
+i8ql_status quantize_act_per_token_fp8(const i8ql_bf16* x, int64_t M, int64_t K, uint8_t* q, float* scale,
+                                       void* stream) {
+    return quantize_weight_per_channel_fp8(x, M, K, q, scale, stream);
+}
+
+i8ql_status w8a8_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
+                          const i8ql_bf16* bias, i8ql_bf16* y, int64_t M, int64_t N, int64_t K, void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_matrix(qx, M));
+    I8QL_TRY(check_vec(sx, M, 4));
+    I8QL_TRY(check_matrix(qw, N));
+    I8QL_TRY(check_vec(sw, N, 4));
+    if (bias != nullptr && !aligned(bias, 2)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_matrix(y, M));
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_fp8_gemm(qx, sx, qw, sw, bias, y, M, N, K, env));
+}
+
+i8ql_status w8a8_fp8_linear(const i8ql_bf16* x, const uint8_t* qw, const float* sw, const i8ql_bf16* bias,
+                            i8ql_bf16* y, uint8_t* qx, float* sx, int64_t M, int64_t N, int64_t K, void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_matrix(x, M));
+    I8QL_TRY(check_matrix(qw, N));
+    I8QL_TRY(check_vec(sw, N, 4));
+    if (bias != nullptr && !aligned(bias, 2)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_matrix(y, M));
+    if (qx != nullptr) I8QL_TRY(check_matrix(qx, M));
+    if (sx != nullptr && !aligned(sx, 4)) return I8QL_ERR_INVALID_ARG;
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_fp8_linear(x, qw, sw, bias, y, qx, sx, M, N, K, env));
+}
+
 i8ql_status i8ql_get_device_error(void* stream) {
     LaunchEnv env;
     i8ql_status s;

@@ -142,5 +142,14 @@ cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float*
 cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                         const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                         int64_t K, const LaunchEnv& env);
+// FP8 E4M3: per-row codes (s = absmax / 448), the tcgen05 kind::f8f6f4 GEMM,
+// and the linear layer from bf16 activations (quantization, then the GEMM).
+cudaError_t launch_quant_rows_fp8(const uint16_t* src, int64_t rows, int64_t K, uint8_t* q, float* s,
+                                  const LaunchEnv& env);
+cudaError_t launch_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
+                            const uint16_t* bias, uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env);
+cudaError_t launch_fp8_linear(const uint16_t* x, const uint8_t* qw, const float* sw, const uint16_t* bias,
+                              uint16_t* y, uint8_t* qx, float* sx, int64_t M, int64_t N, int64_t K,
+                              const LaunchEnv& env);
 
 }  // namespace i8ql

@@ -1,11 +1,12 @@
-// Per-row symmetric int8 quantization: per-output-channel weights and
-// per-token activations share this kernel.
+// Per-row symmetric quantization: per-output-channel weights and per-token
+// activations share this kernel, to int8 codes or to FP8 E4M3 codes.
 //
 // Sources: "Phase 5a: int8 weight-only quantization", Summary (per-output-
 // channel int8, float32 scale arithmetic, zero-channel guard only for
 // all-zero channels); "Day 6 -- Quantize It Yourself", The mechanism,
 // blocks 1, 4 and 5 (q = clamp(round(w / s)), s = absmax / 127, round to
-// nearest, per-token dynamic activation scales).
+// nearest, per-token dynamic activation scales) and block 2 (the E4M3 grid,
+// largest value 448: s = absmax / 448 for FP8 codes).
 //
 // One fused pass: each row is read once from HBM into registers (16-byte
 // vector loads), its absmax is reduced across the threads that own it, and
@@ -124,11 +125,29 @@ __device__ __forceinline__ uint4 load_nc(const uint4* p) {
     return v;
 }
 
+// E4M3 codes of 8 values (two words of bf16 pairs): v / s by IEEE division,
+// then the conversion instruction rounds to nearest even onto the E4M3 grid
+// and saturates at +-448 (satfinite), keeping the sign of zero.
+__device__ __forceinline__ uint2 codes8_fp8(const uint4& v, float s) {
+    const float x[8] = {lo_bf16(v.x), hi_bf16(v.x), lo_bf16(v.y), hi_bf16(v.y),
+                        lo_bf16(v.z), hi_bf16(v.z), lo_bf16(v.w), hi_bf16(v.w)};
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float t0 = __fdiv_rn(x[2 * i], s), t1 = __fdiv_rn(x[2 * i + 1], s);
+        uint16_t pair;
+        // the first source lands in the upper byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(t1), "f"(t0));
+        h[i] = pair;
+    }
+    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
 // TPR threads own one row; VPT > 0 keeps up to VPT 8-element vectors per
-// thread in registers, VPT == 0 streams the row twice.  The codes go to q
-// (int8) and/or qh (the same codes as fp16, for the tensor-core GEMM); either
-// may be null.
-template <int TPR, int VPT>
+// thread in registers, VPT == 0 streams the row twice.  INT8: the codes go to
+// q (int8) and/or qh (the same codes as fp16, for the tensor-core GEMM);
+// either may be null.  FP8 (E4M3, s = absmax / 448): the codes go to q.
+template <int TPR, int VPT, bool FP8>
 __global__ void __launch_bounds__(kQuantThreads)
 quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
                   int8_t* __restrict__ q, uint16_t* __restrict__ qh, float* __restrict__ scale, int one_wave,
@@ -184,9 +203,22 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
     }
 
     // Zero-channel guard: only an all-zero row is special.
-    const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 127.0f);
+    const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, FP8 ? 448.0f : 127.0f);
     if (!valid) return;
     if (lt == 0) scale[row] = s;
+    if constexpr (FP8) {
+        uint2* fp = reinterpret_cast<uint2*>(q + row * K);
+        if constexpr (VPT > 0) {
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int64_t idx = lt + (int64_t)i * TPR;
+                if (idx < nvec) fp[idx] = codes8_fp8(v[i], s);
+            }
+        } else {
+            for (int64_t idx = lt; idx < nvec; idx += TPR) fp[idx] = codes8_fp8(rp[idx], s);
+        }
+        return;
+    }
     RowScale rs;
     rs.s = s;
     rs.r = __frcp_rn(s);
@@ -214,32 +246,43 @@ quant_rows_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t K,
     }
 }
 
-template <int TPR, int VPT>
+template <int TPR, int VPT, bool FP8>
 cudaError_t launch_cfg(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
                        const LaunchEnv& env, unsigned* zero, int nzero) {
     constexpr int kRowsPerCta = kQuantThreads / TPR;
     const int64_t blocks = (rows + kRowsPerCta - 1) / kRowsPerCta;
     // one wave: every CTA resident at once (at least 2 per SM fit, 256 threads each)
     const int one_wave = blocks <= 2LL * env.sm_count ? 1 : 0;
-    return launch_kernel(quant_rows_kernel<TPR, VPT>, dim3((unsigned)blocks), dim3(kQuantThreads), 0, env.stream, kNoCluster,
-                         src, rows, K, q, qh, s, one_wave, zero, nzero);
+    return launch_kernel(quant_rows_kernel<TPR, VPT, FP8>, dim3((unsigned)blocks), dim3(kQuantThreads), 0, env.stream,
+                         kNoCluster, src, rows, K, q, qh, s, one_wave, zero, nzero);
+}
+
+template <bool FP8>
+cudaError_t launch_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
+                        const LaunchEnv& env, unsigned* zero, int nzero) {
+    // Threads per row and vectors per thread (measured on weight and
+    // activation shapes): many rows of moderate length go two warps to a
+    // row (more CTAs resident, no CTA barrier per row pair); long rows keep
+    // at most five vectors per thread, so that more CTAs fit on an SM.
+    const int64_t nvec = K / 8;
+    if (nvec <= 32 * 4) return launch_cfg<32, 4, FP8>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 64 * 6 && rows >= 4096) return launch_cfg<64, 6, FP8>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 128 * 4) return launch_cfg<128, 4, FP8>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 256 * 5) return launch_cfg<256, 5, FP8>(src, rows, K, q, qh, s, env, zero, nzero);
+    if (nvec <= 256 * 8) return launch_cfg<256, 8, FP8>(src, rows, K, q, qh, s, env, zero, nzero);
+    return launch_cfg<256, 0, FP8>(src, rows, K, q, qh, s, env, zero, nzero);
 }
 
 }  // namespace
 
 cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
                               const LaunchEnv& env, unsigned* zero, int nzero) {
-    // Threads per row and vectors per thread (measured on weight and
-    // activation shapes): many rows of moderate length go two warps to a
-    // row (more CTAs resident, no CTA barrier per row pair); long rows keep
-    // at most five vectors per thread, so that more CTAs fit on an SM.
-    const int64_t nvec = K / 8;
-    if (nvec <= 32 * 4) return launch_cfg<32, 4>(src, rows, K, q, qh, s, env, zero, nzero);
-    if (nvec <= 64 * 6 && rows >= 4096) return launch_cfg<64, 6>(src, rows, K, q, qh, s, env, zero, nzero);
-    if (nvec <= 128 * 4) return launch_cfg<128, 4>(src, rows, K, q, qh, s, env, zero, nzero);
-    if (nvec <= 256 * 5) return launch_cfg<256, 5>(src, rows, K, q, qh, s, env, zero, nzero);
-    if (nvec <= 256 * 8) return launch_cfg<256, 8>(src, rows, K, q, qh, s, env, zero, nzero);
-    return launch_cfg<256, 0>(src, rows, K, q, qh, s, env, zero, nzero);
+    return launch_rows<false>(src, rows, K, q, qh, s, env, zero, nzero);
+}
+
+cudaError_t launch_quant_rows_fp8(const uint16_t* src, int64_t rows, int64_t K, uint8_t* q, float* s,
+                                  const LaunchEnv& env) {
+    return launch_rows<true>(src, rows, K, reinterpret_cast<int8_t*>(q), nullptr, s, env, nullptr, 0);
 }
 
 }  // namespace i8ql

@@ -799,6 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // they land within microseconds, so a fixed pause lets them complete
         // before the CTA's shared memory and TMEM are released.
         if (threadIdx.x == 0) {
+            record_fault(p.err, kErrBitTimeout);  // on record however the flag was set
             const uint64_t t0 = global_ns();
             while (global_ns() - t0 < kAbortDrainNs) __nanosleep(1000);
         }

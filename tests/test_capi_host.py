@@ -169,3 +169,39 @@ def test_w8a8_linear_argument_errors(lib):
     assert f(*args) == capi.I8QL_OK                        # M = 0: nothing to do
     if not torch.cuda.is_available():
         assert f(*ok) == capi.I8QL_ERR_NO_DEVICE
+
+
+@pytest.mark.parametrize("fn", ["quantize_weight_per_channel_fp8", "quantize_act_per_token_fp8"])
+def test_fp8_quant_argument_errors(lib, fn):
+    f = getattr(lib, fn)
+    assert f(A, 4, 0, B, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, 4, 24, B, C, None) == capi.I8QL_ERR_UNSUPPORTED
+    assert f(None, 4, 16, B, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, 4, 16, B + 4, C, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(A, 4, 16, B, C + 2, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(None, 0, 16, None, None, None) == capi.I8QL_OK
+
+
+def test_fp8_gemm_and_linear_argument_errors(lib):
+    f = lib.w8a8_fp8_gemm
+    ok = (A, B, C, D, None, A, 8, 16, 64, None)
+    args = list(ok); args[8] = 40
+    assert f(*args) == capi.I8QL_ERR_UNSUPPORTED          # K % 16
+    args = list(ok); args[7] = 0
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG          # N = 0
+    args = list(ok); args[2] = None
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG          # qw
+    args = list(ok); args[4] = A + 1
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG          # bias misaligned
+    args = list(ok); args[6] = 0
+    assert f(*args) == capi.I8QL_OK
+    g = lib.w8a8_fp8_linear
+    ok = (A, B, C, None, D, None, None, 8, 16, 64, None)
+    args = list(ok); args[9] = 40
+    assert g(*args) == capi.I8QL_ERR_UNSUPPORTED
+    args = list(ok); args[5] = A + 8
+    assert g(*args) == capi.I8QL_ERR_INVALID_ARG          # qx misaligned
+    args = list(ok); args[7] = 0
+    assert g(*args) == capi.I8QL_OK
+    if not torch.cuda.is_available():
+        assert f(*(A, B, C, D, None, A, 8, 16, 64, None)) == capi.I8QL_ERR_NO_DEVICE
