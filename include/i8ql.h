@@ -239,6 +239,44 @@ i8ql_status w8a8_fp8_linear(const i8ql_bf16* x, const uint8_t* qw, const float* 
                             void* stream);
 
 /*
+ * Group-128 int4 weight quantization (W4A16-g128).
+ *
+ * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 1 (a
+ * W4A16-g128 tensor is int4 codes plus one bf16 scale per 128 weights along
+ * the input dimension; q = clamp(round(w / s)), s = absmax(group) / largest
+ * code).
+ *
+ * For every row n of w (bf16 [N, K]) and group g (k = 128g .. 128g+127):
+ *   a = max |w[n,k]|;  scale[n,g] = bf16_rne(a / 7) (fp32 IEEE division),
+ *                      or 1 if a == 0;
+ *   q[n,k] = clamp(rint(w[n,k] / scale[n,g]), -7, 7) with one IEEE fp32
+ *            division by the stored (bf16) scale, ties to even.
+ * Outputs: q uint8 [N, K/2], two codes per byte (even k in the low nibble,
+ * 4-bit two's complement); scale bf16 [N, K/128].  K must be a multiple of
+ * 128 (else I8QL_ERR_UNSUPPORTED).  q 16-byte and scale 2-byte aligned.  A
+ * nonzero group whose absmax is below about 2^-131 (its scale rounds to zero
+ * in bf16) is outside the contract.
+ */
+i8ql_status quantize_weight_w4_g128(const i8ql_bf16* w, int64_t N, int64_t K, uint8_t* q, i8ql_bf16* scale,
+                                    void* stream);
+
+/*
+ * Weight-only W4A16 GEMM / GEMV with group-128 scales (decode).
+ *
+ * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 5 (W4A16:
+ * int4 weights dequantized inside the kernel, the product on bf16 math; a
+ * pure memory-bandwidth win) and block 1 (group-128 scales).
+ *
+ *   y[m,n] = bf16_rne(sum_g scale[n,g] * sum_{k in g} q[n,k] * x[m,k])
+ * with bf16 x [M, K], q and scale as quantize_weight_w4_g128 writes them,
+ * y bf16 [M, N].  The codes enter the bf16 product exactly; each group's
+ * sum is accumulated in fp32 and scaled in fp32, so s * q is never rounded.
+ * K % 128 == 0.  Any M is accepted; the kernels are built for M <= 64.
+ */
+i8ql_status w4a16_gemm(const i8ql_bf16* x, const uint8_t* q, const i8ql_bf16* scale, i8ql_bf16* y,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
  * W8A8 GEMM that allocates nothing.
  *
  * No counterpart on the pages: this entry point exists for callers that

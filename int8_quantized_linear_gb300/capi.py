@@ -49,6 +49,8 @@ SIGNATURES = {
     "quantize_act_per_token_fp8": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "w8a8_fp8_gemm": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w8a8_fp8_linear": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "quantize_weight_w4_g128": (_S, [_P, _I64, _I64, _P, _P, _P]),
+    "w4a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
 }
 
 _LIB = None
@@ -341,4 +343,35 @@ def w8a8_fp8_linear(x, qw, sw, bias=None, y=None, qx=None, sx=None, stream=None)
         _need(sx, torch.float32, (m,), "sx")
     _check(lib().w8a8_fp8_linear(_ptr(x), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y), _ptr(qx), _ptr(sx), m, n, k,
                                  _stream(stream)), "w8a8_fp8_linear")
+    return y
+
+
+# ---------------------------------------------------------------- W4A16, group 128
+
+def quantize_weight_w4_g128(w: torch.Tensor, q=None, scale=None, stream=None):
+    """Packed int4 codes [N, K/2] (uint8) and bf16 group scales [N, K/128]."""
+    n, k = w.shape
+    _need(w, torch.bfloat16, (n, k), "w")
+    if q is None:
+        q = torch.empty((n, k // 2), dtype=torch.uint8, device=w.device)
+    if scale is None:
+        scale = torch.empty((n, k // 128), dtype=torch.bfloat16, device=w.device)
+    _need(q, torch.uint8, (n, k // 2), "q")
+    _need(scale, torch.bfloat16, (n, k // 128), "scale")
+    _check(lib().quantize_weight_w4_g128(_ptr(w), n, k, _ptr(q), _ptr(scale), _stream(stream)),
+           "quantize_weight_w4_g128")
+    return q, scale
+
+
+def w4a16_gemm(x, q, scale, y=None, stream=None):
+    """bf16 y [M, N] = bf16(sum_g scale[n, g] * sum_k q[n, k] * x[m, k])."""
+    m, k = x.shape
+    n = q.shape[0]
+    _need(x, torch.bfloat16, (m, k), "x")
+    _need(q, torch.uint8, (n, k // 2), "q")
+    _need(scale, torch.bfloat16, (n, k // 128), "scale")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=q.device)
+    _need(y, torch.bfloat16, (m, n), "y")
+    _check(lib().w4a16_gemm(_ptr(x), _ptr(q), _ptr(scale), _ptr(y), m, n, k, _stream(stream)), "w4a16_gemm")
     return y

@@ -281,6 +281,39 @@ i8ql_status w8a8_fp8_linear(const i8ql_bf16* x, const uint8_t* qw, const float* 
     return from_cuda(launch_fp8_linear(x, qw, sw, bias, y, qx, sx, M, N, K, env));
 }
 
+i8ql_status quantize_weight_w4_g128(const i8ql_bf16* w, int64_t N, int64_t K, uint8_t* q, i8ql_bf16* scale,
+                                    void* stream) {
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_k(K));
+    if (K % 128 != 0) return I8QL_ERR_UNSUPPORTED;
+    I8QL_TRY(check_matrix(w, N));
+    I8QL_TRY(check_matrix(q, N));
+    I8QL_TRY(check_vec(scale, N, 2));
+    if (N == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_quant_w4(w, N, K, q, scale, env));
+}
+
+i8ql_status w4a16_gemm(const i8ql_bf16* x, const uint8_t* q, const i8ql_bf16* scale, i8ql_bf16* y, int64_t M,
+                       int64_t N, int64_t K, void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (K % 128 != 0) return I8QL_ERR_UNSUPPORTED;
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_matrix(x, M));
+    I8QL_TRY(check_matrix(q, N));
+    I8QL_TRY(check_vec(scale, N, 2));
+    I8QL_TRY(check_matrix(y, M));
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_w4a16(x, q, scale, y, M, N, K, env));
+}
+
 i8ql_status i8ql_get_device_error(void* stream) {
     LaunchEnv env;
     i8ql_status s;

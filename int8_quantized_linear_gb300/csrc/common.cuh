@@ -148,6 +148,12 @@ cudaError_t launch_quant_rows_fp8(const uint16_t* src, int64_t rows, int64_t K, 
                                   const LaunchEnv& env);
 cudaError_t launch_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
                             const uint16_t* bias, uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env);
+// W4A16 with bf16 group-128 scales: the quantization of bf16 weights to
+// packed int4 codes and the decode GEMM.
+cudaError_t launch_quant_w4(const uint16_t* w, int64_t N, int64_t K, uint8_t* packed, uint16_t* scale,
+                            const LaunchEnv& env);
+cudaError_t launch_w4a16(const uint16_t* x, const uint8_t* q, const uint16_t* s, uint16_t* y, int64_t M, int64_t N,
+                         int64_t K, const LaunchEnv& env);
 cudaError_t launch_fp8_linear(const uint16_t* x, const uint8_t* qw, const float* sw, const uint16_t* bias,
                               uint16_t* y, uint8_t* qx, float* sx, int64_t M, int64_t N, int64_t K,
                               const LaunchEnv& env);

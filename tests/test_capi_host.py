@@ -205,3 +205,17 @@ def test_fp8_gemm_and_linear_argument_errors(lib):
     assert g(*args) == capi.I8QL_OK
     if not torch.cuda.is_available():
         assert f(*(A, B, C, D, None, A, 8, 16, 64, None)) == capi.I8QL_ERR_NO_DEVICE
+
+
+def test_w4_argument_errors(lib):
+    f = lib.quantize_weight_w4_g128
+    assert f(A, 4, 64, B, C, None) == capi.I8QL_ERR_UNSUPPORTED        # K % 128
+    assert f(A, 4, 128, B, C + 1, None) == capi.I8QL_ERR_INVALID_ARG   # scale misaligned
+    assert f(None, 0, 128, None, None, None) == capi.I8QL_OK
+    g = lib.w4a16_gemm
+    assert g(A, B, C, D, 4, 16, 192, None) == capi.I8QL_ERR_UNSUPPORTED
+    assert g(A, None, C, D, 4, 16, 256, None) == capi.I8QL_ERR_INVALID_ARG
+    assert g(A, B, C, D, 4, 0, 256, None) == capi.I8QL_ERR_INVALID_ARG
+    assert g(None, B, C, None, 0, 16, 256, None) == capi.I8QL_OK
+    if not torch.cuda.is_available():
+        assert g(A, B, C, D, 4, 16, 256, None) == capi.I8QL_ERR_NO_DEVICE

@@ -1,0 +1,145 @@
+"""GPU parity of the W4A16 group-128 path (int4 quantization with bf16 group
+scales, and the decode GEMM) against the CPU oracle, through the C ABI.
+
+Bars:
+ * packed codes and bf16 group scales: bit-exact;
+ * GEMM outputs (weight-only, as W8A16): relative Frobenius error of the
+   whole output <= 2e-3 against the fp64 dequantize-then-matmul oracle (for
+   outputs of at least 1024 elements), and every element within
+   K * 2^-23 * sum_k |s q x| (fp32 accumulation of the group sums and their
+   scaling, any order) + 2^-8 |y| (one bf16 rounding).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_quantized_linear_gb300 import capi, synthetic
+from tests import util
+from tests.golden import load as golden
+
+pytestmark = pytest.mark.gpu
+
+FROB = 2e-3
+# The Frobenius bar is a statistic of the output's bf16 rounding errors; on
+# a handful of elements the rounding alone can exceed it (16 outputs: 2.007e-3
+# for outputs equal to the exact values rounded once), so it applies from
+# this size on, and the per-element bound applies everywhere.
+FROB_MIN_ELEMENTS = 1024
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library(cuda_device):
+    from int8_quantized_linear_gb300 import build
+    build.build()
+    capi.lib()
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    yield
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+
+
+def gpu_quant(w_bf16: torch.Tensor):
+    n, k = w_bf16.shape
+    qbuf, q = util.guarded((n, k // 2), torch.uint8, "cuda", 0xA5)
+    sbuf, s = util.guarded((n, k // 128), torch.int16, "cuda", 0x7F7F)
+    capi.quantize_weight_w4_g128(w_bf16.cuda(), q=q, scale=s.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert util.guard_intact(qbuf, n * k // 2, 0xA5) and util.guard_intact(sbuf, n * (k // 128), 0x7F7F)
+    return q.cpu().numpy(), s.cpu().numpy().view(np.uint16)
+
+
+def check_quant(w_bf16: torch.Tensor):
+    q, s = gpu_quant(w_bf16)
+    q_ref, s_ref = oracle.quant_w4_g128(util.bits(w_bf16))
+    assert np.array_equal(s, s_ref), f"scales differ at {np.argwhere(s != s_ref)[:3].tolist()}"
+    bad = np.argwhere(q != q_ref)
+    assert bad.size == 0, f"{len(bad)} code bytes differ, first at {bad[:3].tolist()}"
+    return q, s
+
+
+@pytest.mark.parametrize("case", golden.w4_groups(), ids=lambda c: c[0])
+def test_w4_quant_golden_groups_on_gpu(case):
+    name, row, scales, groups, nbytes = case
+    src = torch.tensor(np.asarray([row], np.float64)).to(torch.bfloat16)
+    q, s = gpu_quant(src)
+    assert oracle.widen_bf16(s[0]).tolist() == scales, name
+    assert q[0, :len(nbytes)].tolist() == nbytes, name
+
+
+def _adversarial(rows, k, seed):
+    w = synthetic.weight(rows, k, seed).float()
+    g = torch.Generator().manual_seed(seed)
+    if rows > 1:
+        w[1, :128] = 0.0  # an all-zero group beside nonzero ones
+    if rows > 2:
+        w[2] *= 1e-30  # tiny magnitudes keep the full int4 range
+    if rows > 3:
+        w[3] = torch.randint(-14, 15, (k,), generator=g).float() * 0.5  # many exact ties
+    return w.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,k", [(1, 128), (5, 256), (33, 1152), (130, 2560), (7, 12288), (300, 4096)])
+def test_w4_quant_shapes(rows, k):
+    check_quant(_adversarial(rows, k, rows + k))
+
+
+@pytest.mark.parametrize("shape", list(synthetic.QWEN3_8B_SHAPES))
+def test_w4_quant_qwen3_8b_full_size(shape):
+    n, k = synthetic.QWEN3_8B_SHAPES[shape]
+    check_quant(synthetic.weight(n, k, 4))
+
+
+# ------------------------------------------------------------------ GEMM
+
+def gpu_gemm(x_bf16, q, s):
+    m, k = x_bf16.shape
+    n = q.shape[0]
+    ybuf, y = util.guarded((m, n), torch.int16, "cuda", 0x7F7F)
+    capi.w4a16_gemm(x_bf16.cuda(), torch.from_numpy(q).cuda(), util.from_bits(s, "cuda"), y=y.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert util.guard_intact(ybuf, m * n, 0x7F7F)
+    return util.from_bits(y.cpu().numpy().view(np.uint16)).double().numpy()
+
+
+def check_gemm(x_bf16, q, s):
+    y = gpu_gemm(x_bf16, q, s)
+    xb = util.bits(x_bf16)
+    ref = oracle.w4a16(xb, q, s)
+    if ref.size >= FROB_MIN_ELEMENTS:
+        assert util.rel_frobenius(y, ref) <= FROB
+    # magnitudes: the oracle on |x| and |codes| (packed again as nibbles)
+    k = x_bf16.shape[1]
+    codes = np.abs(oracle.w4_unpack(q, k).astype(np.int16))
+    packed_abs = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    mag = oracle.w4a16(xb & np.uint16(0x7FFF), packed_abs, s)
+    bound = mag * (k * 2.0 ** -23) + np.abs(ref) * 2.0 ** -8 + 1e-30
+    assert np.all(np.abs(y - ref) <= bound)
+    return y
+
+
+@pytest.mark.parametrize("m", [1, 3, 8, 9, 16, 17, 32, 33, 64])
+@pytest.mark.parametrize("n,k", [(1, 128), (31, 256), (100, 1152), (2560, 2560)])
+def test_w4a16_shapes(m, n, k):
+    q, s = oracle.quant_w4_g128(util.bits(synthetic.weight(n, k, n + k)))
+    check_gemm(synthetic.activations(m, k, m + n), q, s)
+
+
+@pytest.mark.parametrize("m", [1, 8, 64])
+@pytest.mark.parametrize("shape", list(synthetic.QWEN3_8B_SHAPES))
+def test_w4a16_qwen3_8b_full(shape, m):
+    """The Qwen3-8B projections (the checkpoint the pages quantize to
+    W4A16-g128), whole outputs, with the GPU's own quantization."""
+    n, k = synthetic.QWEN3_8B_SHAPES[shape]
+    w = synthetic.weight(n, k, 4)
+    q, s = check_quant(w)
+    check_gemm(synthetic.activations(m, k, 40 + m), q, s)
+
+
+def test_w4a16_empty_tokens():
+    q = torch.zeros((16, 64), dtype=torch.uint8, device="cuda")
+    s = torch.ones((16, 1), dtype=torch.bfloat16, device="cuda")
+    capi.w4a16_gemm(torch.empty((0, 128), dtype=torch.bfloat16, device="cuda"), q, s,
+                    y=torch.empty((0, 16), dtype=torch.bfloat16, device="cuda"))
