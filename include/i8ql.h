@@ -277,6 +277,89 @@ i8ql_status w4a16_gemm(const i8ql_bf16* x, const uint8_t* q, const i8ql_bf16* sc
                        int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * MoE routing of T tokens on the device (the layer around the grouped GEMM).
+ *
+ * Source: "Phase 5a: int8 weight-only quantization", Summary (the grouped
+ * int8 GEMM serves the MoE layer of deepseek-moe-16b), with that layer's
+ * routing as its benchmark configuration states it: softmax over the gate
+ * logits, top-k routed experts per token, plus shared experts that see every
+ * token.
+ *
+ * Inputs: logits fp32 [T, E] (finite).  For every token t the top_k experts
+ * of largest logit are chosen (equal logits: the lower expert index first;
+ * the softmax is increasing in the logit), in decreasing order.  Outputs
+ * (S = top_k + n_shared slots per token, T * S grouped rows):
+ *   offsets int32 [E + n_shared + 1]: rows of expert e are offsets[e] ..
+ *     offsets[e+1]-1 (routed experts 0 .. E-1, then the shared experts),
+ *     tokens in increasing order within an expert;
+ *   row_token int32 [T * S]: the token of each grouped row;
+ *   token_row int32 [T, S]: the grouped row of each (token, slot), routed
+ *     slots first in decreasing logit order, then the shared experts;
+ *   slot_weight fp32 [T, S]: softmax probability (over all E experts, not
+ *     renormalised over the chosen ones) of each routed slot, 1 for shared.
+ * Limits: E <= 256, n_shared <= 64, T <= 65535 and 8 * E * ceil(T / 32) <=
+ * 200 KiB (one CTA), else I8QL_ERR_UNSUPPORTED.  T = 0 writes zero offsets.
+ */
+i8ql_status moe_route_topk(const float* logits, int64_t T, int64_t E, int64_t top_k, int64_t n_shared,
+                           int32_t* offsets, int32_t* row_token, int32_t* token_row, float* slot_weight,
+                           void* stream);
+
+/*
+ * Grouped W8A16 of a fused gate/up projection with the SiLU-gated product in
+ * its epilogue: the expert MLP's first half.
+ *
+ * Source: "Phase 5a: int8 weight-only quantization", Summary (grouped GEMM
+ * over stacked [E, N, K] expert weights with per-output-channel scales) and
+ * "feat(quantization): support compressed-tensors W8A8 and mixed modules",
+ * Summary (fused gate/up projections).
+ *
+ * Expert e's weights qw[e] (int8 [2I, K], gate rows 0 .. I-1, up rows
+ * I .. 2I-1) and scales sw[e] (fp32 [2I]) act on grouped rows offsets[e] ..
+ * offsets[e+1]-1, row r reading token row_token[r] of x (bf16 [*, K]; or row
+ * r itself when row_token is NULL):
+ *   g = sw[e,j] * sum_k qw[e,j,k] x[k],  u = sw[e,I+j] * sum_k qw[e,I+j,k] x[k]
+ *   h[r,j] = bf16_rne(g / (1 + exp(-g)) * u)                     (fp32)
+ * Output h bf16 [T_total, I].  Offsets rules and errors as
+ * grouped_w8a16_gemm.
+ */
+i8ql_status grouped_w8a16_silu_mul(const i8ql_bf16* x, const int32_t* row_token, const int32_t* offsets, int64_t E,
+                                   const int8_t* qw, const float* sw, i8ql_bf16* h, int64_t T_total, int64_t I,
+                                   int64_t K, void* stream);
+
+/*
+ * Weighted combine of the experts' output rows into each token's output.
+ *
+ * Source: as moe_route_topk.
+ *
+ *   out[t,:] = bf16_rne(sum_s slot_weight[t,s] * yd[token_row[t,s], :])
+ * slots in order, fp32 accumulation.  yd bf16 [rows, H], token_row int32 and
+ * slot_weight fp32 [T, S], out bf16 [T, H].  H % 8 == 0, T <= 65535.
+ */
+i8ql_status moe_combine(const i8ql_bf16* yd, const int32_t* token_row, const float* slot_weight, i8ql_bf16* out,
+                        int64_t T, int64_t S, int64_t H, void* stream);
+
+/*
+ * The MoE expert MLP with int8 weight-only experts, end to end: routing,
+ * grouped gate/up with the SiLU-gated product (token rows gathered),
+ * grouped down, combine.
+ *
+ * Source: "Phase 5a: int8 weight-only quantization", Summary (the grouped
+ * int8 kernel inside MoE decode of deepseek-moe-16b).
+ *
+ * Inputs: x bf16 [T, H], logits fp32 [T, E_routed]; experts E = E_routed +
+ * n_shared (routed first): qw_gate_up int8 [E, 2I, H] with sw_gate_up fp32
+ * [E, 2I], qw_down int8 [E, H, I] with sw_down fp32 [E, H].  Output out bf16
+ * [T, H].  Four kernels; the intermediates (routing arrays, h [T*S, I] and
+ * the down outputs [T*S, H], bf16) live in a temporary stream-ordered
+ * workspace (cudaMallocAsync / cudaFreeAsync on `stream`).  Limits as
+ * moe_route_topk; H and I multiples of 16.
+ */
+i8ql_status moe_expert_mlp_w8a16(const i8ql_bf16* x, const float* logits, int64_t E_routed, int64_t top_k,
+                                 int64_t n_shared, const int8_t* qw_gate_up, const float* sw_gate_up,
+                                 const int8_t* qw_down, const float* sw_down, i8ql_bf16* out, int64_t T, int64_t H,
+                                 int64_t I, void* stream);
+
+/*
  * W8A8 GEMM that allocates nothing.
  *
  * No counterpart on the pages: this entry point exists for callers that

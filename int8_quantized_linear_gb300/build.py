@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libi8ql.so")
-SOURCES = ["capi.cu", "quant.cu", "decode_gemm.cu", "w8a8.cu", "w8a8_fused.cu", "noalloc.cu", "fp8_gemm.cu", "w4a16.cu"]
+SOURCES = ["capi.cu", "quant.cu", "decode_gemm.cu", "w8a8.cu", "w8a8_fused.cu", "noalloc.cu", "fp8_gemm.cu", "w4a16.cu", "moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

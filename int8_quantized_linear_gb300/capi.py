@@ -51,6 +51,10 @@ SIGNATURES = {
     "w8a8_fp8_linear": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "quantize_weight_w4_g128": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "w4a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "moe_route_topk": (_S, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "grouped_w8a16_silu_mul": (_S, [_P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "moe_combine": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "moe_expert_mlp_w8a16": (_S, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
 }
 
 _LIB = None
@@ -375,3 +379,81 @@ def w4a16_gemm(x, q, scale, y=None, stream=None):
     _need(y, torch.bfloat16, (m, n), "y")
     _check(lib().w4a16_gemm(_ptr(x), _ptr(q), _ptr(scale), _ptr(y), m, n, k, _stream(stream)), "w4a16_gemm")
     return y
+
+
+# ---------------------------------------------------------------- MoE expert MLP
+
+def moe_route_topk(logits, top_k, n_shared, stream=None):
+    """Device routing: (offsets [E+n_shared+1], row_token [T*S], token_row
+    [T, S], slot_weight [T, S]) for fp32 logits [T, E]."""
+    t, e = logits.shape
+    _need(logits, torch.float32, (t, e), "logits")
+    s = top_k + n_shared
+    dev = logits.device
+    offsets = torch.empty((e + n_shared + 1,), dtype=torch.int32, device=dev)
+    row_token = torch.empty((t * s,), dtype=torch.int32, device=dev)
+    token_row = torch.empty((t, s), dtype=torch.int32, device=dev)
+    slot_weight = torch.empty((t, s), dtype=torch.float32, device=dev)
+    _check(lib().moe_route_topk(_ptr(logits), t, e, top_k, n_shared, _ptr(offsets), _ptr(row_token),
+                                _ptr(token_row), _ptr(slot_weight), _stream(stream)), "moe_route_topk")
+    return offsets, row_token, token_row, slot_weight
+
+
+def grouped_w8a16_silu_mul(x, row_token, offsets, qw, sw, h=None, rows=None, stream=None):
+    """h [rows, I] = bf16(silu(gate) * up) of the grouped fused gate/up
+    projection qw [E, 2I, K], gathering token rows through row_token."""
+    e, two_i, k = qw.shape
+    inter = two_i // 2
+    if rows is None:
+        rows = row_token.shape[0] if row_token is not None else x.shape[0]
+    _need(x, torch.bfloat16, (x.shape[0], k), "x")
+    _need(offsets, torch.int32, (e + 1,), "offsets")
+    if row_token is not None:
+        _need(row_token, torch.int32, (rows,), "row_token")
+    _need(sw, torch.float32, (e, two_i), "sw")
+    if h is None:
+        h = torch.empty((rows, inter), dtype=torch.bfloat16, device=qw.device)
+    _need(h, torch.bfloat16, (rows, inter), "h")
+    _check(lib().grouped_w8a16_silu_mul(_ptr(x), _ptr(row_token), _ptr(offsets), e, _ptr(qw), _ptr(sw), _ptr(h),
+                                        rows, inter, k, _stream(stream)), "grouped_w8a16_silu_mul")
+    return h
+
+
+def moe_combine(yd, token_row, slot_weight, out=None, stream=None):
+    """out [T, H] = bf16(sum_s slot_weight[t, s] * yd[token_row[t, s]])."""
+    t, s = token_row.shape
+    h = yd.shape[1]
+    _need(token_row, torch.int32, (t, s), "token_row")
+    _need(slot_weight, torch.float32, (t, s), "slot_weight")
+    _need(yd, torch.bfloat16, (yd.shape[0], h), "yd")
+    if out is None:
+        out = torch.empty((t, h), dtype=torch.bfloat16, device=yd.device)
+    _need(out, torch.bfloat16, (t, h), "out")
+    _check(lib().moe_combine(_ptr(yd), _ptr(token_row), _ptr(slot_weight), _ptr(out), t, s, h, _stream(stream)),
+           "moe_combine")
+    return out
+
+
+def moe_expert_mlp_w8a16(x, logits, top_k, n_shared, qw_gate_up, sw_gate_up, qw_down, sw_down, out=None,
+                         stream=None):
+    """The MoE expert MLP end to end (routing, gate/up + SiLU gate, down,
+    combine) for tokens x [T, H] with gate logits [T, E_routed]."""
+    t, hid = x.shape
+    e_r = logits.shape[1]
+    e, two_i, k = qw_gate_up.shape
+    inter = two_i // 2
+    _need(x, torch.bfloat16, (t, hid), "x")
+    _need(logits, torch.float32, (t, e_r), "logits")
+    if e != e_r + n_shared or k != hid:
+        raise ValueError("expert weights do not match the routing or the hidden size")
+    _need(qw_gate_up, torch.int8, (e, two_i, hid), "qw_gate_up")
+    _need(sw_gate_up, torch.float32, (e, two_i), "sw_gate_up")
+    _need(qw_down, torch.int8, (e, hid, inter), "qw_down")
+    _need(sw_down, torch.float32, (e, hid), "sw_down")
+    if out is None:
+        out = torch.empty((t, hid), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (t, hid), "out")
+    _check(lib().moe_expert_mlp_w8a16(_ptr(x), _ptr(logits), e_r, top_k, n_shared, _ptr(qw_gate_up),
+                                      _ptr(sw_gate_up), _ptr(qw_down), _ptr(sw_down), _ptr(out), t, hid, inter,
+                                      _stream(stream)), "moe_expert_mlp_w8a16")
+    return out

@@ -314,6 +314,86 @@ i8ql_status w4a16_gemm(const i8ql_bf16* x, const uint8_t* q, const i8ql_bf16* sc
     return from_cuda(launch_w4a16(x, q, scale, y, M, N, K, env));
 }
 
+i8ql_status moe_route_topk(const float* logits, int64_t T, int64_t E, int64_t top_k, int64_t n_shared,
+                           int32_t* offsets, int32_t* row_token, int32_t* token_row, float* slot_weight,
+                           void* stream) {
+    if (T < 0 || E <= 0 || top_k <= 0 || top_k > E || n_shared < 0) return I8QL_ERR_INVALID_ARG;
+    if (E > 256 || n_shared > 64 || T > 65535 || moe_route_smem(T, E) == kRouteTooLarge)
+        return I8QL_ERR_UNSUPPORTED;
+    if (offsets == nullptr || !aligned(offsets, 4)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_vec(logits, T, 4));
+    I8QL_TRY(check_vec(row_token, T, 4));
+    I8QL_TRY(check_vec(token_row, T, 4));
+    I8QL_TRY(check_vec(slot_weight, T, 4));
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_moe_route(logits, T, E, top_k, n_shared, offsets, row_token, token_row, slot_weight, env));
+}
+
+i8ql_status grouped_w8a16_silu_mul(const i8ql_bf16* x, const int32_t* row_token, const int32_t* offsets, int64_t E,
+                                   const int8_t* qw, const float* sw, i8ql_bf16* h, int64_t T_total, int64_t I,
+                                   int64_t K, void* stream) {
+    I8QL_TRY(check_rows(T_total));
+    I8QL_TRY(check_k(K));
+    if (I <= 0 || E <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(2 * I));
+    if (E > 65535) return I8QL_ERR_UNSUPPORTED;
+    if ((double)E * (double)(2 * I) * (double)K > 9.0e18) return I8QL_ERR_UNSUPPORTED;
+    if (offsets == nullptr || !aligned(offsets, 4)) return I8QL_ERR_INVALID_ARG;
+    if (row_token != nullptr && !aligned(row_token, 4)) return I8QL_ERR_INVALID_ARG;
+    if (x == nullptr && T_total > 0) return I8QL_ERR_INVALID_ARG;
+    if (x != nullptr && !aligned(x, 16)) return I8QL_ERR_INVALID_ARG;
+    if (qw == nullptr || !aligned(qw, 16)) return I8QL_ERR_INVALID_ARG;
+    if (sw == nullptr || !aligned(sw, 4)) return I8QL_ERR_INVALID_ARG;
+    if (T_total > 0 && (h == nullptr || !aligned(h, 2))) return I8QL_ERR_INVALID_ARG;
+    if (T_total == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_w8a16(x, offsets, E, qw, sw, h, T_total, 2 * I, K, env, row_token, I));
+}
+
+i8ql_status moe_combine(const i8ql_bf16* yd, const int32_t* token_row, const float* slot_weight, i8ql_bf16* out,
+                        int64_t T, int64_t S, int64_t H, void* stream) {
+    if (T < 0 || S <= 0 || H <= 0) return I8QL_ERR_INVALID_ARG;
+    if (H % 8 != 0 || T > 65535) return I8QL_ERR_UNSUPPORTED;
+    I8QL_TRY(check_vec(token_row, T, 4));
+    I8QL_TRY(check_vec(slot_weight, T, 4));
+    I8QL_TRY(check_matrix(yd, T));
+    I8QL_TRY(check_matrix(out, T));
+    if (T == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_moe_combine(yd, token_row, slot_weight, out, T, S, H, env));
+}
+
+i8ql_status moe_expert_mlp_w8a16(const i8ql_bf16* x, const float* logits, int64_t E_routed, int64_t top_k,
+                                 int64_t n_shared, const int8_t* qw_gate_up, const float* sw_gate_up,
+                                 const int8_t* qw_down, const float* sw_down, i8ql_bf16* out, int64_t T, int64_t H,
+                                 int64_t I, void* stream) {
+    if (T < 0 || E_routed <= 0 || top_k <= 0 || top_k > E_routed || n_shared < 0 || H <= 0 || I <= 0)
+        return I8QL_ERR_INVALID_ARG;
+    if (E_routed > 256 || n_shared > 64 || T > 65535 || moe_route_smem(T, E_routed) == kRouteTooLarge)
+        return I8QL_ERR_UNSUPPORTED;
+    I8QL_TRY(check_k(H));
+    I8QL_TRY(check_k(I));
+    I8QL_TRY(check_matrix(x, T));
+    I8QL_TRY(check_vec(logits, T, 4));
+    I8QL_TRY(check_matrix(out, T));
+    if (qw_gate_up == nullptr || !aligned(qw_gate_up, 16) || qw_down == nullptr || !aligned(qw_down, 16))
+        return I8QL_ERR_INVALID_ARG;
+    if (sw_gate_up == nullptr || !aligned(sw_gate_up, 4) || sw_down == nullptr || !aligned(sw_down, 4))
+        return I8QL_ERR_INVALID_ARG;
+    if (T == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_moe_mlp(x, logits, E_routed, top_k, n_shared, qw_gate_up, sw_gate_up, qw_down, sw_down,
+                                    out, T, H, I, env));
+}
+
 i8ql_status i8ql_get_device_error(void* stream) {
     LaunchEnv env;
     i8ql_status s;

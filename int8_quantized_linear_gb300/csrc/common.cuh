@@ -106,9 +106,27 @@ constexpr int64_t kW8A8DecodeMaxM = 64;
 // stream-K flags of the GEMM launched after it; nullable).
 cudaError_t launch_quant_rows(const uint16_t* src, int64_t rows, int64_t K, int8_t* q, uint16_t* qh, float* s,
                               const LaunchEnv& env, unsigned* zero = nullptr, int nzero = 0);
+// W8A16 (offsets null) or grouped W8A16; grouped calls may gather their token
+// rows (gather[r] = row of x feeding grouped row r) and may fuse the
+// SiLU-gated product of a gate/up projection with N = 2 * glu rows.
 cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw,
                          const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
-                         const LaunchEnv& env);
+                         const LaunchEnv& env, const int32_t* gather = nullptr, int64_t glu = 0);
+// MoE routing over device logits, and the weighted combine of expert rows.
+cudaError_t launch_moe_route(const float* logits, int64_t T, int64_t E, int64_t topk, int64_t shared,
+                             int32_t* offsets, int32_t* row_token, int32_t* token_row, float* slot_weight,
+                             const LaunchEnv& env);
+cudaError_t launch_moe_combine(const uint16_t* yd, const int32_t* token_row, const float* slot_weight, uint16_t* out,
+                               int64_t T, int64_t S, int64_t H, const LaunchEnv& env);
+// Shared memory of the routing kernel for T tokens over E routed experts
+// (kRouteTooLarge when one CTA cannot hold it).
+constexpr size_t kRouteTooLarge = ~(size_t)0;
+size_t moe_route_smem(int64_t T, int64_t E);
+// The MoE expert MLP: routing, grouped gate/up with the SiLU-gated product,
+// grouped down, combine; intermediates in a stream-ordered workspace.
+cudaError_t launch_moe_mlp(const uint16_t* x, const float* logits, int64_t E_routed, int64_t topk, int64_t shared,
+                           const int8_t* qw_gu, const float* sw_gu, const int8_t* qw_d, const float* sw_d,
+                           uint16_t* out, int64_t T, int64_t H, int64_t I, const LaunchEnv& env);
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                                int64_t K, const LaunchEnv& env);

@@ -74,6 +74,10 @@ struct DecodeParams {
     int64_t E;
     unsigned* err;
     int one_wave;            // every CTA of the grid is resident at once
+    const int32_t* gather;   // grouped: token row of x for each grouped row (null: row r is x's row r)
+    int64_t glu;             // grouped W8A16: intermediate size I of a fused gate/up
+                             // projection (N = 2I) whose SiLU-gated product is the
+                             // output [rows, I]; 0: plain outputs
 };
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
@@ -232,12 +236,23 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
     // Lane base pointers.  Rows past N read row N-1 and tokens past the
     // chunk read its last token: their products land only in outputs that
     // are never stored, so the main loop needs no predicates.
+    // With a fused gate/up projection (p.glu = I) a CTA owns 16 output
+    // columns j0 .. j0+15: m-tile 0 holds their gate rows, m-tile 1 the up
+    // rows I + j0 .. (MT == 2 there).
     const int8_t* wbase[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-            wbase[mt][h] = qw + min(n0 + mt * 16 + g + 8 * h, N - 1) * K + 16 * t + ks_begin * 64;
+        for (int h = 0; h < 2; ++h) {
+            int64_t n;
+            if (p.glu) {
+                const int64_t j = min((int64_t)blockIdx.x * 16 + g + 8 * h, p.glu - 1);
+                n = mt == 0 ? j : p.glu + j;
+            } else {
+                n = min(n0 + mt * 16 + g + 8 * h, N - 1);
+            }
+            wbase[mt][h] = qw + n * K + 16 * t + ks_begin * 64;
+        }
 
     using XT = std::conditional_t<OP == Op::kW8A16, uint16_t, int8_t>;
     constexpr int kXW = OP == Op::kW8A16 ? 8 : 4;  // 32-bit words of x per lane per k-step
@@ -247,8 +262,11 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
         const int nt_active = (int)((chunk_hi - c0 + 7) / 8);
         const XT* xbase[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            xbase[nt] = static_cast<const XT*>(p.x) + min(c0 + nt * 8 + g, chunk_hi - 1) * K + 16 * t + ks_begin * 64;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int64_t r = min(c0 + nt * 8 + g, chunk_hi - 1);
+            const int64_t src = p.gather ? (int64_t)p.gather[r] : r;  // the token feeding grouped row r
+            xbase[nt] = static_cast<const XT*>(p.x) + src * K + 16 * t + ks_begin * 64;
+        }
 
         Acc acc[MT][NT][4];
 #pragma unroll
@@ -385,25 +403,46 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
             __syncthreads();
         else
             cluster.sync();
-        const int total = nt_active * 8 * kRows;
+        // the sum over the cluster of tile entry i, in rank order
+        auto reduced = [&](int i) -> Acc {
+            if (S == 1) return part[0][i];
+            Acc v[kMaxClusterSplit];
+#pragma unroll
+            for (int r = 0; r < kMaxClusterSplit; ++r)
+                v[r] = r < S ? cluster.map_shared_rank(&part[0][0], r)[i] : Acc(0);
+            Acc s = v[0];
+#pragma unroll
+            for (int r = 1; r < kMaxClusterSplit; ++r)
+                if (r < S) s += v[r];
+            return s;
+        };
+        if (OP == Op::kW8A16 && p.glu) {
+            // SiLU-gated product of the fused gate/up rows: tile rows r and
+            // 16 + r hold gate and up of output column j0 + r
+            const int64_t j0 = (int64_t)blockIdx.x * 16;
+            const int total = nt_active * 8 * 16;
+            const int per = (total + S - 1) / S;
+            const int i_begin = rank * per;
+            const int i_end = min(total, i_begin + per);
+            for (int i = i_begin + (int)threadIdx.x; i < i_end; i += kThreads) {
+                const int r = i % 16;
+                const int tok = i / 16;
+                const Acc gs = reduced(tok * kRows + r), us = reduced(tok * kRows + 16 + r);
+                const int64_t j = j0 + r;
+                const int64_t m = c0 + tok;
+                if (j < p.glu && m < hi) {
+                    const float gv = (float)gs * sw[j];
+                    const float uv = (float)us * sw[p.glu + j];
+                    p.y[m * p.glu + j] = f32_to_bf16_rn(gv / (1.0f + expf(-gv)) * uv);
+                }
+            }
+        }
+        const int total = (OP == Op::kW8A16 && p.glu) ? 0 : nt_active * 8 * kRows;
         const int per = (total + S - 1) / S;
         const int i_begin = rank * per;
         const int i_end = min(total, i_begin + per);
         for (int i = i_begin + (int)threadIdx.x; i < i_end; i += kThreads) {
-            Acc s;
-            if (S == 1) {
-                s = part[0][i];
-            } else {
-                // all peers' loads in flight before the rank-ordered sum
-                Acc v[kMaxClusterSplit];
-#pragma unroll
-                for (int r = 0; r < kMaxClusterSplit; ++r)
-                    v[r] = r < S ? cluster.map_shared_rank(&part[0][0], r)[i] : Acc(0);
-                s = v[0];
-#pragma unroll
-                for (int r = 1; r < kMaxClusterSplit; ++r)
-                    if (r < S) s += v[r];
-            }
+            const Acc s = reduced(i);  // all peers' loads in flight before the rank-ordered sum
             const int row = i % kRows;
             const int tok = i / kRows;
             const int64_t n = n0 + row;
@@ -429,10 +468,16 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
     }
 }
 
+// Row blocks of the grid: 16 * MT weight rows each, or 16 gated output
+// columns each with a fused gate/up projection.
+template <int MT>
+int64_t row_blocks_of(const DecodeParams& p) {
+    return p.glu ? (p.glu + 15) / 16 : (p.N + 16 * MT - 1) / (16 * MT);
+}
+
 template <Op OP, int MT, int NT, bool GROUPED>
 cudaError_t launch_cfg(const DecodeParams& p, int split, cudaStream_t stream) {
-    constexpr int kRows = 16 * MT;
-    const int64_t row_blocks = (p.N + kRows - 1) / kRows;
+    const int64_t row_blocks = row_blocks_of<MT>(p);
     return launch_kernel(decode_gemm_kernel<OP, MT, NT, GROUPED>,
                          dim3((unsigned)row_blocks, (unsigned)split, (unsigned)(GROUPED ? p.E : 1)), dim3(kThreads),
                          0, stream, dim3(1, (unsigned)split, 1), p);
@@ -465,7 +510,7 @@ int choose_split(int64_t row_blocks, int64_t groups, int64_t K, int64_t capacity
 
 template <Op OP, int MT, int NT, bool GROUPED>
 cudaError_t launch_auto(DecodeParams p, int64_t groups_hint, int sms, cudaStream_t stream) {
-    const int64_t row_blocks = (p.N + 16 * MT - 1) / (16 * MT);
+    const int64_t row_blocks = row_blocks_of<MT>(p);
     const int64_t capacity = (int64_t)sms * resident_ctas<OP, MT, NT, GROUPED>();
     const int split = choose_split(row_blocks, groups_hint, p.K, capacity);
     p.one_wave = row_blocks * split * (GROUPED ? p.E : 1) <= capacity ? 1 : 0;
@@ -483,8 +528,9 @@ cudaError_t dispatch(const DecodeParams& p, int64_t tokens_hint, int64_t groups_
 }  // namespace
 
 cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw, const float* sw,
-                         uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env) {
-    DecodeParams p{x, nullptr, offsets, qw, sw, nullptr, y, nullptr, M, N, K, E, env.err, 0};
+                         uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env, const int32_t* gather,
+                         int64_t glu) {
+    DecodeParams p{x, nullptr, offsets, qw, sw, nullptr, y, nullptr, M, N, K, E, env.err, 0, gather, glu};
     if (offsets == nullptr) return dispatch<Op::kW8A16, false>(p, M, 1, env.sm_count, env.stream);
     // Grouped: at most min(E, T_total) experts have rows, on average
     // T_total / active rows each.
@@ -496,7 +542,7 @@ cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, c
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                const LaunchEnv& env) {
-    DecodeParams p{qx, sx, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err, 0};
+    DecodeParams p{qx, sx, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err, 0, nullptr, 0};
     return dispatch<Op::kW8A8, false>(p, M, 1, env.sm_count, env.stream);
 }
 

@@ -219,3 +219,30 @@ def test_w4_argument_errors(lib):
     assert g(None, B, C, None, 0, 16, 256, None) == capi.I8QL_OK
     if not torch.cuda.is_available():
         assert g(A, B, C, D, 4, 16, 256, None) == capi.I8QL_ERR_NO_DEVICE
+
+
+def test_moe_argument_errors(lib):
+    r = lib.moe_route_topk
+    assert r(A, 8, 64, 0, 2, B, C, D, A, None) == capi.I8QL_ERR_INVALID_ARG      # top_k = 0
+    assert r(A, 8, 64, 65, 2, B, C, D, A, None) == capi.I8QL_ERR_INVALID_ARG     # top_k > E
+    assert r(A, 8, 300, 6, 2, B, C, D, A, None) == capi.I8QL_ERR_UNSUPPORTED     # E > 256
+    assert r(A, 8, 64, 6, 2, None, C, D, A, None) == capi.I8QL_ERR_INVALID_ARG   # offsets
+    g = lib.grouped_w8a16_silu_mul
+    ok = [A, None, B, 66, C, D, A, 8, 16, 64, None]
+    a = list(ok); a[9] = 40
+    assert g(*a) == capi.I8QL_ERR_UNSUPPORTED                                    # K % 16
+    a = list(ok); a[2] = None
+    assert g(*a) == capi.I8QL_ERR_INVALID_ARG                                    # offsets
+    a = list(ok); a[7] = 0
+    assert g(*a) == capi.I8QL_OK                                                 # no rows
+    c = lib.moe_combine
+    assert c(A, B, C, D, 4, 8, 12, None) == capi.I8QL_ERR_UNSUPPORTED            # H % 8
+    assert c(A, B, C, D, 0, 8, 16, None) == capi.I8QL_OK
+    m = lib.moe_expert_mlp_w8a16
+    ok = [A, B, 64, 6, 2, C, D, A, B, C, 8, 2048, 1408, None]
+    a = list(ok); a[11] = 2050
+    assert m(*a) == capi.I8QL_ERR_UNSUPPORTED                                    # H % 16
+    a = list(ok); a[10] = 0
+    assert m(*a) == capi.I8QL_OK
+    if not torch.cuda.is_available():
+        assert m(*ok) == capi.I8QL_ERR_NO_DEVICE
