@@ -130,6 +130,13 @@ cudaError_t launch_moe_mlp(const uint16_t* x, const float* logits, int64_t E_rou
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N,
                                int64_t K, const LaunchEnv& env);
+// W8A8 from bf16 tokens in one launch (M <= kW8A8FusedMaxM): the decode
+// kernel quantizes its token rows itself; qx / sx receive the codes and
+// scales when not null.
+constexpr int64_t kW8A8FusedMaxM = 8;
+cudaError_t launch_w8a8_decode_fused(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
+                                     uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                                     const LaunchEnv& env);
 // Tile width (N side of the output tile), split-K factor and CTA-pair mode
 // (0 single CTAs, 1 pairs, 2 pairs with stream-K) the tcgen05 kernel uses
 // for a W8A8 problem, with or without a stream-K workspace; all 0 when M is

@@ -47,6 +47,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "quant_math.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -57,7 +58,9 @@ constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxClusterSplit = 8;
 
-enum class Op { kW8A16, kW8A8 };
+// kW8A8Q: W8A8 whose token rows arrive in bf16 and are quantized per token
+// inside the kernel (the activation quantization fused into the GEMM).
+enum class Op { kW8A16, kW8A8, kW8A8Q };
 
 struct DecodeParams {
     const void* x;           // bf16 [rows, K] (W8A16) or int8 [rows, K] (W8A8)
@@ -75,6 +78,8 @@ struct DecodeParams {
     unsigned* err;
     int one_wave;            // every CTA of the grid is resident at once
     const int32_t* gather;   // grouped: token row of x for each grouped row (null: row r is x's row r)
+    int8_t* qx_out;          // kW8A8Q: receives the token codes and scales when not null
+    float* sx_out;
     int64_t glu;             // grouped W8A16: intermediate size I of a fused gate/up
                              // projection (N = 2I) whose SiLU-gated product is the
                              // output [rows, I]; 0: plain outputs
@@ -156,16 +161,18 @@ struct WeightRegs {
 template <Op OP, int NT, bool GROUPED>
 struct Tuning {
     static constexpr bool kW8A16One = OP == Op::kW8A16 && NT == 1;
-    static constexpr int kStages = OP == Op::kW8A8 ? 4 : (NT == 1 ? 2 : 3);
+    static constexpr bool kInt = OP != Op::kW8A16;  // int8 x int8 -> int32
+    // (the token quantization of kW8A8Q needs the registers of one stage)
+    static constexpr int kStages = OP == Op::kW8A8 ? 4 : (OP == Op::kW8A8Q ? 3 : (NT == 1 ? 2 : 3));
     static constexpr int kMinCtas = (kW8A16One && GROUPED) ? 6 : (NT <= 2 ? 4 : (NT <= 4 ? 3 : 2));
-    static constexpr bool kXAhead = OP == Op::kW8A8 ? NT <= 2 : (kW8A16One && !GROUPED);
+    static constexpr bool kXAhead = kInt ? NT <= 2 : (kW8A16One && !GROUPED);
 };
 
 // MT 16-row m-tiles per warp, NT 8-token n-tiles per pass.
 template <Op OP, int MT, int NT, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
     decode_gemm_kernel(const DecodeParams p) {
-    using Acc = std::conditional_t<OP == Op::kW8A8, int32_t, float>;
+    using Acc = std::conditional_t<OP != Op::kW8A16, int32_t, float>;
     constexpr int kRows = 16 * MT;
     constexpr int kToks = 8 * NT;
     constexpr int kStages = Tuning<OP, NT, GROUPED>::kStages;
@@ -254,7 +261,43 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
             wbase[mt][h] = qw + n * K + 16 * t + ks_begin * 64;
         }
 
-    using XT = std::conditional_t<OP == Op::kW8A16, uint16_t, int8_t>;
+    // kW8A8Q: the per-token scales s = absmax / 127 over all of K, from
+    // the cluster's CTAs (each takes the absmax over its own k range; 16
+    // threads per token, at most 8 tokens), before any code is formed.
+    __shared__ float tok_amax[8];
+    __shared__ float tok_scale[8];
+    if constexpr (OP == Op::kW8A8Q) {
+        const int64_t k_lo = ksteps * rank / S * 64, k_hi = min(ksteps * (rank + 1) / S * 64, K);
+        const int tok = threadIdx.x >> 4, sub = threadIdx.x & 15;
+        const uint16_t* xr = static_cast<const uint16_t*>(p.x) + min((int64_t)tok, p.rows - 1) * K;
+        float a = 0.0f;
+        if (tok < p.rows)
+            for (int64_t k = k_lo + sub * 8; k < k_hi; k += 128) a = absmax8(ldg_cached(xr + k), a);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+        if (sub == 0) tok_amax[tok] = a;
+        if (S == 1)
+            __syncthreads();
+        else
+            cluster.sync();
+        if (threadIdx.x < 8) {
+            float full = tok_amax[threadIdx.x];
+            for (int r = 0; r < S; ++r) full = fmaxf(full, cluster.map_shared_rank(&tok_amax[0], r)[threadIdx.x]);
+            const float sc = full == 0.0f ? 1.0f : __fdiv_rn(full, 127.0f);  // zero-row guard
+            tok_scale[threadIdx.x] = sc;
+            if (p.sx_out && blockIdx.x == 0 && rank == 0 && threadIdx.x < p.rows) p.sx_out[threadIdx.x] = sc;
+        }
+        __syncthreads();
+        if (p.qx_out && blockIdx.x == 0 && tok < p.rows) {
+            // the codes themselves, for a caller that keeps them: row block 0
+            // writes each CTA's k range
+            const RowScale rs = make_row_scale(tok_scale[tok]);
+            for (int64_t k = k_lo + sub * 8; k < k_hi; k += 128)
+                *reinterpret_cast<uint2*>(p.qx_out + tok * K + k) = codes8(ldg_cached(xr + k), rs);
+        }
+    }
+
+    using XT = std::conditional_t<OP != Op::kW8A8, uint16_t, int8_t>;
     constexpr int kXW = OP == Op::kW8A16 ? 8 : 4;  // 32-bit words of x per lane per k-step
 
     for (int64_t c0 = lo; c0 < hi; c0 += kToks) {
@@ -276,10 +319,29 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[mt][nt][i] = Acc(0);
 
+        // kW8A8Q: each lane's token scale (for the reciprocal-based codes)
+        RowScale rsx[NT];
+        if constexpr (OP == Op::kW8A8Q) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                rsx[nt] = make_row_scale(tok_scale[min(c0 + nt * 8 + g, chunk_hi - 1) - c0]);
+        }
         auto load_x = [&](uint32_t (&xb)[NT][kXW], int i, bool ok) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                if (nt < nt_active && ok) {
+                if constexpr (OP == Op::kW8A8Q) {
+                    if (nt < nt_active && ok) {
+                        // 16 bf16 values -> 16 int8 codes, exactly as the
+                        // quantization kernel forms them
+                        const XT* xp = xbase[nt] + (int64_t)i * 64;
+                        const uint2 c0w = codes8(ldg_cached(xp), rsx[nt]);
+                        const uint2 c1w = codes8(ldg_cached(xp + 8), rsx[nt]);
+                        xb[nt][0] = c0w.x; xb[nt][1] = c0w.y; xb[nt][2] = c1w.x; xb[nt][3] = c1w.y;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < kXW; ++q) xb[nt][q] = 0u;
+                    }
+                } else if (nt < nt_active && ok) {
                     const XT* xp = xbase[nt] + (int64_t)i * 64;
                     const uint4 v0 = ldg_cached(xp);
                     xb[nt][0] = v0.x; xb[nt][1] = v0.y; xb[nt][2] = v0.z; xb[nt][3] = v0.w;
@@ -451,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
                 if constexpr (OP == Op::kW8A16) {
                     p.y[m * N + n] = f32_to_bf16_rn(s * sw[n]);
                 } else {
-                    float f = __fmul_rn(__fmul_rn(__int2float_rn(s), p.sx[m]), sw[n]);
+                    const float sxm = OP == Op::kW8A8Q ? tok_scale[m - c0] : p.sx[m];
+                    float f = __fmul_rn(__fmul_rn(__int2float_rn(s), sxm), sw[n]);
                     if (p.bias) f = __fadd_rn(f, bf16_to_f32(p.bias[n]));
                     p.y[m * N + n] = f32_to_bf16_rn(f);
                     if (p.acc) p.acc[m * N + n] = s;
@@ -530,7 +593,7 @@ cudaError_t dispatch(const DecodeParams& p, int64_t tokens_hint, int64_t groups_
 cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, const int8_t* qw, const float* sw,
                          uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env, const int32_t* gather,
                          int64_t glu) {
-    DecodeParams p{x, nullptr, offsets, qw, sw, nullptr, y, nullptr, M, N, K, E, env.err, 0, gather, glu};
+    DecodeParams p{x, nullptr, offsets, qw, sw, nullptr, y, nullptr, M, N, K, E, env.err, 0, gather, nullptr, nullptr, glu};
     if (offsets == nullptr) return dispatch<Op::kW8A16, false>(p, M, 1, env.sm_count, env.stream);
     // Grouped: at most min(E, T_total) experts have rows, on average
     // T_total / active rows each.
@@ -539,10 +602,17 @@ cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, c
     return dispatch<Op::kW8A16, true>(p, std::max<int64_t>(per_expert, 1), active, env.sm_count, env.stream);
 }
 
+cudaError_t launch_w8a8_decode_fused(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
+                                     uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
+                                     const LaunchEnv& env) {
+    DecodeParams p{x, nullptr, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err, 0, nullptr, qx, sx, 0};
+    return launch_auto<Op::kW8A8Q, 2, 1, false>(p, 1, env.sm_count, env.stream);
+}
+
 cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                                const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                const LaunchEnv& env) {
-    DecodeParams p{qx, sx, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err, 0, nullptr, 0};
+    DecodeParams p{qx, sx, nullptr, qw, sw, bias, y, acc, M, N, K, 1, env.err, 0, nullptr, nullptr, nullptr, 0};
     return dispatch<Op::kW8A8, false>(p, M, 1, env.sm_count, env.stream);
 }
 

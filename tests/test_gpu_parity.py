@@ -434,6 +434,63 @@ def test_w8a8_linear_matches_quantize_then_gemm(m, n, k):
     assert util.max_ulp_diff(util.bits(y)[pm, pn], ref_y) <= 1
 
 
+def _fused_linear_check(x, qw_ref, sw_ref, bias_bits=None):
+    """One fused call (quantization inside the decode kernel) against the
+    two calls and the oracle: codes, scales, accumulators bit-exact, outputs
+    bit-identical to the two calls."""
+    m, k = x.shape
+    n = qw_ref.shape[0]
+    qw, sw = dev(torch.from_numpy(qw_ref)), dev(torch.from_numpy(sw_ref))
+    bias = None if bias_bits is None else util.from_bits(bias_bits, "cuda")
+    xd = dev(x)
+    ybuf, y = util.guarded((m, n), torch.int16, "cuda", 0x7F7F)
+    qbuf, qx = util.guarded((m, k), torch.int8, "cuda", 77)
+    sbuf, sx = util.guarded((m,), torch.float32, "cuda", -3.0)
+    acc = torch.empty((m, n), dtype=torch.int32, device="cuda")
+    capi.w8a8_linear(xd, qw, sw, bias=bias, y=y.view(torch.bfloat16), qx=qx, sx=sx, acc_debug=acc)
+    qx2, sx2 = capi.quantize_act_per_token_int8(xd)
+    y2 = capi.w8a8_gemm(qx2, sx2, qw, sw, bias=bias)
+    torch.cuda.synchronize()
+    assert util.guard_intact(ybuf, m * n, 0x7F7F) and util.guard_intact(qbuf, m * k, 77)
+    assert util.guard_intact(sbuf, m, -3.0)
+    assert torch.equal(qx, qx2) and torch.equal(sx, sx2)
+    assert torch.equal(y, y2.view(torch.int16))
+    qx_ref, sx_ref = oracle.quant_rows(util.bits(x))
+    assert np.array_equal(qx.cpu().numpy(), qx_ref) and np.array_equal(sx.cpu().numpy(), sx_ref)
+    pm, pn = _points(m, n, 3000, m * 5 + n + k)
+    ref_acc, _, ref_y = oracle.w8a8_points(qx_ref, sx_ref, qw_ref, sw_ref, bias_bits, pm, pn)
+    assert np.array_equal(acc.cpu().numpy()[pm, pn].astype(np.int64), ref_acc)
+    assert util.max_ulp_diff(y.cpu().numpy().view(np.uint16)[pm, pn], ref_y) <= 1
+
+
+@pytest.mark.parametrize("m", [1, 2, 5, 8])
+@pytest.mark.parametrize("n,k", [(16, 16), (40, 48), (300, 1040), (2560, 2560), (513, 9744)])
+def test_w8a8_linear_fused_decode_shapes(m, n, k):
+    """A few tokens: the decode kernel quantizes its own token rows (the
+    cluster shares each token's absmax over its k ranges); ragged K, zero and
+    near-tie token rows included."""
+    x = synthetic.activations(m, k, 3 * m + k).float()
+    if m > 1:
+        x[1] = 0.0  # the zero-row guard inside the kernel
+    if m > 2:
+        g = np.random.default_rng(k)
+        js = g.integers(0, 127, k)
+        x[2] = torch.tensor([64 * (j + 0.5) / 127 * (1 if j % 2 else -1) for j in js])  # near-ties
+        x[2, 0] = 64.0
+    w = synthetic.weight(n, k, n + 3 * k)
+    qw_ref, sw_ref = oracle.quant_rows(util.bits(w))
+    bias_bits = util.bits(synthetic.bias(n, n)) if m % 2 else None
+    _fused_linear_check(x.to(torch.bfloat16), qw_ref, sw_ref, bias_bits)
+
+
+@pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
+def test_w8a8_linear_fused_qwen3_4b_decode(shape):
+    n, k = synthetic.QWEN3_4B_SHAPES[shape]
+    qw_ref, sw_ref = oracle.quant_rows(util.bits(synthetic.weight(n, k, 1)))
+    for m in (1, 4, 8):
+        _fused_linear_check(synthetic.activations(m, k, 60 + m), qw_ref, sw_ref)
+
+
 # ------------------------------------------------------------------ W8A16
 
 def gpu_w8a16(x_bf16, qw, sw):
