@@ -23,6 +23,16 @@ CUDA graph of one step and timed on its own, and prints ONE JSON line:
     o [4096, 4096], fused gate_up [24576, 4096], down [4096, 12288]; W8A16
     for M in {1, 2, 4, 8, 16, 32, 64} and the W8A8 linear layer for M in
     {1, 2, 4, 8, 16, 32, 64, 128, 512, 2048, 8192}.
+  FP8 prefill (block "fp8_prefill", TOPS against the 8-bit pipe): the
+    Qwen3-4B prefill shapes through the FP8 E4M3 linear layer.
+  W4A16 decode (block "w4a16_decode", GB/s): int4 group-128 quantization of
+    the Qwen3-8B weights and the W4A16 GEMM at M in {1, 4, 8}.
+  MoE expert MLP (block "moe_mlp", GB/s): the DeepSeek-MoE-16B layer for
+    T in {1, 8, 64}: device routing, gate/up with the SiLU-gated product,
+    down, weighted combine, one call each.
+  One-launch W8A8 (block "w8a8_linear_one_launch", GB/s): the Qwen3-4B
+    decode shapes through w8a8_linear_fused, the per-token quantization
+    inside the decode GEMM (the decode part runs the faster two launches).
 
 Every GEMM launch of a step reads its own copy of the int8 weights, and each
 part touches more than the 129 MB L2 per step, so no launch finds its
@@ -36,8 +46,11 @@ value (decode) = algorithmic HBM bytes of all launches / step time (GB/s);
 prefill TOPS = 2*M*N*K summed over the W8A8 launches / step time.
 Algorithmic bytes per launch: quantization 3*R*K + 4*R; W8A8
 M*K + N*K + 4*(M+N) + 2*M*N (+2*N bias); the W8A8 linear layer adds the
-quantization pass of its activations; W8A16 N*K + 4*N + 2*M*K + 2*M*N;
-grouped sum over experts with rows of (N*K + 4*N) + 2*rows*(K+N).
+quantization pass of its activations, except in one launch (decode), where
+it reads the bf16 tokens once: 2*M*K + N*K + 4*N + 2*M*N; W8A16
+N*K + 4*N + 2*M*K + 2*M*N; grouped sum over experts with rows of
+(N*K + 4*N) + 2*rows*(K+N); W4A16 N*K/2 + 2*N*K/128 + 2*M*K + 2*M*N; the
+expert MLP its experts' weights and scales plus its row traffic.
 
 cpu_baseline times the CPU oracle (the only reference implementation: the
 pages ship no code) on the host cores, with one thread and with every core,
@@ -69,6 +82,7 @@ DECODE_MS = (1, 4, 8)
 PREFILL_MS = (128, 512, 2048, 4096)
 MOE_TOKENS = (1, 8, 64)
 SWEEP_W8A16_MS = (1, 2, 4, 8, 16, 32, 64)
+W4_MS = (1, 4, 8)
 SWEEP_W8A8_MS = (1, 2, 4, 8, 16, 32, 64, 128, 512, 2048, 8192)
 W8A8_DECODE_MAX_M = 64  # above it a W8A8 call runs on the tensor-core kernel
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -79,8 +93,15 @@ PART_CLASSES = {
     "decode": ("quant_w", "quant_x", "w8a8", "w8a16", "grouped"),
     "prefill": ("w8a8",),
     "sweep8b": ("w8a16", "w8a8_decode", "w8a8_prefill"),
+    "fp8": ("fp8",),
+    "w4": ("quant_w4", "w4a16"),
+    "moe": ("moe_mlp",),
+    "fused": ("w8a8_fused",),
 }
-TENSOR_CLASSES = {("prefill", "w8a8"), ("sweep8b", "w8a8_prefill")}
+# tensor-bound classes and the peak each is measured against: the int8
+# W8A8 kernel runs on the fp16 pipe (the bf16 rate), FP8 on the 8-bit pipe
+# (twice the bf16 rate, the nominal ratio)
+TENSOR_CLASSES = {("prefill", "w8a8"): 1.0, ("sweep8b", "w8a8_prefill"): 1.0, ("fp8", "fp8"): 2.0}
 
 
 # ---------------------------------------------------------------- accounting
@@ -102,6 +123,30 @@ def bytes_grouped(counts, n, k):
     return len(active) * (n * k + 4 * n) + 2 * sum(active) * (k + n)
 
 
+def bytes_linear_fused(m, n, k, bias):
+    """W8A8 from bf16 tokens in one pass: the tokens are read once as bf16
+    and their codes never leave the kernel."""
+    return 2 * m * k + n * k + 4 * n + 2 * m * n + (2 * n if bias else 0)
+
+
+def bytes_w4a16(m, n, k):
+    return n * k // 2 + 2 * n * (k // 128) + 2 * m * k + 2 * m * n
+
+
+def bytes_quant_w4(n, k):
+    return 2 * n * k + n * k // 2 + 2 * n * (k // 128)
+
+
+def bytes_moe(counts, tokens, hidden, inter, routed):
+    """The expert MLP: the weights and scales of every expert with rows
+    (gate/up and down), the gathered tokens, h written and read, the down
+    outputs written and read by the combine, the outputs and the logits."""
+    active = [int(c) for c in counts if c > 0]
+    rows = sum(active)
+    weights = len(active) * (2 * inter * hidden + 8 * inter + hidden * inter + 4 * hidden)
+    return weights + 2 * rows * hidden + 4 * rows * inter + 4 * rows * hidden + 2 * tokens * hidden + 4 * tokens * routed
+
+
 def workload_name(part):
     if part == "decode":
         return ("Qwen3-4B decode linears (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, "
@@ -111,6 +156,18 @@ def workload_name(part):
     if part == "prefill":
         return ("Qwen3-4B prefill W8A8 (QKV 6144x2560, o 2560x2560, gate_up 19456x2560, down 9728->2560; "
                 "M in {128,512,2048,4096}; W8A8 linear from bf16 activations (per-token act quant fused), bias on)")
+    if part == "fp8":
+        return ("Qwen3-4B prefill FP8 E4M3 W8A8 (same four shapes, M in {128,512,2048,4096}, per-token dynamic "
+                "FP8 activations and per-channel FP8 weights, bias on; FP8 linear from bf16 activations)")
+    if part == "w4":
+        return ("Qwen3-8B W4A16 group-128 decode (QKV 6144x4096, o 4096x4096, gate_up 24576x4096, down 12288->4096; "
+                "M in {1,4,8}; int4 weight quantization + W4A16 GEMM)")
+    if part == "fused":
+        return ("Qwen3-4B decode W8A8 linear layer in one launch (per-token quantization inside the decode GEMM; "
+                "the four shapes, M in {1,4,8})")
+    if part == "moe":
+        return ("DeepSeek-MoE-16B expert MLP, int8 weight-only (66 experts, top-6 + 2 shared; device routing, "
+                "gate_up 2816x2048 with the SiLU-gated product, down 2048x1408, weighted combine; T in {1,8,64})")
     return ("Qwen3-8B sweep (QKV 6144x4096, o 4096x4096, gate_up 24576x4096, down 12288->4096; "
             "W8A16 for M in {1,2,4,8,16,32,64}; W8A8 linear from bf16 activations for "
             "M in {1,2,4,8,16,32,64,128,512,2048,8192})")
@@ -172,17 +229,14 @@ class Workload:
     """Device buffers and the ordered launch list of one step of a part."""
 
     def __init__(self, part, device, seed=1):
+        from int8_quantized_linear_gb300 import capi
+        self._capi = capi
         self.part = part
         self.device = device
         self.launches: list[Launch] = []
         self.h2d: list[tuple[torch.Tensor, torch.Tensor]] = []  # (pinned host, device) inputs
         self.d2h: list[tuple[torch.Tensor, torch.Tensor]] = []  # (device, pinned host) results
-        if part == "decode":
-            self._decode(seed)
-        elif part == "prefill":
-            self._prefill(seed)
-        else:
-            self._sweep8b(seed)
+        getattr(self, "_" + part)(seed)
         # Launches of one kernel class run back to back (stable order
         # otherwise), so that consecutive launches can overlap through
         # programmatic dependent launch and a pair of events brackets each
@@ -308,6 +362,86 @@ class Workload:
                 self._linear(kind, x, qs[c], s, None, f"w8a8_linear {name}")
                 c += 1
 
+    def _fp8(self, seed):
+        from int8_quantized_linear_gb300 import capi, synthetic
+        for si, (name, (n, k)) in enumerate(synthetic.QWEN3_4B_SHAPES.items()):
+            w = synthetic.weight(n, k, seed + si, device=self.device)
+            q0, s = capi.quantize_weight_per_channel_fp8(w)
+            del w
+            bias = synthetic.bias(n, seed + si, device=self.device)
+            for mi, m in enumerate(PREFILL_MS):
+                q = q0 if mi == 0 else q0.clone()
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=self.device)
+                self._pin_in(x)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=self.device)
+                self.launches.append(Launch(
+                    "fp8", lambda x=x, q=q, s=s, b=bias, y=y: capi.w8a8_fp8_linear(x, q, s, bias=b, y=y),
+                    bytes_quant(m, k) + bytes_w8a8(m, n, k, True), 2 * m * n * k, f"fp8_linear {name} M={m}",
+                    gpu_kernels=2))
+                self._pin_out(y)
+
+    def _w4(self, seed):
+        from int8_quantized_linear_gb300 import capi, synthetic
+        seed += 40
+        for si, (name, (n, k)) in enumerate(synthetic.QWEN3_8B_SHAPES.items()):
+            w = synthetic.weight(n, k, seed + si, device=self.device)
+            self._pin_in(w)
+            q0, s0 = capi.quantize_weight_w4_g128(w)
+            self.launches.append(Launch(
+                "quant_w4", lambda w=w, q=q0, s=s0: capi.quantize_weight_w4_g128(w, q=q, scale=s),
+                bytes_quant_w4(n, k), 0, f"quant_w4 {name}"))
+            for mi, m in enumerate(W4_MS):
+                q = q0.clone()
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=self.device)
+                self._pin_in(x)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=self.device)
+                self.launches.append(Launch(
+                    "w4a16", lambda x=x, q=q, s=s0, y=y: capi.w4a16_gemm(x, q, s, y=y),
+                    bytes_w4a16(m, n, k), 2 * m * n * k, f"w4a16 {name} M={m}"))
+                self._pin_out(y)
+
+    def _fused(self, seed):
+        from int8_quantized_linear_gb300 import synthetic
+        for si, (name, (n, k)) in enumerate(synthetic.QWEN3_4B_SHAPES.items()):
+            w, qs, s = self._weight_copies(n, k, seed + si, len(DECODE_MS))
+            del w
+            for mi, m in enumerate(DECODE_MS):
+                x = synthetic.activations(m, k, 100 * seed + 10 * si + mi, device=self.device)
+                self._pin_in(x)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=self.device)
+                self.launches.append(Launch(
+                    "w8a8_fused", lambda x=x, q=qs[mi], s=s, y=y: self._capi.w8a8_linear(x, q, s, y=y, fused=True),
+                    bytes_linear_fused(m, n, k, False), 2 * m * n * k, f"w8a8_linear_fused {name} M={m}"))
+                self._pin_out(y)
+
+    def _moe(self, seed):
+        from int8_quantized_linear_gb300 import capi, synthetic
+        dev = self.device
+        (inter2, hidden), (_, inter) = synthetic.DSMOE_SHAPES["gate_up"], synthetic.DSMOE_SHAPES["down"]
+        e_count = synthetic.DSMOE_ROUTED + synthetic.DSMOE_SHARED
+        for ti, tokens in enumerate(MOE_TOKENS):
+            weights = []
+            for pi, (proj, (n, k)) in enumerate(synthetic.DSMOE_SHAPES.items()):
+                q = torch.empty((e_count, n, k), dtype=torch.int8, device=dev)
+                s = torch.empty((e_count, n), dtype=torch.float32, device=dev)
+                for e in range(e_count):
+                    we = synthetic.weight(n, k, 1000 + 100 * pi + e, device=dev)
+                    capi.quantize_weight_per_channel_int8(we, q=q[e], scale=s[e])
+                weights += [q, s]
+            x = synthetic.activations(tokens, hidden, 600 + ti, device=dev)
+            logits = synthetic.gate_logits(tokens, synthetic.DSMOE_ROUTED, 3 + ti).to(dev)
+            self._pin_in(x)
+            self._pin_in(logits)
+            out = torch.empty((tokens, hidden), dtype=torch.bfloat16, device=dev)
+            counts = np.diff(synthetic.moe_routing(tokens, seed=3 + ti).offsets)
+            rows = int(counts.sum())
+            self.launches.append(Launch(
+                "moe_mlp", lambda x=x, lg=logits, w=weights, o=out: capi.moe_expert_mlp_w8a16(
+                    x, lg, synthetic.DSMOE_TOPK, synthetic.DSMOE_SHARED, w[0], w[1], w[2], w[3], out=o),
+                bytes_moe(counts, tokens, hidden, inter, synthetic.DSMOE_ROUTED),
+                2 * rows * (inter2 * hidden + hidden * inter), f"moe_mlp T={tokens}", gpu_kernels=4))
+            self._pin_out(out)
+
     def run(self, events=None):
         """One step; events[b] = (start, end) brackets batch b."""
         for b, (_, launches) in enumerate(self.batches):
@@ -395,12 +529,17 @@ def oracle_step(sample):
             _, src = item
             oracle.quant_rows(src)
             total_b += bytes_quant(*src.shape)
-        elif kind == "w8a8":
+        elif kind in ("w8a8", "linear"):
+            # per-token quantization then the W8A8 GEMM, counted as the GPU
+            # step counts it (one pass over bf16 tokens for "linear")
             _, xb, qw, sw, bias = item
             qx, sx = oracle.quant_rows(xb)
             oracle.w8a8(qx, sx, qw, sw, bias)
             m, k = xb.shape
-            total_b += bytes_quant(m, k) + bytes_w8a8(m, qw.shape[0], k, bias is not None)
+            if kind == "linear":
+                total_b += bytes_linear_fused(m, qw.shape[0], k, bias is not None)
+            else:
+                total_b += bytes_quant(m, k) + bytes_w8a8(m, qw.shape[0], k, bias is not None)
             total_ops += 2 * m * qw.shape[0] * k
         elif kind == "w8a16":
             _, xb, qw, sw = item
@@ -526,9 +665,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     import oracle
-    part = "decode" if args.workload == "all" else args.workload
-    if part == "sweep8b":
-        part = "decode"
+    part = "prefill" if args.workload in ("prefill", "fp8") else "decode"
     frac = args.ref_row_frac
     sample = build_oracle_sample(part, frac)
     cores = oracle.set_threads(os.cpu_count() or 1)
@@ -640,7 +777,7 @@ def time_part(part, args, world, local, stream):
             tops = e["flops"] / (e["ms"] / 1e3) / 1e12
             entry["TOPS"] = tops
             if (part, name) in TENSOR_CLASSES:
-                entry["tensor_frac"] = tops / peaks["bf16_tflops"]
+                entry["tensor_frac"] = tops / (peaks["bf16_tflops"] * TENSOR_CLASSES[(part, name)])
         kernels[name] = entry
 
     e2e = run_e2e(args, wl, stream, g_warm, world, part)
@@ -660,10 +797,13 @@ def roofline(part, res, kernel=None):
     d = per[dom]
     per_launch_bytes = d["bytes"] / d["launches"]
     if (part, dom) in TENSOR_CLASSES:
+        ratio = TENSOR_CLASSES[(part, dom)]
         achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
-                "peak_source": f"{peak_src} bf16_tflops burst (fp16 kind::f16 pipe, nominal ratio 1)",
+        peak = peaks["bf16_tflops"] * ratio
+        pipe = "fp8 kind::f8f6f4 pipe" if ratio == 2.0 else "fp16 kind::f16 pipe"
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16_tflops burst x {ratio:g} ({pipe}, nominal ratio {ratio:g})",
                 "kernel": dom}
     else:
         achieved = per_launch_bytes / (d["ms"] / d["launches"] / 1e3) / 1e9
@@ -674,11 +814,22 @@ def roofline(part, res, kernel=None):
     return roof
 
 
+ALL_PARTS = ("decode", "prefill", "sweep8b", "fp8", "w4", "moe", "fused")
+
+
+def part_value(part, wl, ms, world):
+    """The part's throughput in its unit: TOPS (2*M*N*K of the tensor-core
+    launches) for the prefill parts, algorithmic GB/s otherwise."""
+    if part in ("prefill", "fp8"):
+        return world * wl.step_flops(set(PART_CLASSES[part])) / (ms / 1e3) / 1e12, "TOPS"
+    return world * wl.step_bytes / (ms / 1e3) / 1e9, "GB/s"
+
+
 def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     stream = torch.cuda.Stream(device)
-    parts = ("decode", "prefill", "sweep8b") if args.workload == "all" else (args.workload,)
+    parts = ALL_PARTS if args.workload == "all" else (args.workload,)
     results = {}
     for part in parts:
         results[part] = time_part(part, args, world, local, stream)
@@ -686,11 +837,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
     top = parts[0]
     r = results[top]
-    wl = r["wl"]
-    if top == "prefill":
-        value, unit = world * wl.step_flops({"w8a8"}) / (r["ms_step"] / 1e3) / 1e12, "TOPS"
-    else:
-        value, unit = world * wl.step_bytes / (r["ms_step"] / 1e3) / 1e9, "GB/s"
+    value, unit = part_value(top, r["wl"], r["ms_step"], world)
     reasons = sorted({x for res in results.values() for x in res["clocks"].get("reasons", [])})
     clocks = dict(r["clocks"])
     clocks["reasons"] = reasons
@@ -731,9 +878,17 @@ def run_ours(args, world, rank, local):
             line.update({k: v for k, v in block.items() if k in ("kernels",)})
         else:
             line["qwen3_8b_sweep"] = block
+    for part, key in (("fp8", "fp8_prefill"), ("w4", "w4a16_decode"), ("moe", "moe_mlp"),
+                      ("fused", "w8a8_linear_one_launch")):
+        if part in results and top != part:
+            b = results[part]
+            v, u = part_value(part, b["wl"], b["ms_step"], world)
+            line[key] = {"workload": workload_name(part), "value": v, "unit": u, "ms_per_step": b["ms_step"],
+                         "roofline": roofline(part, b), "kernels": b["kernels"], "e2e": b["e2e"],
+                         "clocks": b["clocks"], "gpu_launches": b["launches"]}
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
-        frac = args.cpu_row_frac if args.cpu_row_frac is not None else (1 / 2 if top == "decode" else 1 / 8)
-        cpu_part = top if top != "sweep8b" else "decode"
+        frac = args.cpu_row_frac if args.cpu_row_frac is not None else (1 / 8 if top in ("prefill", "fp8") else 1 / 2)
+        cpu_part = "prefill" if top in ("prefill", "fp8") else "decode"
         line["cpu_baseline"] = cpu_baseline(cpu_part, frac)
         if "prefill" in line:
             line["prefill"]["cpu_baseline"] = cpu_baseline("prefill", 1 / 8)
@@ -766,10 +921,7 @@ def run_e2e(args, wl, stream, graph, world, part):
         end.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(start.elapsed_time(end), world) / steps
-    if part == "prefill":
-        value, unit = world * wl.step_flops({"w8a8"}) / (ms / 1e3) / 1e12, "TOPS"
-    else:
-        value, unit = world * wl.step_bytes / (ms / 1e3) / 1e9, "GB/s"
+    value, unit = part_value(part, wl, ms, world)
     return {"value": value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": steps}
 
@@ -837,7 +989,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["all", "decode", "prefill", "sweep8b"], default="all")
+    ap.add_argument("--workload", choices=["all", *ALL_PARTS], default="all")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-row-frac", type=float, default=None,

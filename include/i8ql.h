@@ -144,6 +144,29 @@ i8ql_status w8a8_linear(const i8ql_bf16* x, const int8_t* qw, const float* sw, c
                         int64_t M, int64_t N, int64_t K, void* stream);
 
 /*
+ * The W8A8 linear layer from bf16 activations in ONE launch, for up to 8
+ * tokens: the per-token activation quantization runs inside the decode
+ * GEMM itself (its prologue and its token loads), not as a separate pass.
+ *
+ * Source: "Day 6 -- Quantize It Yourself", "Some interesting facts I
+ * recently learned", item 2 (per-token activation quantization is extra work
+ * in every forward pass) and The mechanism, block 5.
+ *
+ * Computes exactly what w8a8_linear computes (the same codes, scales,
+ * accumulators and outputs, bit for bit; same arguments).  The CTAs that
+ * split one row block's k range share each token's absmax through
+ * distributed shared memory, then form the int8 codes from the bf16 tokens
+ * in their main loop.  No workspace.  M > 8 returns I8QL_ERR_UNSUPPORTED.
+ * Measured on GB300 it is slower than w8a8_linear's two launches, whose
+ * quantization pass overlaps the GEMM's prologue through programmatic
+ * dependent launch, so w8a8_linear does not use it; it serves callers that
+ * want one kernel per layer.
+ */
+i8ql_status w8a8_linear_fused(const i8ql_bf16* x, const int8_t* qw, const float* sw, const i8ql_bf16* bias,
+                              i8ql_bf16* y, int8_t* qx, float* sx, int32_t* acc_debug, int64_t M, int64_t N, int64_t K,
+                              void* stream);
+
+/*
  * Weight-only W8A16 GEMM / GEMV (decode).
  *
  * Source: "Day 6 -- Quantize It Yourself", The mechanism, block 5 (int8

@@ -51,6 +51,7 @@ SIGNATURES = {
     "w8a8_fp8_linear": (_S, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "quantize_weight_w4_g128": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "w4a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w8a8_linear_fused": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "moe_route_topk": (_S, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "grouped_w8a16_silu_mul": (_S, [_P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P]),
     "moe_combine": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -143,10 +144,11 @@ def quantize_act_per_token_int8(x: torch.Tensor, q=None, scale=None, stream=None
     return _quant("quantize_act_per_token_int8", x, q, scale, stream)
 
 
-def w8a8_linear(x, qw, sw, bias=None, y=None, qx=None, sx=None, acc_debug=None, stream=None):
+def w8a8_linear(x, qw, sw, bias=None, y=None, qx=None, sx=None, acc_debug=None, stream=None, fused=False):
     """bf16 y [M, N] = w8a8_gemm(quantize_act_per_token_int8(x), qw, sw, bias),
     with the quantization fused into the call; qx / sx, when given, receive
-    the token codes and scales."""
+    the token codes and scales.  fused=True takes the one-launch entry point
+    (w8a8_linear_fused, M <= 8)."""
     m, k = x.shape
     n = qw.shape[0]
     _need(x, torch.bfloat16, (m, k), "x")
@@ -163,9 +165,10 @@ def w8a8_linear(x, qw, sw, bias=None, y=None, qx=None, sx=None, acc_debug=None, 
         _need(sx, torch.float32, (m,), "sx")
     if acc_debug is not None:
         _need(acc_debug, torch.int32, (m, n), "acc_debug")
-    st = lib().w8a8_linear(_ptr(x), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y), _ptr(qx), _ptr(sx),
-                           _ptr(acc_debug), m, n, k, _stream(stream))
-    _check(st, "w8a8_linear")
+    name = "w8a8_linear_fused" if fused else "w8a8_linear"
+    st = getattr(lib(), name)(_ptr(x), _ptr(qw), _ptr(sw), _ptr(bias), _ptr(y), _ptr(qx), _ptr(sx),
+                              _ptr(acc_debug), m, n, k, _stream(stream))
+    _check(st, name)
     return y
 
 

@@ -185,6 +185,29 @@ i8ql_status w8a8_linear(const i8ql_bf16* x, const int8_t* qw, const float* sw, c
     return from_cuda(launch_w8a8_linear(x, qw, sw, bias, y, qx, sx, acc_debug, M, N, K, env));
 }
 
+i8ql_status w8a8_linear_fused(const i8ql_bf16* x, const int8_t* qw, const float* sw, const i8ql_bf16* bias,
+                              i8ql_bf16* y, int8_t* qx, float* sx, int32_t* acc_debug, int64_t M, int64_t N, int64_t K,
+                              void* stream) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    if (M > kW8A8FusedMaxM) return I8QL_ERR_UNSUPPORTED;
+    I8QL_TRY(check_rows(N));
+    I8QL_TRY(check_matrix(x, M));
+    I8QL_TRY(check_matrix(qw, N));
+    I8QL_TRY(check_vec(sw, N, 4));
+    if (bias != nullptr && !aligned(bias, 2)) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_matrix(y, M));
+    if (qx != nullptr) I8QL_TRY(check_matrix(qx, M));
+    if (sx != nullptr && !aligned(sx, 4)) return I8QL_ERR_INVALID_ARG;
+    if (acc_debug != nullptr && !aligned(acc_debug, 16)) return I8QL_ERR_INVALID_ARG;
+    if (M == 0) return I8QL_OK;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(stream, &env, &s)) return s;
+    return from_cuda(launch_w8a8_decode_fused(x, qw, sw, bias, y, qx, sx, acc_debug, M, N, K, env));
+}
+
 i8ql_status w8a16_gemm(const i8ql_bf16* x, const int8_t* qw, const float* sw, i8ql_bf16* y,
                        int64_t M, int64_t N, int64_t K, void* stream) {
     I8QL_TRY(check_rows(M));

@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
     // threads per token, at most 8 tokens), before any code is formed.
     __shared__ float tok_amax[8];
     __shared__ float tok_scale[8];
-    if constexpr (OP == Op::kW8A8Q) {
+    // kW8A8Q: called once the first weight loads are in flight, so that
+    // this pass over the tokens overlaps their latency.
+    auto quant_prologue = [&]() {
         const int64_t k_lo = ksteps * rank / S * 64, k_hi = min(ksteps * (rank + 1) / S * 64, K);
         const int tok = threadIdx.x >> 4, sub = threadIdx.x & 15;
         const uint16_t* xr = static_cast<const uint16_t*>(p.x) + min((int64_t)tok, p.rows - 1) * K;
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
             for (int64_t k = k_lo + sub * 8; k < k_hi; k += 128)
                 *reinterpret_cast<uint2*>(p.qx_out + tok * K + k) = codes8(ldg_cached(xr + k), rs);
         }
-    }
+    };
 
     using XT = std::conditional_t<OP != Op::kW8A8, uint16_t, int8_t>;
     constexpr int kXW = OP == Op::kW8A16 ? 8 : 4;  // 32-bit words of x per lane per k-step
@@ -319,13 +321,9 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[mt][nt][i] = Acc(0);
 
-        // kW8A8Q: each lane's token scale (for the reciprocal-based codes)
+        // kW8A8Q: each lane's token scale (for the reciprocal-based codes),
+        // set once the scales are known, before the first token load
         RowScale rsx[NT];
-        if constexpr (OP == Op::kW8A8Q) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                rsx[nt] = make_row_scale(tok_scale[min(c0 + nt * 8 + g, chunk_hi - 1) - c0]);
-        }
         auto load_x = [&](uint32_t (&xb)[NT][kXW], int i, bool ok) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -399,6 +397,13 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
 #pragma unroll
             for (int s = 0; s < kStages; ++s)
                 if (s < main_count) load_w(ring[s], s);
+            if constexpr (OP == Op::kW8A8Q) {
+                // (a single token chunk: M <= 8)
+                quant_prologue();
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    rsx[nt] = make_row_scale(tok_scale[min(c0 + nt * 8 + g, chunk_hi - 1) - c0]);
+            }
             uint32_t xb[NT][kXW];
             if constexpr (kXAhead) load_x(xb, 0, main_count > 0);
             for (int i0 = 0; i0 < main_count; i0 += kStages) {

@@ -122,8 +122,6 @@ cudaError_t linear_layout(int64_t M, int64_t N, int64_t K, bool have_qx, bool ha
 cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias, uint16_t* y,
                                int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                const LaunchEnv& env) {
-    // a few tokens: one launch, the decode kernel quantizes its token rows
-    if (M <= kW8A8FusedMaxM) return launch_w8a8_decode_fused(x, qw, sw, bias, y, qx, sx, acc, M, N, K, env);
     LinearLayout l;
     cudaError_t e = linear_layout(M, N, K, qx != nullptr, sx != nullptr, env.sm_count, &l);
     if (e != cudaSuccess) return e;

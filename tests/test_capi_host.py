@@ -246,3 +246,16 @@ def test_moe_argument_errors(lib):
     assert m(*a) == capi.I8QL_OK
     if not torch.cuda.is_available():
         assert m(*ok) == capi.I8QL_ERR_NO_DEVICE
+
+
+def test_w8a8_linear_fused_argument_errors(lib):
+    f = lib.w8a8_linear_fused
+    ok = (A, B, C, None, D, None, None, None, 8, 16, 64, None)
+    args = list(ok); args[8] = 9
+    assert f(*args) == capi.I8QL_ERR_UNSUPPORTED          # more than 8 tokens
+    args = list(ok); args[10] = 40
+    assert f(*args) == capi.I8QL_ERR_UNSUPPORTED          # K % 16
+    args = list(ok); args[0] = None
+    assert f(*args) == capi.I8QL_ERR_INVALID_ARG
+    args = list(ok); args[8] = 0
+    assert f(*args) == capi.I8QL_OK

@@ -435,9 +435,9 @@ def test_w8a8_linear_matches_quantize_then_gemm(m, n, k):
 
 
 def _fused_linear_check(x, qw_ref, sw_ref, bias_bits=None):
-    """One fused call (quantization inside the decode kernel) against the
-    two calls and the oracle: codes, scales, accumulators bit-exact, outputs
-    bit-identical to the two calls."""
+    """The one-launch layer (quantization inside the decode kernel) against
+    the two calls and the oracle: codes, scales, accumulators bit-exact,
+    outputs bit-identical to the two calls."""
     m, k = x.shape
     n = qw_ref.shape[0]
     qw, sw = dev(torch.from_numpy(qw_ref)), dev(torch.from_numpy(sw_ref))
@@ -447,14 +447,15 @@ def _fused_linear_check(x, qw_ref, sw_ref, bias_bits=None):
     qbuf, qx = util.guarded((m, k), torch.int8, "cuda", 77)
     sbuf, sx = util.guarded((m,), torch.float32, "cuda", -3.0)
     acc = torch.empty((m, n), dtype=torch.int32, device="cuda")
-    capi.w8a8_linear(xd, qw, sw, bias=bias, y=y.view(torch.bfloat16), qx=qx, sx=sx, acc_debug=acc)
+    capi.w8a8_linear(xd, qw, sw, bias=bias, y=y.view(torch.bfloat16), qx=qx, sx=sx, acc_debug=acc, fused=True)
+    y_plain = capi.w8a8_linear(xd, qw, sw, bias=bias, fused=True)  # no optional outputs
     qx2, sx2 = capi.quantize_act_per_token_int8(xd)
     y2 = capi.w8a8_gemm(qx2, sx2, qw, sw, bias=bias)
     torch.cuda.synchronize()
     assert util.guard_intact(ybuf, m * n, 0x7F7F) and util.guard_intact(qbuf, m * k, 77)
     assert util.guard_intact(sbuf, m, -3.0)
     assert torch.equal(qx, qx2) and torch.equal(sx, sx2)
-    assert torch.equal(y, y2.view(torch.int16))
+    assert torch.equal(y, y2.view(torch.int16)) and torch.equal(y_plain.view(torch.int16), y)
     qx_ref, sx_ref = oracle.quant_rows(util.bits(x))
     assert np.array_equal(qx.cpu().numpy(), qx_ref) and np.array_equal(sx.cpu().numpy(), sx_ref)
     pm, pn = _points(m, n, 3000, m * 5 + n + k)
