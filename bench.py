@@ -740,6 +740,8 @@ def time_part(part, args, world, local, stream):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)  # let the sampler start
+    if args.profile_timed:
+        torch.cuda.profiler.start()
     with torch.cuda.stream(stream):
         start.record(stream)
         if use_graph:
@@ -749,6 +751,8 @@ def time_part(part, args, world, local, stream):
                 wl.run(events[s])
         end.record(stream)
     torch.cuda.synchronize()
+    if args.profile_timed:
+        torch.cuda.profiler.stop()
     clk = clocks.stop()
     barrier(world)
     ms_step = max_over_ranks(start.elapsed_time(end), world) / steps
@@ -954,6 +958,52 @@ def run_single(args, local):
         else:
             fns = [lambda q=q: capi.w8a16_gemm(x, q, s, y=y) for q in qs]
             nbytes, flops = bytes_w8a16(m, n, k), 2 * m * n * k
+    elif kind in ("w4a16", "fp8"):
+        m, n, k = dims
+        w = synthetic.weight(n, k, 1, device=dev)
+        x = synthetic.activations(m, k, 2, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        if kind == "w4a16":
+            q0, s = capi.quantize_weight_w4_g128(w)
+            copies = max(1, -(-l2 // (n * k // 2)))
+            qs = [q0] + [q0.clone() for _ in range(copies - 1)]
+            fns = [lambda q=q: capi.w4a16_gemm(x, q, s, y=y) for q in qs]
+            nbytes, flops = bytes_w4a16(m, n, k), 2 * m * n * k
+        else:
+            q0, s = capi.quantize_weight_per_channel_fp8(w)
+            copies = max(1, -(-l2 // (n * k)))
+            qs = [q0] + [q0.clone() for _ in range(copies - 1)]
+            fns = [lambda q=q: capi.w8a8_fp8_linear(x, q, s, y=y) for q in qs]
+            nbytes, flops = bytes_quant(m, k) + bytes_w8a8(m, n, k, False), 2 * m * n * k
+        del w
+    elif kind == "quant_w4":
+        r, k = dims
+        copies = max(1, -(-l2 // (2 * r * k)))
+        ws = [synthetic.weight(r, k, 1 + c, device=dev) for c in range(copies)]
+        q = torch.empty((r, k // 2), dtype=torch.uint8, device=dev)
+        sc = torch.empty((r, k // 128), dtype=torch.bfloat16, device=dev)
+        fns = [lambda w=w: capi.quantize_weight_w4_g128(w, q=q, scale=sc) for w in ws]
+        nbytes, flops = bytes_quant_w4(r, k), 0
+    elif kind == "moe":
+        (tokens,) = dims
+        (inter2, hidden), (_, inter) = synthetic.DSMOE_SHAPES["gate_up"], synthetic.DSMOE_SHAPES["down"]
+        e_count = synthetic.DSMOE_ROUTED + synthetic.DSMOE_SHARED
+        weights = []
+        for pi, (n, k) in enumerate(synthetic.DSMOE_SHAPES.values()):
+            q = torch.empty((e_count, n, k), dtype=torch.int8, device=dev)
+            sc = torch.empty((e_count, n), dtype=torch.float32, device=dev)
+            for e in range(e_count):
+                capi.quantize_weight_per_channel_int8(synthetic.weight(n, k, 1000 + 100 * pi + e, device=dev),
+                                                      q=q[e], scale=sc[e])
+            weights += [q, sc]
+        x = synthetic.activations(tokens, hidden, 600, device=dev)
+        logits = synthetic.gate_logits(tokens, synthetic.DSMOE_ROUTED, 3).to(dev)
+        out = torch.empty((tokens, hidden), dtype=torch.bfloat16, device=dev)
+        fns = [lambda: capi.moe_expert_mlp_w8a16(x, logits, synthetic.DSMOE_TOPK, synthetic.DSMOE_SHARED,
+                                                 *weights, out=out)]
+        counts = np.diff(synthetic.moe_routing(tokens, seed=3).offsets)
+        nbytes = bytes_moe(counts, tokens, hidden, inter, synthetic.DSMOE_ROUTED)
+        flops = 2 * int(counts.sum()) * (inter2 * hidden + hidden * inter)
     elif kind == "quant":
         r, k = dims
         copies = max(1, -(-l2 // (2 * r * k)))
@@ -992,12 +1042,16 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["all", *ALL_PARTS], default="all")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-timed", action="store_true",
+                    help="bracket each part's timed region with cudaProfilerStart/Stop, so that "
+                         "`ncu --profile-from-start off` lists exactly the timed launches")
     ap.add_argument("--cpu-row-frac", type=float, default=None,
                     help="row fraction of the cpu_baseline sample (default: 1/2 for decode, 1/8 for prefill)")
     ap.add_argument("--ref-row-frac", type=float, default=1 / 8)
     ap.add_argument("--single", default=None,
-                    help="time one kernel: w8a8:M:N:K, linear:M:N:K, w8a16:M:N:K or quant:R:K "
-                         "(eager, for profiling)")
+                    help="time one call: w8a8:M:N:K, linear:M:N:K, w8a16:M:N:K, quant:R:K, "
+                         "w4a16:M:N:K, quant_w4:N:K, fp8:M:N:K (the FP8 linear layer) or moe:T "
+                         "(the DeepSeek-MoE expert MLP) (eager, for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

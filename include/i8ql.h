@@ -237,9 +237,10 @@ i8ql_status quantize_act_per_token_fp8(const i8ql_bf16* x, int64_t M, int64_t K,
  * Inputs: qx uint8 [M, K] and qw uint8 [N, K] E4M3 codes (K-contiguous),
  * sx fp32 [M], sw fp32 [N], bias bf16 [N] or NULL.  Output y bf16 [M, N].
  * Every product of two E4M3 values is exact in fp32; the sum is accumulated
- * in fp32 by the tensor core, so y differs from the exact value by fp32
- * accumulation rounding and one bf16 rounding.  No workspace.  Argument
- * rules and errors as w8a8_gemm.
+ * in fp32 by the tensor core (with split-K, see i8ql_fp8_plan, as the sum of
+ * the CTAs' fp32 partial sums in a fixed order), so y differs from the exact
+ * value by fp32 accumulation rounding and one bf16 rounding.  No workspace.
+ * Argument rules and errors as w8a8_gemm.
  */
 i8ql_status w8a8_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
                           const i8ql_bf16* bias, i8ql_bf16* y, int64_t M, int64_t N, int64_t K, void* stream);
@@ -413,6 +414,19 @@ i8ql_status moe_expert_mlp_w8a16(const i8ql_bf16* x, const float* logits, int64_
 i8ql_status w8a8_gemm_noalloc(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                               const i8ql_bf16* bias, i8ql_bf16* y, int32_t* acc_debug,
                               int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * Reports how w8a8_fp8_gemm would run a problem of this size on the current
+ * device, without launching anything.
+ *
+ * No counterpart on the pages: a query for tests and profiling.  *tile_n is
+ * the width (N side) of the output tiles (128 or 256), *split_k the number
+ * of CTAs of a thread-block cluster that share one tile's k range (1: no
+ * split; each CTA then walks tiles persistently), *cta_pair 1 when pairs of
+ * CTAs on two SMs share 256-row tiles through one two-SM MMA.  Same argument
+ * rules as w8a8_fp8_gemm; the outputs are HOST pointers.
+ */
+i8ql_status i8ql_fp8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k, int32_t* cta_pair);
 
 /*
  * Reports how w8a8_gemm would run a problem of this size on the current

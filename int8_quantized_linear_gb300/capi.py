@@ -40,6 +40,7 @@ SIGNATURES = {
     "w8a16_gemm": (_S, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "grouped_w8a16_gemm": (_S, [_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _P]),
     "i8ql_w8a8_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
+    "i8ql_fp8_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
     "i8ql_w8a8_noalloc_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
     "i8ql_get_device_error": (_S, [_P]),
     "i8ql_status_string": (ctypes.c_char_p, [_S]),
@@ -265,6 +266,12 @@ def i8ql_w8a8_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
     2 pairs with stream-K) w8a8_gemm uses for an M x N x K problem on the
     current device; (0, 0, 0) in the decode range (M <= 64)."""
     return _plan("i8ql_w8a8_plan", m, n, k)
+
+
+def i8ql_fp8_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
+    """(tile width, split-K factor, CTA pairs 0/1) w8a8_fp8_gemm uses for an
+    M x N x K problem on the current device."""
+    return _plan("i8ql_fp8_plan", m, n, k)
 
 
 def i8ql_w8a8_noalloc_plan(m: int, n: int, k: int) -> tuple[int, int, int]:

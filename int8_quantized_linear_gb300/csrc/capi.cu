@@ -466,6 +466,23 @@ i8ql_status i8ql_w8a8_noalloc_plan(int64_t M, int64_t N, int64_t K, int32_t* til
     return plan_query(M, N, K, false, tile_n, split_k, cta_pair);
 }
 
+i8ql_status i8ql_fp8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k, int32_t* cta_pair) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    if (tile_n == nullptr || split_k == nullptr || cta_pair == nullptr) return I8QL_ERR_INVALID_ARG;
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(nullptr, &env, &s)) return s;
+    int bn = 0, split = 0, pair = 0;
+    I8QL_TRY(from_cuda(fp8_plan(M, N, K, env.sm_count, &bn, &split, &pair)));
+    *tile_n = bn;
+    *split_k = split;
+    *cta_pair = pair;
+    return I8QL_OK;
+}
+
 const char* i8ql_status_string(i8ql_status status) {
     switch (status) {
         case I8QL_OK: return "ok";

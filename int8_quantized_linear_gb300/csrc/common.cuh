@@ -171,6 +171,8 @@ cudaError_t launch_w8a8(const int8_t* qx, const float* sx, const int8_t* qw, con
 // and the linear layer from bf16 activations (quantization, then the GEMM).
 cudaError_t launch_quant_rows_fp8(const uint16_t* src, int64_t rows, int64_t K, uint8_t* q, float* s,
                                   const LaunchEnv& env);
+// The plan launch_fp8_gemm would run (tile width, split-K, CTA pairs).
+cudaError_t fp8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k, int* pair);
 cudaError_t launch_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
                             const uint16_t* bias, uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env);
 // W4A16 with bf16 group-128 scales: the quantization of bf16 weights to

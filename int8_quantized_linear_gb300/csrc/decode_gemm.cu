@@ -34,9 +34,14 @@
 //    disjoint k-ranges of the same rows; the four warps of a CTA are reduced
 //    in shared memory, then the cluster through distributed shared memory, in
 //    a fixed rank order (deterministic; exact for the int32 W8A8 sums).
-//  * Grouped: blockIdx.z is the expert; an expert without rows exits before
-//    reading any weight.  Offsets are validated on the device; a bad expert
-//    is skipped and reported through the sticky fault word.
+//  * Grouped: blockIdx.z walks the experts from the last one down (the
+//    hardware dispatches z in increasing order), so the experts at the end
+//    of the list -- the shared experts of an MoE layer, which see every
+//    token and loop over the most token chunks -- start first instead of
+//    forming the grid's tail (DeepSeek-MoE T = 64: gate_up 114.6 -> 89.8 us,
+//    down 73.0 -> 52.0 us).  An expert without rows exits before reading any
+//    weight.  Offsets are validated on the device; a bad expert is skipped
+//    and reported through the sticky fault word.
 // HBM traffic per launch: N*K weight bytes + 4N scale bytes (per active
 // expert) + token and output bytes.
 
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
     const int8_t* qw = p.qw;
     const float* sw = p.sw;
     if constexpr (GROUPED) {
-        const int64_t e = blockIdx.z;
+        const int64_t e = p.E - 1 - (int64_t)blockIdx.z;  // last expert first
         const int64_t a = p.offsets[e], b = p.offsets[e + 1];
         const bool bad = a < 0 || b < a || b > p.rows || (e == 0 && a != 0) || (e == p.E - 1 && b != p.rows);
         if (bad) {

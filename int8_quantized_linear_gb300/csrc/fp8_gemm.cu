@@ -33,6 +33,11 @@
 // BN weight rows, so each SM pulls a quarter less from L2 per k-block; the
 // copies of both complete on the leader's barrier, the leader issues the
 // MMAs and its commits reach both CTAs.
+// With few tiles (small M or N) single CTAs split K instead: a cluster of S
+// CTAs shares one tile, CTA r running k-blocks [nkb*r/S, nkb*(r+1)/S); each
+// parks its fp32 partial tile in its idle stage memory, and after a cluster
+// barrier CTA r reduces rows [128r/S, 128(r+1)/S) over all partials through
+// distributed shared memory, in rank order, and writes them.
 // Every mbarrier wait is bounded (1 s); on expiry the CTA records
 // I8QL_ERR_TIMEOUT, all roles leave, the MMA issuer waits (bounded) for its
 // MMAs, a 50 us pause lets bulk copies in flight land, and TMEM is freed.
@@ -71,6 +76,7 @@ struct Fp8Params {
     int64_t tiles_a, tiles_b;  // token tiles (128 or 256 rows) x BN-wide weight tiles
     uint32_t tmem_cols;
     int tma_store;             // outputs leave through TMA tensor stores (N % 8 == 0)
+    int split;                 // split-K CTAs per tile (a cluster; single CTAs only)
     unsigned* err;
 };
 
@@ -108,6 +114,9 @@ struct F8Cfg {
     static constexpr int kCtlOff = kOutOff + kF8OutBytes;      // barriers and flags after it
     static constexpr int kSmemBytes = kCtlOff + kF8CtlBytes + 1024;
     static_assert(kStages >= 3, "ring depth");
+    // split-K: the fp32 partial tile parks in the idle stage memory
+    static constexpr int kPartStride = BN + 4;  // floats per partial row (padding against bank conflicts)
+    static_assert(PAIR || kBM * kPartStride * 4 <= kStages * kStage, "split-K partial tile must fit the stages");
     static_assert(kAStage % 1024 == 0 && kBStage % 1024 == 0, "stages keep 1024-byte alignment");
 };
 
@@ -218,8 +227,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const int64_t tiles = p.tiles_a * p.tiles_b;
     const int prank = PAIR ? (int)cluster_rank() : 0;  // half of the pair this CTA holds
     const bool leader = prank == 0;
-    const int64_t unit0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
-    const int64_t unit_step = PAIR ? gridDim.x / 2 : gridDim.x;
+    // split-K (single CTAs): this CTA's k-blocks of its cluster's tile
+    const int ksplit = PAIR ? 1 : p.split;
+    const int krank = ksplit > 1 ? (int)cluster_rank() : 0;
+    const int kb_lo = (int)((int64_t)nkb * krank / ksplit), kb_hi = (int)((int64_t)nkb * (krank + 1) / ksplit);
+    const int csize = PAIR ? 2 : ksplit;
+    const int64_t unit0 = blockIdx.x / csize;
+    const int64_t unit_step = gridDim.x / csize;
     int* abort = &ctl->abort_flag;
     auto leader_addr = [&](uint64_t* bar) -> uint32_t { return PAIR ? mapa(smem_u32(bar), 0) : smem_u32(bar); };
 
@@ -275,7 +289,22 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const int64_t m = m0 + lane;
             const float sxm = m < p.M ? __ldg(p.sx + m) : 0.0f;
             const int64_t n_half = tb * BN + half * kHalf;
-            if (p.tma_store) {
+            if (ksplit > 1) {
+                // park this warp's 32 rows x kHalf columns of the fp32
+                // partial in the stage memory (every MMA of the tile, and so
+                // every read of the stages, has completed)
+                float* prow = reinterpret_cast<float*>(smem) + row * Cfg::kPartStride + half * kHalf;
+#pragma unroll 4
+                for (int c = 0; c < kHalf; c += 8) {
+                    uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    if (kb_hi > kb_lo) {
+                        tmem_ld8(lane_base + (uint32_t)(b * BN + half * kHalf + c), r);
+                        tmem_wait_ld();
+                    }
+                    *reinterpret_cast<uint4*>(prow + c) = make_uint4(r[0], r[1], r[2], r[3]);
+                    *reinterpret_cast<uint4*>(prow + c + 4) = make_uint4(r[4], r[5], r[6], r[7]);
+                }
+            } else if (p.tma_store) {
                 // 32 columns at a time: stage the warp's 32 x 32 box, then
                 // one thread stores it; the buffer used two boxes earlier is
                 // free once that store has read it
@@ -329,7 +358,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 f8_tile_coords(p, tile, ta, tb);
                 const int32_t xrow = (int32_t)(ta * Cfg::kTileM + prank * kBM);
                 const int32_t wrow = (int32_t)(tb * BN + prank * Cfg::kWRows);
-                for (int kb = 0; kb < nkb; ++kb, ++kg) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb, ++kg) {
                     const int s = (int)(kg % S);
                     if (!mbar_wait(&ctl->empty[s], (uint32_t)(((kg / S) & 1) ^ 1), abort, p.err)) {
                         alive = false;
@@ -369,7 +398,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 if (!mbar_wait(&ctl->acc_empty[b], (uint32_t)(((lt >> 1) & 1) ^ 1), abort, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * BN);
-                for (int kb = 0; kb < nkb; ++kb, ++kg) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb, ++kg) {
                     const int s = (int)(kg % S);
                     if (!mbar_wait(&ctl->full[s], (uint32_t)((kg / S) & 1), abort, p.err)) {
                         alive = false;
@@ -382,7 +411,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     for (int kk = 0; kk < kF8BK / 32; ++kk) {
                         const uint64_t ad = sw128_desc(a_st + kk * 32);
                         const uint64_t bd = sw128_desc(b_st + kk * 32);
-                        const uint32_t acc = (kb != 0 || kk != 0) ? 1u : 0u;
+                        const uint32_t acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
                         if constexpr (PAIR)
                             mma_f8_pair(d, ad, bd, idesc, acc);
                         else
@@ -427,6 +456,47 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tc_fence_after();
         if (warp == kF8MmaWarp) tmem_dealloc_pair(tmem, p.tmem_cols);
         return;
+    }
+    if (ksplit > 1) {
+        // Split-K: reduce this CTA's rows of the tile over the cluster's
+        // partials (rank order: deterministic), apply the epilogue, store.
+        cluster_sync_all();  // every partial is parked
+        if (unit0 < tiles) {
+            int64_t ta, tb;
+            f8_tile_coords(p, unit0, ta, tb);
+            const int r_lo = kBM * krank / ksplit, r_hi = kBM * (krank + 1) / ksplit;
+            constexpr int kC8 = BN / 8;
+            for (int i = threadIdx.x; i < (r_hi - r_lo) * kC8; i += kF8Threads) {
+                const int row = r_lo + i / kC8, c = (i % kC8) * 8;
+                const int64_t m = ta * kBM + row, n0 = tb * BN + c;
+                if (m >= p.M || n0 >= p.N) continue;
+                const uint32_t off = base + (uint32_t)((row * Cfg::kPartStride + c) * 4);
+                float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int q = 0; q < ksplit; ++q) {
+                    const int4 v0 = ld_dsmem_v4(off, (uint32_t)q), v1 = ld_dsmem_v4(off + 16, (uint32_t)q);
+                    a[0] += __int_as_float(v0.x);
+                    a[1] += __int_as_float(v0.y);
+                    a[2] += __int_as_float(v0.z);
+                    a[3] += __int_as_float(v0.w);
+                    a[4] += __int_as_float(v1.x);
+                    a[5] += __int_as_float(v1.y);
+                    a[6] += __int_as_float(v1.z);
+                    a[7] += __int_as_float(v1.w);
+                }
+                uint32_t r[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = __float_as_uint(a[j]);
+                const float sxm = __ldg(p.sx + m);
+                if (p.tma_store) {  // rows start on 16-byte boundaries
+                    uint32_t w[4];
+                    f8_epi8(p, n0, sxm, r, w);
+                    *reinterpret_cast<uint4*>(p.y + m * p.N + n0) = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+                    f8_store8(p, m, n0, sxm, r);
+                }
+            }
+        }
+        cluster_sync_all();  // no partial is released while another CTA reads it
     }
     if (warp == kF8MmaWarp) tmem_dealloc(tmem, p.tmem_cols);
 }
@@ -475,7 +545,7 @@ cudaError_t prepare_fp8(int dev) {
 
 template <int BN, bool PAIR>
 cudaError_t launch_bn(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw, const uint16_t* bias,
-                      uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env) {
+                      uint16_t* y, int64_t M, int64_t N, int64_t K, int split, const LaunchEnv& env) {
     using Cfg = F8Cfg<BN, PAIR>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -492,6 +562,7 @@ cudaError_t launch_bn(const uint8_t* qx, const float* sx, const uint8_t* qw, con
     p.tiles_a = (M + Cfg::kTileM - 1) / Cfg::kTileM;
     p.tiles_b = (N + BN - 1) / BN;
     p.tmem_cols = 2 * BN;  // two fp32 accumulator buffers (256 or 512 columns)
+    p.split = PAIR ? 1 : split;
     p.err = env.err;
     CUtensorMap map_x, map_w, map_y = {};
     if (!make_map_fp8(&map_x, qx, M, K, kBM) || !make_map_fp8(&map_w, qw, N, K, Cfg::kWRows))
@@ -499,22 +570,117 @@ cudaError_t launch_bn(const uint8_t* qx, const float* sx, const uint8_t* qw, con
     // rows of y start on 16-byte boundaries only when N % 8 == 0
     p.tma_store = (N % 8) == 0 ? 1 : 0;
     if (p.tma_store && !make_map_out(&map_y, y, M, N)) return cudaErrorInvalidValue;
-    const int64_t units = std::min<int64_t>(p.tiles_a * p.tiles_b, PAIR ? env.sm_count / 2 : env.sm_count);
+    const int64_t tiles = p.tiles_a * p.tiles_b;
+    if (p.split > 1) {
+        // one tile per cluster of `split` CTAs (the planner keeps them to one wave)
+        return launch_kernel(fp8_gemm_kernel<BN, PAIR>, dim3((unsigned)(tiles * p.split)), dim3(kF8Threads),
+                             Cfg::kSmemBytes, env.stream, dim3((unsigned)p.split, 1, 1), map_x, map_w, map_y, p);
+    }
+    const int64_t units = std::min<int64_t>(tiles, PAIR ? env.sm_count / 2 : env.sm_count);
     const int64_t grid = PAIR ? 2 * units : units;
     return launch_kernel(fp8_gemm_kernel<BN, PAIR>, dim3((unsigned)grid), dim3(kF8Threads), Cfg::kSmemBytes,
                          env.stream, PAIR ? dim3(2, 1, 1) : kNoCluster, map_x, map_w, map_y, p);
+}
+
+// Clusters of `csize` CTAs of the single-CTA kernel that fit on the GPU at
+// once (one CTA per SM; clusters do not span GPCs).
+template <int BN>
+int f8_active_clusters(int dev, int csize) {
+    static std::mutex mu;
+    static int cache[64][kMaxSplit + 1] = {};
+    if (dev < 0 || dev >= 64 || csize < 1 || csize > kMaxSplit) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int& slot = cache[dev][csize];
+    if (slot == 0) {
+        if (prepare_fp8<BN, false>(dev) != cudaSuccess) return 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)csize);
+        cfg.blockDim = dim3(kF8Threads);
+        cfg.dynamicSmemBytes = F8Cfg<BN, false>::kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)csize;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<BN, false>, &cfg) != cudaSuccess) n = 0;
+        slot = n > 0 ? n : -1;
+    }
+    return slot > 0 ? slot : 0;
+}
+
+struct F8Plan {
+    int bn;
+    bool pair;
+    int split;
+};
+
+// Tile width, CTA pairs, and split-K.  A k-block of a 128 x BN tile costs
+// BN + 64 (MMA and weight bytes, plus the token tile); a persistent launch
+// costs its waves of tiles times the k-blocks of a tile, a split launch the
+// k-blocks of one CTA plus a fixed allowance for the cluster reduction (one
+// wave of clusters, each within the GPU's cluster occupancy).  Pairs (M >
+// 128) measured no faster per SM than single CTAs, and win ties.
+F8Plan plan_fp8(int dev, int64_t M, int64_t N, int64_t K, int sms) {
+    const int64_t nkb = (K + kF8BK - 1) / kF8BK;
+    F8Plan best{N > 128 ? 256 : 128, false, 1};
+    double best_cost = 1e300;
+    auto waves = [](int64_t units, int64_t slots) { return (double)((units + slots - 1) / slots); };
+    if (M > kBM && N > 128) {
+        const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + 255) / 256);
+        best_cost = waves(tiles, sms / 2) * (double)nkb * (256 + 64);
+        best = F8Plan{256, true, 1};
+    }
+    for (int bn : {256, 128}) {
+        if (bn == 256 && N <= 128) continue;
+        const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+        const double per_kb = bn + 64.0;
+        double cost = waves(tiles, sms) * (double)nkb * per_kb;
+        int split = 1;
+        if (tiles < sms) {
+            for (int s = 2; s <= kMaxSplit && 2 * s <= nkb; ++s) {
+                if (tiles * s > sms) break;
+                const int fit = bn == 256 ? f8_active_clusters<256>(dev, s) : f8_active_clusters<128>(dev, s);
+                if (tiles > fit) continue;
+                const double c = ((double)((nkb + s - 1) / s) + 6.0) * per_kb;
+                if (c < cost) {
+                    cost = c;
+                    split = s;
+                }
+            }
+        }
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = F8Plan{bn, false, split};
+        }
+    }
+    return best;
 }
 
 }  // namespace
 
 cudaError_t launch_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
                             const uint16_t* bias, uint16_t* y, int64_t M, int64_t N, int64_t K, const LaunchEnv& env) {
-    // 256-wide weight tiles unless N is small; CTA pairs (256 token rows per
-    // tile, each SM loading half of the weight tile) when M spans more than
-    // one 128-row tile
-    if (M > kBM && N > 128) return launch_bn<256, true>(qx, sx, qw, sw, bias, y, M, N, K, env);
-    if (N > 128) return launch_bn<256, false>(qx, sx, qw, sw, bias, y, M, N, K, env);
-    return launch_bn<128, false>(qx, sx, qw, sw, bias, y, M, N, K, env);
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const F8Plan plan = plan_fp8(dev, M, N, K, env.sm_count);
+    if (plan.pair) return launch_bn<256, true>(qx, sx, qw, sw, bias, y, M, N, K, 1, env);
+    if (plan.bn == 256) return launch_bn<256, false>(qx, sx, qw, sw, bias, y, M, N, K, plan.split, env);
+    return launch_bn<128, false>(qx, sx, qw, sw, bias, y, M, N, K, plan.split, env);
+}
+
+cudaError_t fp8_plan(int64_t M, int64_t N, int64_t K, int sms, int* tile_n, int* split_k, int* pair) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const F8Plan plan = plan_fp8(dev, M, N, K, sms);
+    *tile_n = plan.bn;
+    *split_k = plan.split;
+    *pair = plan.pair ? 1 : 0;
+    return cudaSuccess;
 }
 
 cudaError_t launch_fp8_linear(const uint16_t* x, const uint8_t* qw, const float* sw, const uint16_t* bias,

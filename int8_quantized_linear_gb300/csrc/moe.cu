@@ -15,13 +15,15 @@
 //   combine: out[t,:] = bf16(sum_s w[t,s] * yd[token_row[t,s], :]), slots in
 //     order, fp32.
 //
-// The routing runs in one CTA: every warp takes tokens in turn (softmax and
-// top-k by warp reductions, ties to the lower index), marks each chosen
+// Routing is two kernels.  The selection spreads the tokens over the GPU,
+// one warp per token (softmax denominator and top-k by warp reductions, ties
+// to the lower index).  The grouping runs in one CTA: it marks each chosen
 // (expert, token) in a per-expert token bitmap in shared memory, and then
 // every (token, slot) finds its row as the expert's offset plus the number
 // of earlier tokens in the expert's bitmap.  The grouping is therefore
-// deterministic and identical to the definition, with no atomics on
-// global memory.
+// deterministic and identical to the definition, with no atomics on global
+// memory.  (One CTA doing both measured 19.7 us at T = 64, issue-bound on
+// its one SM.)
 
 #include <cuda_runtime.h>
 
@@ -33,6 +35,7 @@ namespace i8ql {
 namespace {
 
 constexpr int kRouteThreads = 1024;
+constexpr int kSelectThreads = 256;
 constexpr int kMaxLogitsPerLane = 8;  // E <= 256
 
 struct RouteParams {
@@ -44,27 +47,24 @@ struct RouteParams {
     float* slot_weight;  // [T, topk + shared]
 };
 
-__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const RouteParams p) {
-    extern __shared__ uint32_t route_smem[];
-    const int64_t W = (p.T + 31) / 32;               // bitmap words per expert
-    uint32_t* bits = route_smem;                      // [E][W]
-    uint32_t* before = route_smem + p.E * W;          // [E][W] set bits in earlier words
-    __shared__ int32_t offs[257 + 64];
+// Selection, one warp per token (tokens spread over the whole GPU): the
+// softmax denominator and the top_k largest logits by repeated warp argmax
+// (equal logits: the lower index).  Writes each routed slot's expert id into
+// token_row (the grouping kernel turns it into a row) and its weight, and
+// weight 1 for the shared slots.
+__global__ void __launch_bounds__(kSelectThreads) moe_select_kernel(const RouteParams p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t S = p.topk + p.shared;
+    const int E = (int)p.E, topk = (int)p.topk, S = (int)(p.topk + p.shared);
     pdl_wait();
-    for (int64_t i = threadIdx.x; i < p.E * W; i += kRouteThreads) bits[i] = 0u;
-    __syncthreads();
-
-    // ---- softmax and top-k, one token per warp at a time
-    for (int64_t t = warp; t < p.T; t += kRouteThreads / 32) {
+    for (int t = blockIdx.x * (kSelectThreads / 32) + warp; t < (int)p.T; t += gridDim.x * (kSelectThreads / 32)) {
+        const float* lt = p.logits + (int64_t)t * E;
         float l[kMaxLogitsPerLane];
         float mx = -INFINITY;
 #pragma unroll
         for (int i = 0; i < kMaxLogitsPerLane; ++i) {
-            const int64_t e = lane + 32 * i;
-            l[i] = e < p.E ? p.logits[t * p.E + e] : -INFINITY;
+            const int e = lane + 32 * i;
+            l[i] = e < E ? __ldg(lt + e) : -INFINITY;
             mx = fmaxf(mx, l[i]);
         }
 #pragma unroll
@@ -72,18 +72,18 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const RoutePar
         float sum = 0.0f;
 #pragma unroll
         for (int i = 0; i < kMaxLogitsPerLane; ++i)
-            if (lane + 32 * i < p.E) sum += expf(l[i] - mx);
+            if (lane + 32 * i < E) sum += expf(l[i] - mx);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         unsigned taken = 0u;  // this lane's chosen logits
-        for (int64_t s = 0; s < p.topk; ++s) {
+        for (int s = 0; s < topk; ++s) {
             // the lane's best untaken logit, lowest index first among equals
             float bv = -INFINITY;
             int bi = 0x7fffffff;
 #pragma unroll
             for (int i = 0; i < kMaxLogitsPerLane; ++i) {
                 const int e = lane + 32 * i;
-                if (e < p.E && !(taken >> i & 1u) && (l[i] > bv || bi == 0x7fffffff)) {
+                if (e < E && !(taken >> i & 1u) && (l[i] > bv || bi == 0x7fffffff)) {
                     bv = l[i];
                     bi = e;
                 }
@@ -98,56 +98,97 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const RoutePar
                 }
             }
             if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-            if (lane == 0) {
-                p.token_row[t * S + s] = bi;
-                p.slot_weight[t * S + s] = expf(bv - mx) / sum;
-                atomicOr(&bits[bi * W + (t >> 5)], 1u << (t & 31));
+            if (lane == (s & 31)) {  // slot s is written by one lane (top_k may exceed 32)
+                p.token_row[(int64_t)t * S + s] = bi;
+                p.slot_weight[(int64_t)t * S + s] = expf(bv - mx) / sum;
             }
         }
+        for (int s = topk + lane; s < S; s += 32) p.slot_weight[(int64_t)t * S + s] = 1.0f;
+    }
+}
+
+// Grouping, one CTA: each (token, routed slot) marks its expert's token
+// bitmap in shared memory; per-expert counts give the offsets (a warp scan),
+// and every (token, slot) finds its row as the expert's offset plus the
+// number of earlier tokens in the expert's bitmap -- deterministic, with no
+// atomics on global memory.
+__global__ void __launch_bounds__(kRouteThreads) moe_group_kernel(const RouteParams p) {
+    extern __shared__ uint32_t route_smem[];
+    const int T = (int)p.T, E = (int)p.E, topk = (int)p.topk, shared = (int)p.shared;
+    const int S = topk + shared;
+    const int W = (T + 31) / 32;               // bitmap words per expert
+    uint32_t* bits = route_smem;               // [E][W]
+    uint32_t* before = route_smem + E * W;     // [E][W] set bits in earlier words
+    __shared__ int32_t offs[257 + 64];
+    pdl_wait();
+    for (int i = threadIdx.x; i < E * W; i += kRouteThreads) bits[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * topk; i += kRouteThreads) {
+        const int t = i / topk, s = i - t * topk;
+        const int e = p.token_row[(int64_t)t * S + s];
+        atomicOr(&bits[e * W + (t >> 5)], 1u << (t & 31));
     }
     __syncthreads();
 
-    // ---- per-expert counts, running counts of earlier words, offsets
-    for (int64_t e = threadIdx.x; e < p.E; e += kRouteThreads) {
+    // ---- per-expert counts and running counts of earlier words
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) {
         uint32_t run = 0;
-        for (int64_t w = 0; w < W; ++w) {
+        for (int w = 0; w < W; ++w) {
             before[e * W + w] = run;
             run += __popc(bits[e * W + w]);
         }
         offs[e] = (int32_t)run;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t acc = 0;
-        for (int64_t e = 0; e < p.E + p.shared; ++e) {
-            const int32_t c = e < p.E ? offs[e] : (int32_t)p.T;
+    if (threadIdx.x < 32) {
+        // offsets: exclusive scan of the counts (routed, then shared: T each),
+        // each lane summing a run of consecutive experts
+        const int lane = threadIdx.x;
+        const int n = E + shared;
+        const int per = (n + 31) / 32;
+        const int lo = min(n, lane * per), hi = min(n, lo + per);
+        int32_t local = 0;
+        for (int e = lo; e < hi; ++e) local += e < E ? offs[e] : T;
+        int32_t incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int32_t acc = incl - local;
+        __syncwarp();
+        for (int e = lo; e < hi; ++e) {
+            const int32_t c = e < E ? offs[e] : T;
             offs[e] = acc;
             p.offsets[e] = acc;
             acc += c;
         }
-        offs[p.E + p.shared] = acc;
-        p.offsets[p.E + p.shared] = acc;
+        if (lane == 31) {
+            offs[n] = incl;
+            p.offsets[n] = incl;
+        }
     }
     __syncthreads();
 
     // ---- rows of every (token, slot)
-    for (int64_t i = threadIdx.x; i < p.T * S; i += kRouteThreads) {
-        const int64_t t = i / S, s = i % S;
-        int64_t row;
-        if (s < p.topk) {
-            const int64_t e = p.token_row[i];
+    for (int i = threadIdx.x; i < T * S; i += kRouteThreads) {
+        const int t = i / S, s = i - t * S;
+        int row;
+        if (s < topk) {
+            const int e = p.token_row[i];
             const uint32_t mask = (1u << (t & 31)) - 1u;
-            row = offs[e] + before[e * W + (t >> 5)] + __popc(bits[e * W + (t >> 5)] & mask);
+            row = offs[e] + (int)before[e * W + (t >> 5)] + __popc(bits[e * W + (t >> 5)] & mask);
         } else {
-            row = offs[p.E + (s - p.topk)] + t;
-            p.slot_weight[i] = 1.0f;
+            row = offs[E + (s - topk)] + t;
         }
-        p.token_row[i] = (int32_t)row;
-        p.row_token[row] = (int32_t)t;
+        p.token_row[i] = row;
+        p.row_token[row] = t;
     }
 }
 
 // out[t, :] for 8 columns per thread: the slots' rows weighted in order.
+// The slot rows and weights, then the slots' output vectors, are loaded in
+// batches of 8 ahead of the arithmetic, so the gathers overlap.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint16_t* __restrict__ yd,
                                                           const int32_t* __restrict__ token_row,
                                                           const float* __restrict__ slot_weight,
@@ -157,15 +198,28 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint16_t* __rest
     const int64_t c = ((int64_t)blockIdx.x * 256 + threadIdx.x) * 8;
     if (c >= H) return;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int64_t s = 0; s < S; ++s) {
-        const int64_t row = token_row[t * S + s];
-        const float w = slot_weight[t * S + s];
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(yd + row * H + c));
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    for (int64_t s0 = 0; s0 < S; s0 += 8) {
+        int32_t row[8];
+        float w[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            acc[2 * j] = fmaf(w, __uint_as_float(words[j] << 16), acc[2 * j]);
-            acc[2 * j + 1] = fmaf(w, __uint_as_float(words[j] & 0xffff0000u), acc[2 * j + 1]);
+        for (int j = 0; j < 8; ++j) {
+            const bool ok = s0 + j < S;
+            row[j] = ok ? __ldg(token_row + t * S + s0 + j) : 0;
+            w[j] = ok ? __ldg(slot_weight + t * S + s0 + j) : 0.0f;
+        }
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = s0 + j < S ? __ldg(reinterpret_cast<const uint4*>(yd + (int64_t)row[j] * H + c)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (s0 + j >= S) break;
+            const uint32_t words[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[2 * q] = fmaf(w[j], __uint_as_float(words[q] << 16), acc[2 * q]);
+                acc[2 * q + 1] = fmaf(w[j], __uint_as_float(words[q] & 0xffff0000u), acc[2 * q + 1]);
+            }
         }
     }
     uint32_t o[4];
@@ -196,13 +250,18 @@ cudaError_t launch_moe_route(const float* logits, int64_t T, int64_t E, int64_t 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && !opted[dev]) {
-        if ((e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
+        if ((e = cudaFuncSetAttribute(moe_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
             cudaSuccess)
             return e;
         opted[dev] = true;
     }
     RouteParams p{logits, T, E, topk, shared, offsets, row_token, token_row, slot_weight};
-    return launch_kernel(moe_route_kernel, dim3(1), dim3(kRouteThreads), smem, env.stream, kNoCluster, p);
+    if (T > 0) {
+        const int64_t blocks = std::min<int64_t>((T + kSelectThreads / 32 - 1) / (kSelectThreads / 32), 4 * env.sm_count);
+        e = launch_kernel(moe_select_kernel, dim3((unsigned)blocks), dim3(kSelectThreads), 0, env.stream, kNoCluster, p);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_kernel(moe_group_kernel, dim3(1), dim3(kRouteThreads), smem, env.stream, kNoCluster, p);
 }
 
 cudaError_t launch_moe_combine(const uint16_t* yd, const int32_t* token_row, const float* slot_weight, uint16_t* out,

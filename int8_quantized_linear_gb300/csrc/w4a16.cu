@@ -35,6 +35,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "quant_math.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -51,43 +52,75 @@ __device__ __forceinline__ uint16_t bf16r(float f) { return __bfloat16_as_ushort
 
 // ------------------------------------------------------------------ quantization
 
-// 16 threads own one group of 128 weights (8 per thread, one 16-byte vector).
-__global__ void __launch_bounds__(256) quant_w4_kernel(const uint16_t* __restrict__ w, int64_t groups, int64_t K,
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+
+// Four threads own one group of 128 weights (32 per thread: four 16-byte
+// vectors, all loaded before any arithmetic so that 64 bytes per thread are
+// in flight).  The codes are the int8 quantization's arithmetic with the
+// stored bf16 scale as divisor (codes8: rint of the quotient through the
+// correctly rounded reciprocal, with the IEEE division near half-integers).
+// Its fast-path argument holds here a fortiori: s = bf16(fl32(a / 7)) is at
+// least (a / 7)(1 - 2^-24)(1 - 2^-9), so |w / s| <= 7.014 and rint never
+// leaves [-7, 7].  A scale that is subnormal in bf16 (a group whose absmax is
+// below 7 * 2^-126) loses that bound, so such a group takes the IEEE division
+// with the clamp, element by element.
+__device__ __forceinline__ uint32_t nibbles8(uint2 b) {
+    // bytes c0..c7 (two's complement) -> c0 | c1 << 4 | ... | c7 << 28
+    uint32_t lo = b.x & 0x0f0f0f0fu, hi = b.y & 0x0f0f0f0fu;
+    lo |= lo >> 4;
+    hi |= hi >> 4;
+    return __byte_perm(lo, hi, 0x6420);
+}
+
+__global__ void __launch_bounds__(256) quant_w4_kernel(const uint16_t* __restrict__ w, int64_t groups,
                                                         uint8_t* __restrict__ packed, uint16_t* __restrict__ scale) {
     pdl_wait();
-    const int64_t gidx = ((int64_t)blockIdx.x * 256 + threadIdx.x) / 16;
-    const int sub = threadIdx.x & 15;
+    const int64_t gidx = ((int64_t)blockIdx.x * 256 + threadIdx.x) / 4;
+    const int sub = threadIdx.x & 3;
     const bool valid = gidx < groups;
-    const int64_t gpr = K / kGroup;  // groups per row
-    const int64_t row = valid ? gidx / gpr : 0, g = valid ? gidx % gpr : 0;
-    const int64_t k0 = g * kGroup + sub * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (valid) v = __ldg(reinterpret_cast<const uint4*>(w + row * K + k0));
-    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-    float x[8];
+    // the matrix is contiguous and K % 128 == 0: group g covers elements
+    // [128 g, 128 g + 128), its codes bytes [64 g, 64 g + 64)
+    const uint4* src = reinterpret_cast<const uint4*>(w + gidx * kGroup + sub * 32);
+    uint4 v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(words[i] << 16);
-        x[2 * i + 1] = __uint_as_float(words[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < 4; ++i) v[i] = valid ? ldg_stream16(src + i) : make_uint4(0, 0, 0, 0);
     float a = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    for (int i = 0; i < 4; ++i) a = absmax8(v[i], a);
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
     if (!valid) return;
     // the stored scale is bf16; the codes divide by it (zero group: 1)
     const uint16_t sb = a == 0.0f ? bf16r(1.0f) : bf16r(__fdiv_rn(a, 7.0f));
     const float s = bf16f(sb);
     if (sub == 0) scale[gidx] = sb;
-    uint32_t word = 0;
+    const RowScale rs = make_row_scale(s);
+    uint32_t word[4];
+    if ((sb & 0x7f80u) != 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int c = __float2int_rn(__fdiv_rn(x[i], s));
-        c = max(-7, min(7, c));
-        word |= (uint32_t)(c & 15) << (4 * i);
+        for (int i = 0; i < 4; ++i) word[i] = nibbles8(codes8(v[i], rs));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t vw[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t acc = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float x = (j & 1) ? hi_bf16(vw[j / 2]) : lo_bf16(vw[j / 2]);
+                const int c = max(-7, min(7, __float2int_rn(__fdiv_rn(x, s))));
+                acc |= (uint32_t)(c & 15) << (4 * j);
+            }
+            word[i] = acc;
+        }
     }
-    *reinterpret_cast<uint32_t*>(packed + row * (K / 2) + k0 / 2) = word;
+    *reinterpret_cast<uint4*>(packed + gidx * (kGroup / 2) + sub * 16) = make_uint4(word[0], word[1], word[2], word[3]);
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -100,14 +133,6 @@ struct W4Params {
     int64_t M, N, K;
     int one_wave;
 };
-
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // Eight codes of one 32-bit word (code i in bits 4i..4i+3) -> four bf16x2
 // words holding the code pairs (0, 4), (1, 5), (2, 6), (3, 7), exactly: the
@@ -375,8 +400,8 @@ cudaError_t w4_launch(W4Params p, const LaunchEnv& env) {
 cudaError_t launch_quant_w4(const uint16_t* w, int64_t N, int64_t K, uint8_t* packed, uint16_t* scale,
                             const LaunchEnv& env) {
     const int64_t groups = N * (K / kGroup);
-    const int64_t blocks = (groups * 16 + 255) / 256;
-    return launch_kernel(quant_w4_kernel, dim3((unsigned)blocks), dim3(256), 0, env.stream, kNoCluster, w, groups, K,
+    const int64_t blocks = (groups * 4 + 255) / 256;
+    return launch_kernel(quant_w4_kernel, dim3((unsigned)blocks), dim3(256), 0, env.stream, kNoCluster, w, groups,
                          packed, scale);
 }
 

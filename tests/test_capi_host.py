@@ -139,7 +139,7 @@ def test_valid_call_without_device_reports_no_device(lib):
     assert lib.w8a16_gemm(A, B, C, D, 4, 16, 64, None) == capi.I8QL_ERR_NO_DEVICE
 
 
-@pytest.mark.parametrize("fn", ["i8ql_w8a8_plan", "i8ql_w8a8_noalloc_plan"])
+@pytest.mark.parametrize("fn", ["i8ql_w8a8_plan", "i8ql_w8a8_noalloc_plan", "i8ql_fp8_plan"])
 def test_w8a8_plan_argument_errors(lib, fn):
     import ctypes
     a, b, c = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)

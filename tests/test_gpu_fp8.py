@@ -158,7 +158,8 @@ def test_fp8_gemm_small_integers_exact():
     ints = np.arange(1, 17, dtype=np.float32)
     codes = oracle.fp8_encode(ints)
     assert np.array_equal(oracle.fp8_decode(codes), ints)
-    for (m, n, k) in [(1, 16, 16), (7, 40, 48), (129, 300, 1040), (256, 256, 4096), (300, 513, 2064)]:
+    for (m, n, k) in [(1, 16, 16), (7, 40, 48), (129, 300, 1040), (256, 256, 4096), (300, 513, 2064),
+                      (64, 640, 4096), (128, 520, 9728)]:
         g = np.random.default_rng(m + n + k)
         qx = codes[g.integers(0, 16, (m, k))] | (g.integers(0, 2, (m, k)) * 0x80).astype(np.uint8)
         qw = codes[g.integers(0, 16, (n, k))] | (g.integers(0, 2, (n, k)) * 0x80).astype(np.uint8)
@@ -185,16 +186,33 @@ def test_fp8_gemm_shapes(m, n, k):
     check_gemm(qx, sx, qw, sw, bias)
 
 
+def test_fp8_plans_cover_split_k_tile_widths_and_pairs():
+    """The prefill shapes exercise every launch form: split-K clusters of
+    single CTAs at both tile widths (few tiles), persistent single CTAs, and
+    CTA pairs."""
+    plans = {capi.i8ql_fp8_plan(m, n, k) for m in (1, 64, 128, 512, 2048, 4096)
+             for n, k in synthetic.QWEN3_4B_SHAPES.values()}
+    assert any(s > 1 and t == 128 for t, s, _ in plans), plans
+    assert any(s > 1 and t == 256 for t, s, _ in plans), plans
+    assert any(s == 1 and p == 0 for _, s, p in plans), plans
+    assert any(p == 1 for _, _, p in plans), plans
+    assert all(s == 1 for _, s, p in plans if p == 1)
+    for m, n, k in [(1, 2560, 9728), (128, 2560, 2560), (128, 2560, 9728)]:
+        assert capi.i8ql_fp8_plan(m, n, k)[1] > 1, (m, n, k)
+
+
+@pytest.mark.parametrize("m", [128, 512, 2048])
 @pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
-def test_fp8_gemm_qwen3_4b_prefill_sampled(shape):
-    """Qwen3-4B prefill shapes at M = 2048 (outlier weights and activation
-    channels), bias on, sampled outputs against the exact oracle."""
+def test_fp8_gemm_qwen3_4b_prefill_sampled(shape, m):
+    """Qwen3-4B prefill shapes (outlier weights and activation channels),
+    bias on, sampled outputs against the exact oracle; M = 128 and 512 run
+    split-K clusters, M = 2048 CTA pairs."""
     n, k = synthetic.QWEN3_4B_SHAPES[shape]
     qw, sw = oracle.quant_rows_fp8(util.bits(synthetic.weight(n, k, 1)))
-    qx, sx = oracle.quant_rows_fp8(util.bits(synthetic.activations(2048, k, 2)))
+    qx, sx = oracle.quant_rows_fp8(util.bits(synthetic.activations(m, k, 2)))
     bias = util.bits(synthetic.bias(n, 3))
-    g = np.random.default_rng(n)
-    pm = np.concatenate([g.integers(0, 2048, 3000), [0, 2047]])
+    g = np.random.default_rng(n + m)
+    pm = np.concatenate([g.integers(0, m, 3000), [0, m - 1]])
     pn = np.concatenate([g.integers(0, n, 3000), [n - 1, 0]])
     check_gemm(qx, sx, qw, sw, bias, pm, pn)
 
