@@ -561,7 +561,8 @@ cudaError_t launch_bn(const uint8_t* qx, const float* sx, const uint8_t* qw, con
     p.K = K;
     p.tiles_a = (M + Cfg::kTileM - 1) / Cfg::kTileM;
     p.tiles_b = (N + BN - 1) / BN;
-    p.tmem_cols = 2 * BN;  // two fp32 accumulator buffers (256 or 512 columns)
+    // two fp32 accumulator buffers of BN columns (the allocation is a power of two)
+    p.tmem_cols = BN <= 128 ? 256u : 512u;
     p.split = PAIR ? 1 : split;
     p.err = env.err;
     CUtensorMap map_x, map_w, map_y = {};
@@ -617,7 +618,10 @@ struct F8Plan {
     int split;
 };
 
-// Tile width, CTA pairs, and split-K.  A k-block of a 128 x BN tile costs
+// Tile width, CTA pairs, and split-K.  Pair tiles are 256 x 256 or 256 x
+// 192 (the narrower one when its tiles fill the last wave of pairs better:
+// N = 2560 at M = 4096 is 160 wide tiles, 2.1 waves of 76 pairs, or 224
+// narrower ones, 2.9 waves).  A k-block of a 128 x BN tile costs
 // BN + 64 (MMA and weight bytes, plus the token tile); a persistent launch
 // costs its waves of tiles times the k-blocks of a tile, a split launch the
 // k-blocks of one CTA plus a fixed allowance for the cluster reduction (one
@@ -629,9 +633,15 @@ F8Plan plan_fp8(int dev, int64_t M, int64_t N, int64_t K, int sms) {
     double best_cost = 1e300;
     auto waves = [](int64_t units, int64_t slots) { return (double)((units + slots - 1) / slots); };
     if (M > kBM && N > 128) {
-        const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + 255) / 256);
-        best_cost = waves(tiles, sms / 2) * (double)nkb * (256 + 64);
-        best = F8Plan{256, true, 1};
+        // 192-wide pair tiles when they fill the last wave of pairs better
+        for (int bn : {256, 192}) {
+            const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + bn - 1) / bn);
+            const double cost = waves(tiles, sms / 2) * (double)nkb * (bn + 64);
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = F8Plan{bn, true, 1};
+            }
+        }
     }
     for (int bn : {256, 128}) {
         if (bn == 256 && N <= 128) continue;
@@ -667,6 +677,7 @@ cudaError_t launch_fp8_gemm(const uint8_t* qx, const float* sx, const uint8_t* q
     const cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const F8Plan plan = plan_fp8(dev, M, N, K, env.sm_count);
+    if (plan.pair && plan.bn == 192) return launch_bn<192, true>(qx, sx, qw, sw, bias, y, M, N, K, 1, env);
     if (plan.pair) return launch_bn<256, true>(qx, sx, qw, sw, bias, y, M, N, K, 1, env);
     if (plan.bn == 256) return launch_bn<256, false>(qx, sx, qw, sw, bias, y, M, N, K, plan.split, env);
     return launch_bn<128, false>(qx, sx, qw, sw, bias, y, M, N, K, plan.split, env);

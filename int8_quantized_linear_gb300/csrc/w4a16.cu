@@ -170,11 +170,12 @@ template <int MT>
 struct W4Regs {
     uint4 q[MT][2];      // rows g and g+8 of each 16-row m-tile: 32 codes each
     uint32_t s[MT];      // the two rows' group scales (bf16 bits, g low, g+8 high)
+    uint4 x[4];          // one token tile (NT == 1): the step's 32 token values
 };
 
 // MT 16-row m-tiles per warp, NT 8-token n-tiles per pass.
 template <int MT, int NT, int STAGES>
-__global__ void __launch_bounds__(kW4Threads, NT >= 4 ? 2 : 4) w4a16_kernel(const W4Params p) {
+__global__ void __launch_bounds__(kW4Threads, NT >= 4 ? 2 : (NT == 1 ? 3 : 4)) w4a16_kernel(const W4Params p) {
     constexpr int kRows = 16 * MT;
     constexpr int kToks = 8 * NT;
     __shared__ float part[kW4Warps][kToks * kRows];
@@ -244,6 +245,12 @@ __global__ void __launch_bounds__(kW4Threads, NT >= 4 ? 2 : 4) w4a16_kernel(cons
                 for (int h = 0; h < 2; ++h) w.q[mt][h] = ldg_stream16(qbase[mt][h] + (int64_t)i * (kGroup / 2));
                 w.s[mt] = (uint32_t)__ldg(sbase[mt][0] + i) | ((uint32_t)__ldg(sbase[mt][1] + i) << 16);
             }
+            if constexpr (NT == 1) {
+                // the token values travel in the ring too: their L1 latency
+                // then stays off the step's critical path
+#pragma unroll
+                for (int v = 0; v < 4; ++v) w.x[v] = __ldg(reinterpret_cast<const uint4*>(xbase[0] + (int64_t)i * kGroup) + v);
+            }
         };
         auto step = [&](const W4Regs<MT>& w, int i) {
             float part_acc[MT][NT][4];  // this k-step's group sums
@@ -260,7 +267,9 @@ __global__ void __launch_bounds__(kW4Threads, NT >= 4 ? 2 : 4) w4a16_kernel(cons
                 uint32_t xb[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    if (nt < nt_active) {
+                    if constexpr (NT == 1) {
+                        pair_tokens(w.x[v], xb[nt]);
+                    } else if (nt < nt_active) {
                         pair_tokens(__ldg(reinterpret_cast<const uint4*>(xbase[nt] + (int64_t)i * kGroup) + v), xb[nt]);
                     } else {
 #pragma unroll

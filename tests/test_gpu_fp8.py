@@ -189,13 +189,14 @@ def test_fp8_gemm_shapes(m, n, k):
 def test_fp8_plans_cover_split_k_tile_widths_and_pairs():
     """The prefill shapes exercise every launch form: split-K clusters of
     single CTAs at both tile widths (few tiles), persistent single CTAs, and
-    CTA pairs."""
+    CTA pairs with 256- and 192-wide tiles."""
     plans = {capi.i8ql_fp8_plan(m, n, k) for m in (1, 64, 128, 512, 2048, 4096)
              for n, k in synthetic.QWEN3_4B_SHAPES.values()}
     assert any(s > 1 and t == 128 for t, s, _ in plans), plans
     assert any(s > 1 and t == 256 for t, s, _ in plans), plans
     assert any(s == 1 and p == 0 for _, s, p in plans), plans
-    assert any(p == 1 for _, _, p in plans), plans
+    assert any(p == 1 and t == 256 for t, _, p in plans), plans
+    assert any(p == 1 and t == 192 for t, _, p in plans), plans
     assert all(s == 1 for _, s, p in plans if p == 1)
     for m, n, k in [(1, 2560, 9728), (128, 2560, 2560), (128, 2560, 9728)]:
         assert capi.i8ql_fp8_plan(m, n, k)[1] > 1, (m, n, k)
@@ -206,7 +207,7 @@ def test_fp8_plans_cover_split_k_tile_widths_and_pairs():
 def test_fp8_gemm_qwen3_4b_prefill_sampled(shape, m):
     """Qwen3-4B prefill shapes (outlier weights and activation channels),
     bias on, sampled outputs against the exact oracle; M = 128 and 512 run
-    split-K clusters, M = 2048 CTA pairs."""
+    split-K clusters, M = 2048 CTA pairs (192-wide tiles for N = 2560)."""
     n, k = synthetic.QWEN3_4B_SHAPES[shape]
     qw, sw = oracle.quant_rows_fp8(util.bits(synthetic.weight(n, k, 1)))
     qx, sx = oracle.quant_rows_fp8(util.bits(synthetic.activations(m, k, 2)))
