@@ -195,8 +195,12 @@ i8ql_status w8a16_gemm(const i8ql_bf16* x, const int8_t* qw, const float* sw, i8
  *   y[r,n] = bf16_rne(sw[e,n] * sum_k qw[e,n,k] * x[r,k]).
  * offsets: int32 [E + 1] in DEVICE memory, offsets[0] = 0, non-decreasing,
  * offsets[E] = T_total; the host never reads it.  An expert with no rows
- * reads none of its weights.  If the offsets break these rules the kernel
- * skips the bad experts and records I8QL_ERR_BAD_OFFSETS in the sticky word.
+ * reads none of its weights (with T_total <= E / 2 and E <= 256 its CTAs are
+ * not even launched: one expert slot per row, each finding its expert in
+ * the offsets).  If the offsets break these rules the kernel skips the bad
+ * experts (and, in the per-row slot form, any expert with rows beyond the
+ * first T_total found from the last) and records I8QL_ERR_BAD_OFFSETS in the
+ * sticky word.
  * qw int8 [E, N, K], sw fp32 [E, N], y bf16 [T_total, N].  E >= 1.
  */
 i8ql_status grouped_w8a16_gemm(const i8ql_bf16* x, const int32_t* offsets, int64_t E,

@@ -661,6 +661,54 @@ def test_grouped_dsmoe_sampled(dsmoe_experts, tokens, proj):
     assert util.rel_frobenius(np.concatenate(got), np.concatenate(want)) <= W8A16_FROB
 
 
+@pytest.mark.parametrize("placement", ["last", "first", "middle3", "spread4", "spread20", "bunched20"])
+def test_grouped_few_rows_compact_slots(placement):
+    """At most E/2 rows: the launch has one expert slot per row and each slot
+    finds its expert by scanning the offsets (experts without rows get no
+    CTAs); every placement of the rows gives the oracle's result."""
+    e_count, n, k = 40, 48, 96
+    counts = np.zeros(e_count, np.int64)
+    if placement == "last":
+        counts[-1] = 1
+    elif placement == "first":
+        counts[0] = 1
+    elif placement == "middle3":
+        counts[17] = 3
+    elif placement == "spread4":
+        counts[[0, 13, 39]] = [1, 1, 2]
+    elif placement == "spread20":
+        counts[::2] = 1
+    else:
+        counts[[3, 9, 21, 30, 38]] = 4
+    q, s = _experts(e_count, n, k, 90)
+    off = np.zeros(e_count + 1, np.int32)
+    off[1:] = np.cumsum(counts)
+    assert 2 * off[-1] <= e_count
+    x = synthetic.activations(int(off[-1]), k, 91)
+    y = gpu_grouped(x, off, q, s)
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    xb = util.bits(x)
+    ref = oracle.grouped_w8a16(xb, off, q, s)
+    if ref.size >= 1024:
+        assert util.rel_frobenius(y, ref) <= W8A16_FROB
+    ax, aq = _abs_inputs(xb, q)
+    check_elementwise(y, ref, oracle.grouped_w8a16(ax, off, aq, s), k)
+
+
+def test_grouped_bad_offsets_reported_with_few_rows():
+    """The per-row slot launch checks every expert's offsets too."""
+    n, k = 16, 32
+    q, s = _experts(12, n, k, 72)
+    x = synthetic.activations(4, k, 73)
+    good = np.array([0, 0, 2, 2, 3, 3, 3, 3, 3, 3, 3, 3, 4], np.int32)
+    y_good = gpu_grouped(x, good, q, s)
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    bad = np.array([0, 0, 2, 1, 3, 3, 3, 3, 3, 3, 3, 3, 4], np.int32)  # expert 2 runs backwards
+    y_bad = gpu_grouped(x, bad, q, s)
+    assert capi.i8ql_get_device_error() == capi.I8QL_ERR_BAD_OFFSETS
+    assert np.array_equal(y_bad[3], y_good[3])  # expert 11 (row 3) was still computed
+
+
 def test_grouped_bad_offsets_reported():
     n, k = 16, 32
     q, s = _experts(3, n, k, 70)
