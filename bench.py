@@ -190,6 +190,7 @@ KERNEL_SOURCES = {
     "prefill": {"w8a8": ["w8a8.cu", "w8a8_fused.cu", "tc_common.cuh", "quant.cu"]},
     "sweep8b": {"w8a16": ["decode_gemm.cu"], "w8a8_decode": ["decode_gemm.cu", "quant.cu"],
                 "w8a8_prefill": ["w8a8.cu", "w8a8_fused.cu", "tc_common.cuh", "quant.cu"]},
+    "w4": {"w4a16": ["w4a16.cu"], "quant_w4": ["w4a16.cu", "quant_math.cuh"]},
 }
 
 
