@@ -22,8 +22,9 @@
 // every (token, slot) finds its row as the expert's offset plus the number
 // of earlier tokens in the expert's bitmap.  The grouping is therefore
 // deterministic and identical to the definition, with no atomics on global
-// memory.  (One CTA doing both measured 19.7 us at T = 64, issue-bound on
-// its one SM.)
+// memory.  Up to 32 tokens the grouping CTA's warps select them first (one
+// launch); beyond, one CTA doing both measured 19.7 us at T = 64, issue-bound
+// on its one SM, so the selection is its own launch.
 
 #include <cuda_runtime.h>
 
@@ -36,6 +37,7 @@ namespace {
 
 constexpr int kRouteThreads = 1024;
 constexpr int kSelectThreads = 256;
+constexpr int kInlineSelectTokens = kRouteThreads / 32;  // tokens the grouping CTA selects itself
 constexpr int kMaxLogitsPerLane = 8;  // E <= 256
 
 struct RouteParams {
@@ -47,64 +49,67 @@ struct RouteParams {
     float* slot_weight;  // [T, topk + shared]
 };
 
-// Selection, one warp per token (tokens spread over the whole GPU): the
-// softmax denominator and the top_k largest logits by repeated warp argmax
-// (equal logits: the lower index).  Writes each routed slot's expert id into
-// token_row (the grouping kernel turns it into a row) and its weight, and
-// weight 1 for the shared slots.
-__global__ void __launch_bounds__(kSelectThreads) moe_select_kernel(const RouteParams p) {
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+// Selection of token t by one warp: the softmax denominator and the top_k
+// largest logits by repeated warp argmax (equal logits: the lower index).
+// Writes each routed slot's expert id into token_row (the grouping turns it
+// into a row) and its weight, and weight 1 for the shared slots.
+__device__ __forceinline__ void select_token(const RouteParams& p, int t, int lane) {
     const int E = (int)p.E, topk = (int)p.topk, S = (int)(p.topk + p.shared);
-    pdl_wait();
-    for (int t = blockIdx.x * (kSelectThreads / 32) + warp; t < (int)p.T; t += gridDim.x * (kSelectThreads / 32)) {
-        const float* lt = p.logits + (int64_t)t * E;
-        float l[kMaxLogitsPerLane];
-        float mx = -INFINITY;
+    const float* lt = p.logits + (int64_t)t * E;
+    float l[kMaxLogitsPerLane];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxLogitsPerLane; ++i) {
+        const int e = lane + 32 * i;
+        l[i] = e < E ? __ldg(lt + e) : -INFINITY;
+        mx = fmaxf(mx, l[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxLogitsPerLane; ++i)
+        if (lane + 32 * i < E) sum += expf(l[i] - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    unsigned taken = 0u;  // this lane's chosen logits
+    for (int s = 0; s < topk; ++s) {
+        // the lane's best untaken logit, lowest index first among equals
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < kMaxLogitsPerLane; ++i) {
             const int e = lane + 32 * i;
-            l[i] = e < E ? __ldg(lt + e) : -INFINITY;
-            mx = fmaxf(mx, l[i]);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float sum = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kMaxLogitsPerLane; ++i)
-            if (lane + 32 * i < E) sum += expf(l[i] - mx);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        unsigned taken = 0u;  // this lane's chosen logits
-        for (int s = 0; s < topk; ++s) {
-            // the lane's best untaken logit, lowest index first among equals
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < kMaxLogitsPerLane; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !(taken >> i & 1u) && (l[i] > bv || bi == 0x7fffffff)) {
-                    bv = l[i];
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-            if (lane == (s & 31)) {  // slot s is written by one lane (top_k may exceed 32)
-                p.token_row[(int64_t)t * S + s] = bi;
-                p.slot_weight[(int64_t)t * S + s] = expf(bv - mx) / sum;
+            if (e < E && !(taken >> i & 1u) && (l[i] > bv || bi == 0x7fffffff)) {
+                bv = l[i];
+                bi = e;
             }
         }
-        for (int s = topk + lane; s < S; s += 32) p.slot_weight[(int64_t)t * S + s] = 1.0f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+        if (lane == (s & 31)) {  // slot s is written by one lane (top_k may exceed 32)
+            p.token_row[(int64_t)t * S + s] = bi;
+            p.slot_weight[(int64_t)t * S + s] = expf(bv - mx) / sum;
+        }
     }
+    for (int s = topk + lane; s < S; s += 32) p.slot_weight[(int64_t)t * S + s] = 1.0f;
+}
+
+// Selection, one warp per token, the tokens spread over the whole GPU.
+__global__ void __launch_bounds__(kSelectThreads) moe_select_kernel(const RouteParams p) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    pdl_wait();
+    for (int t = blockIdx.x * (kSelectThreads / 32) + warp; t < (int)p.T; t += gridDim.x * (kSelectThreads / 32))
+        select_token(p, t, lane);
 }
 
 // Grouping, one CTA: each (token, routed slot) marks its expert's token
@@ -121,6 +126,10 @@ __global__ void __launch_bounds__(kRouteThreads) moe_group_kernel(const RoutePar
     uint32_t* before = route_smem + E * W;     // [E][W] set bits in earlier words
     __shared__ int32_t offs[257 + 64];
     pdl_wait();
+    if (T <= kInlineSelectTokens) {
+        // few tokens: this CTA's warps select them too (no separate launch)
+        if ((int)(threadIdx.x >> 5) < T) select_token(p, (int)(threadIdx.x >> 5), (int)(threadIdx.x & 31));
+    }
     for (int i = threadIdx.x; i < E * W; i += kRouteThreads) bits[i] = 0u;
     __syncthreads();
     for (int i = threadIdx.x; i < T * topk; i += kRouteThreads) {
@@ -256,7 +265,7 @@ cudaError_t launch_moe_route(const float* logits, int64_t T, int64_t E, int64_t 
         opted[dev] = true;
     }
     RouteParams p{logits, T, E, topk, shared, offsets, row_token, token_row, slot_weight};
-    if (T > 0) {
+    if (T > kInlineSelectTokens) {
         const int64_t blocks = std::min<int64_t>((T + kSelectThreads / 32 - 1) / (kSelectThreads / 32), 4 * env.sm_count);
         e = launch_kernel(moe_select_kernel, dim3((unsigned)blocks), dim3(kSelectThreads), 0, env.stream, kNoCluster, p);
         if (e != cudaSuccess) return e;
