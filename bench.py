@@ -40,7 +40,11 @@ weights in L2 (between timed steps nothing is reused either).  The timed
 region replays K steps of the part's graph back to back.  Launches of one
 kernel class run back to back (programmatic dependent launch overlaps their
 prologues), and an external CUDA event pair around each class's batch times
-it live: average launch duration = batch time / launches.
+it live: average launch duration = batch time / launches.  The decode,
+sweep and one-launch parts run with the library's early weight loads on
+(i8ql_set_early_weight_loads: split-K decode GEMMs start their weight
+stream before waiting for the previous kernel, whose outputs they do not
+read as weights); config.early_weight_loads names those parts.
 
 value (decode) = algorithmic HBM bytes of all launches / step time (GB/s);
 prefill TOPS = 2*M*N*K summed over the W8A8 launches / step time.
@@ -695,8 +699,23 @@ def run_reference(args, world, rank):
     return 0
 
 
+# Parts whose decode GEMMs run with early weight loads (the serving option of
+# i8ql_set_early_weight_loads): their weights are static during the step, and
+# no GEMM follows a kernel that writes its weights.
+EARLY_WEIGHT_PARTS = ("decode", "sweep8b", "fused")
+
+
 def time_part(part, args, world, local, stream):
     """Build, capture and time one part; returns its measurements."""
+    from int8_quantized_linear_gb300 import capi
+    capi.i8ql_set_early_weight_loads(part in EARLY_WEIGHT_PARTS)
+    try:
+        return _time_part(part, args, world, local, stream)
+    finally:
+        capi.i8ql_set_early_weight_loads(False)
+
+
+def _time_part(part, args, world, local, stream):
     from int8_quantized_linear_gb300 import capi
     device = torch.device("cuda", local)
     wl = Workload(part, device)
@@ -854,6 +873,7 @@ def run_ours(args, world, rank, local):
                    "top_level": workload_name(top),
                    "l2": "inputs larger than L2: every GEMM launch reads its own weight copy, "
                          ">1 GB touched per step of each part",
+                   "early_weight_loads": list(EARLY_WEIGHT_PARTS),
                    "graph": r["graph"]},
         "roofline": roofline(top, r),
         "kernels": r["kernels"],

@@ -486,6 +486,24 @@ int32_t i8ql_version(void);
  */
 void i8ql_debug_stream_k_timeout(int32_t on);
 
+/*
+ * Early weight loads for the decode GEMMs (serving option, no counterpart on
+ * the pages).  Every kernel of this library waits for the kernel launched
+ * before it on the same stream (programmatic dependent launch) before it
+ * reads anything.  With `on` nonzero (process-wide; default off) the
+ * decode-size GEMMs -- w8a16_gemm, w8a8_gemm and w8a8_linear with M <= 64,
+ * w8a8_linear_fused; not the grouped ones, whose weight addresses depend on
+ * device offsets -- instead load the first few k-steps of their weights
+ * before that wait, so the weight stream starts while the previous kernel
+ * drains; tokens, scales, bias and outputs still wait.  The caller promises
+ * that the kernel launched immediately before such a call on its stream does
+ * not write that call's weights (a weight quantization followed directly by
+ * a GEMM on its output needs the option off, or any other kernel between
+ * them).  Results are identical either way.
+ */
+void i8ql_set_early_weight_loads(int32_t on);
+int32_t i8ql_early_weight_loads(void);
+
 #ifdef __cplusplus
 }
 #endif

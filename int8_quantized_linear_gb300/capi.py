@@ -46,6 +46,8 @@ SIGNATURES = {
     "i8ql_status_string": (ctypes.c_char_p, [_S]),
     "i8ql_version": (_S, []),
     "i8ql_debug_stream_k_timeout": (None, [_S]),
+    "i8ql_set_early_weight_loads": (None, [_S]),
+    "i8ql_early_weight_loads": (_S, []),
     "quantize_weight_per_channel_fp8": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "quantize_act_per_token_fp8": (_S, [_P, _I64, _I64, _P, _P, _P]),
     "w8a8_fp8_gemm": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -292,6 +294,17 @@ def i8ql_debug_stream_k_timeout(on: bool) -> None:
     """Test hook: while on, stream-K finishers wait for a flag nothing writes
     (1 ms limit), so the call records I8QL_ERR_TIMEOUT without hanging."""
     lib().i8ql_debug_stream_k_timeout(1 if on else 0)
+
+
+def i8ql_set_early_weight_loads(on: bool) -> None:
+    """Serving option: decode-size GEMMs load their first weights before
+    waiting for the previous kernel on the stream (which must not write
+    them).  Process-wide; off by default."""
+    lib().i8ql_set_early_weight_loads(1 if on else 0)
+
+
+def i8ql_early_weight_loads() -> bool:
+    return bool(lib().i8ql_early_weight_loads())
 
 
 # ---------------------------------------------------------------- FP8 E4M3

@@ -29,6 +29,7 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<int> g_debug_sk_timeout{0};
+std::atomic<int> g_early_weights{0};
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -67,6 +68,7 @@ i8ql_status from_cuda(cudaError_t e) { return e == cudaSuccess ? I8QL_OK : I8QL_
 }  // namespace
 
 bool debug_sk_timeout() { return g_debug_sk_timeout.load(std::memory_order_relaxed) != 0; }
+bool early_weight_loads() { return g_early_weights.load(std::memory_order_relaxed) != 0; }
 
 bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status) {
     int dev = -1;
@@ -501,5 +503,9 @@ const char* i8ql_status_string(i8ql_status status) {
 int32_t i8ql_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 void i8ql_debug_stream_k_timeout(int32_t on) { g_debug_sk_timeout.store(on != 0 ? 1 : 0, std::memory_order_relaxed); }
+
+void i8ql_set_early_weight_loads(int32_t on) { g_early_weights.store(on != 0 ? 1 : 0, std::memory_order_relaxed); }
+
+int32_t i8ql_early_weight_loads(void) { return g_early_weights.load(std::memory_order_relaxed); }
 
 }  // extern "C"

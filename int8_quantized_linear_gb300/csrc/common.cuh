@@ -96,6 +96,9 @@ bool launch_env(void* stream, LaunchEnv* env, i8ql_status* status);
 // Test hook (i8ql_debug_stream_k_timeout): stream-K finishers wait for a
 // flag value that is never written, with a 1 ms limit.
 bool debug_sk_timeout();
+// i8ql_set_early_weight_loads: decode GEMMs may load weights before waiting
+// for the previous kernel on the stream.
+bool early_weight_loads();
 
 // Kernel launchers.  They assume validated arguments.
 // W8A8 up to this many tokens runs on the decode kernel (int8 mma.sync,

@@ -259,3 +259,14 @@ def test_w8a8_linear_fused_argument_errors(lib):
     assert f(*args) == capi.I8QL_ERR_INVALID_ARG
     args = list(ok); args[8] = 0
     assert f(*args) == capi.I8QL_OK
+
+
+def test_early_weight_loads_setting(lib):
+    """Process-wide option, off by default; setting it needs no device."""
+    assert lib.i8ql_early_weight_loads() == 0
+    lib.i8ql_set_early_weight_loads(1)
+    try:
+        assert lib.i8ql_early_weight_loads() == 1
+    finally:
+        lib.i8ql_set_early_weight_loads(0)
+    assert lib.i8ql_early_weight_loads() == 0

@@ -464,6 +464,44 @@ def _fused_linear_check(x, qw_ref, sw_ref, bias_bits=None):
     assert util.max_ulp_diff(y.cpu().numpy().view(np.uint16)[pm, pn], ref_y) <= 1
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 16, 16), (3, 300, 1040), (8, 2560, 2560), (8, 19456, 2560), (17, 513, 9744),
+                                   (64, 6144, 2560)])
+def test_early_weight_loads_give_identical_results(m, n, k):
+    """With early weight loads on, the decode GEMMs start their weight stream
+    before waiting for the previous kernel; here the previous kernel writes
+    the tokens (the activation quantization), which must still be waited
+    for.  Every output and accumulator equals the option-off result bit for
+    bit."""
+    w = synthetic.weight(n, k, 11, device="cuda")
+    qw, sw = capi.quantize_weight_per_channel_int8(w)
+    x = synthetic.activations(m, k, 12, device="cuda")
+    torch.cuda.synchronize()  # the weights are ready before any early load
+
+    def run():
+        qx, sx = capi.quantize_act_per_token_int8(x)
+        acc = torch.empty((m, n), dtype=torch.int32, device="cuda")
+        y8 = capi.w8a8_gemm(qx, sx, qw, sw, acc_debug=acc)
+        y16 = capi.w8a16_gemm(x, qw, sw)
+        yl = capi.w8a8_linear(x, qw, sw)
+        outs = [y8.view(torch.int16).clone(), acc.clone(), y16.view(torch.int16).clone(), yl.view(torch.int16).clone()]
+        if m <= 8:
+            outs.append(capi.w8a8_linear(x, qw, sw, fused=True).view(torch.int16).clone())
+        torch.cuda.synchronize()
+        return outs
+
+    assert not capi.i8ql_early_weight_loads()
+    ref = run()
+    capi.i8ql_set_early_weight_loads(True)
+    try:
+        assert capi.i8ql_early_weight_loads()
+        got = run()
+    finally:
+        capi.i8ql_set_early_weight_loads(False)
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+
+
 @pytest.mark.parametrize("m", [1, 2, 5, 8])
 @pytest.mark.parametrize("n,k", [(16, 16), (40, 48), (300, 1040), (2560, 2560), (513, 9744)])
 def test_w8a8_linear_fused_decode_shapes(m, n, k):
