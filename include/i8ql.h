@@ -131,13 +131,17 @@ i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const
  * Computes exactly what quantize_act_per_token_int8(x) followed by w8a8_gemm
  * computes (same codes, scales, accumulators and outputs), in fewer passes
  * over memory: for M > 64 the quantization pass writes the codes in the form
- * the tensor-core GEMM reads, so the GEMM needs no separate conversion pass.
+ * the tensor-core GEMM reads, so the GEMM needs no separate conversion pass;
+ * for M <= 8 with a weight whose decode GEMM is one wave without split-K
+ * (large N, up to about 600 row blocks of 32) it is w8a8_linear_fused (one
+ * launch).
  * Inputs: x bf16 [M, K], qw int8 [N, K], sw fp32 [N], bias bf16 [N] or NULL.
  * Outputs: y bf16 [M, N]; qx int8 [M, K] and sx fp32 [M] receive the token
  * codes and scales when given (each may be NULL); acc_debug int32 [M, N] or
  * NULL.  Takes a temporary stream-ordered workspace (at most 2*M*K + 4*M
  * bytes, plus the stream-K workspace of w8a8_gemm when the plan runs
- * stream-K).  Errors and argument rules as w8a8_gemm, with x checked like y.
+ * stream-K; none in the one-launch case).  Errors and argument rules as
+ * w8a8_gemm, with x checked like y.
  */
 i8ql_status w8a8_linear(const i8ql_bf16* x, const int8_t* qw, const float* sw, const i8ql_bf16* bias,
                         i8ql_bf16* y, int8_t* qx, float* sx, int32_t* acc_debug,
@@ -157,10 +161,11 @@ i8ql_status w8a8_linear(const i8ql_bf16* x, const int8_t* qw, const float* sw, c
  * split one row block's k range share each token's absmax through
  * distributed shared memory, then form the int8 codes from the bf16 tokens
  * in their main loop.  No workspace.  M > 8 returns I8QL_ERR_UNSUPPORTED.
- * Measured on GB300 it is slower than w8a8_linear's two launches, whose
- * quantization pass overlaps the GEMM's prologue through programmatic
- * dependent launch, so w8a8_linear does not use it; it serves callers that
- * want one kernel per layer.
+ * Measured on GB300 it is faster than a quantization launch plus the GEMM
+ * when the GEMM runs unsplit (Qwen3-4B gate_up at M <= 8: 14.7 against
+ * 16.0 us), and slower on split-K shapes, where the cluster's absmax
+ * exchange sits in front of the token loads (qkv: 9.1 against 8.3 us), and
+ * beyond one wave of CTAs; w8a8_linear takes it in the first case.
  */
 i8ql_status w8a8_linear_fused(const i8ql_bf16* x, const int8_t* qw, const float* sw, const i8ql_bf16* bias,
                               i8ql_bf16* y, int8_t* qx, float* sx, int32_t* acc_debug, int64_t M, int64_t N, int64_t K,

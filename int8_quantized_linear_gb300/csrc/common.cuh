@@ -137,6 +137,9 @@ cudaError_t launch_w8a8_decode(const int8_t* qx, const float* sx, const int8_t* 
 // kernel quantizes its token rows itself; qx / sx receive the codes and
 // scales when not null.
 constexpr int64_t kW8A8FusedMaxM = 8;
+// Whether the one-launch kernel runs an N x K weight as one unsplit wave
+// (where it measured faster than a quantization launch plus the GEMM).
+bool w8a8_decode_fused_preferred(int64_t N, int64_t K, int sms);
 cudaError_t launch_w8a8_decode_fused(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
                                      uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                      const LaunchEnv& env);

@@ -679,6 +679,15 @@ cudaError_t launch_w8a16(const uint16_t* x, const int32_t* offsets, int64_t E, c
     return dispatch<Op::kW8A16, true>(p, std::max<int64_t>(per_expert, 1), active, env.sm_count, env.stream);
 }
 
+bool w8a8_decode_fused_preferred(int64_t N, int64_t K, int sms) {
+    DecodeParams p{};
+    p.N = N;
+    p.K = K;
+    const int64_t capacity = (int64_t)sms * resident_ctas<Op::kW8A8Q, 2, 1, false>();
+    const int64_t row_blocks = row_blocks_of<2>(p);
+    return choose_split(row_blocks, 1, K, capacity) == 1 && row_blocks <= capacity;
+}
+
 cudaError_t launch_w8a8_decode_fused(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
                                      uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                      const LaunchEnv& env) {

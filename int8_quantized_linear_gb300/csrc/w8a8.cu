@@ -122,6 +122,14 @@ cudaError_t linear_layout(int64_t M, int64_t N, int64_t K, bool have_qx, bool ha
 cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias, uint16_t* y,
                                int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                const LaunchEnv& env) {
+    // Few tokens and a weight whose decode GEMM is one unsplit wave: the
+    // one-launch form, which quantizes the tokens inside the GEMM, measured
+    // faster there (Qwen3-4B gate_up: 14.7 against 16.0 us) and slower on
+    // split-K shapes (qkv 9.1 against 8.3 us) and beyond one wave (Qwen3-8B
+    // gate_up); its results are the same bit for bit, and it needs no
+    // workspace.
+    if (M <= kW8A8FusedMaxM && w8a8_decode_fused_preferred(N, K, env.sm_count))
+        return launch_w8a8_decode_fused(x, qw, sw, bias, y, qx, sx, acc, M, N, K, env);
     LinearLayout l;
     cudaError_t e = linear_layout(M, N, K, qx != nullptr, sx != nullptr, env.sm_count, &l);
     if (e != cudaSuccess) return e;

@@ -403,10 +403,12 @@ def test_w8a8_stream_k_timeout_is_reported_and_recoverable():
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 256, 1024), (7, 300, 2064), (64, 513, 1040), (65, 640, 2560),
-                                   (128, 2560, 2560), (300, 1000, 4160), (2048, 2560, 2560)])
+                                   (128, 2560, 2560), (300, 1000, 4160), (2048, 2560, 2560),
+                                   (3, 19456, 2560), (8, 12288, 4096)])
 def test_w8a8_linear_matches_quantize_then_gemm(m, n, k):
     """The fused layer gives the two-call result bit for bit, and the oracle's
-    codes, scales, accumulators and outputs."""
+    codes, scales, accumulators and outputs (the last two shapes take the
+    one-launch form: few tokens, an unsplit decode GEMM)."""
     x = synthetic.activations(m, k, m + k)
     w = synthetic.weight(n, k, n + k)
     qw_ref, sw_ref = oracle.quant_rows(util.bits(w))
