@@ -36,6 +36,7 @@ import torch
 
 __all__ = [
     "QWEN3_4B_SHAPES",
+    "QWEN3_4B_EXTRA_SHAPES",
     "QWEN3_8B_SHAPES",
     "DSMOE_SHAPES",
     "weight",
@@ -56,6 +57,9 @@ QWEN3_4B_SHAPES = {
     "gate_up": (19456, 2560),
     "down": (2560, 9728),
 }
+# The o projection with the input width its attention implies (32 query
+# heads x 128 = 4096), next to the stated [2560, 2560]: an extra parity case.
+QWEN3_4B_EXTRA_SHAPES = {"o_heads": (2560, 4096)}
 QWEN3_8B_SHAPES = {
     "qkv": (6144, 4096),
     "o": (4096, 4096),

@@ -224,10 +224,13 @@ def _points(m, n, count, seed):
     return pm, pn
 
 
-@pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
+QWEN3_4B_ALL = {**synthetic.QWEN3_4B_SHAPES, **synthetic.QWEN3_4B_EXTRA_SHAPES}
+
+
+@pytest.mark.parametrize("shape", list(QWEN3_4B_ALL))
 @pytest.mark.parametrize("m", [128, 2048])
 def test_w8a8_qwen3_4b_prefill_sampled(shape, m):
-    n, k = synthetic.QWEN3_4B_SHAPES[shape]
+    n, k = QWEN3_4B_ALL[shape]
     w = synthetic.weight(n, k, 1)
     x = synthetic.activations(m, k, 2)
     qw, sw = check_quant(w, True)
@@ -256,11 +259,11 @@ def gpu_w8a8_points(qx, sx, qw, sw, bias_bits, pm, pn):
     return a, yy
 
 
-@pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
+@pytest.mark.parametrize("shape", list(QWEN3_4B_ALL))
 def test_w8a8_qwen3_4b_decode_full_size(shape):
     """Qwen3-4B decode linears, M in {1, 4, 8}, bias off: the int8 mma.sync
     decode kernel at full size, sampled against the oracle."""
-    n, k = synthetic.QWEN3_4B_SHAPES[shape]
+    n, k = QWEN3_4B_ALL[shape]
     qw, sw = oracle.quant_rows(util.bits(synthetic.weight(n, k, 1)))
     for m in (1, 4, 8):
         qx, sx = oracle.quant_rows(util.bits(synthetic.activations(m, k, 20 + m)))
@@ -583,9 +586,9 @@ def test_w8a16_tiny_layer():
     check_w8a16(x, qw, sw)
 
 
-@pytest.mark.parametrize("shape", list(synthetic.QWEN3_4B_SHAPES))
+@pytest.mark.parametrize("shape", list(QWEN3_4B_ALL))
 def test_w8a16_qwen3_4b_decode_full(shape):
-    n, k = synthetic.QWEN3_4B_SHAPES[shape]
+    n, k = QWEN3_4B_ALL[shape]
     qw, sw = check_quant(synthetic.weight(n, k, 1), True)
     for m in (1, 4, 8):
         check_w8a16(synthetic.activations(m, k, 10 + m), qw, sw)
