@@ -186,6 +186,21 @@ def test_fp8_gemm_shapes(m, n, k):
     check_gemm(qx, sx, qw, sw, bias)
 
 
+@pytest.mark.parametrize("m,n,k", [(3, 40, 131072), (130, 257, 65552)])
+def test_fp8_gemm_longest_k(m, n, k):
+    """The longest K the exact oracle covers (2^17 products: its fp64 sum of
+    multiples of 2^-18 below 2^18 is exact up to there), and a long K on the
+    split-K path: the fp32 accumulation over the whole range stays within
+    its bound."""
+    qx, sx = _fp8_codes(m, k, m + 3)
+    qw, sw = _fp8_codes(n, k, n + 4, 0.02)
+    pm, pn = (a.ravel() for a in np.meshgrid(np.arange(m), np.arange(n), indexing="ij"))
+    if pm.size > 4000:
+        g = np.random.default_rng(k)
+        pm, pn = g.integers(0, m, 4000), g.integers(0, n, 4000)
+    check_gemm(qx, sx, qw, sw, None, pm, pn)
+
+
 def test_fp8_plans_cover_split_k_tile_widths_and_pairs():
     """The prefill shapes exercise every launch form: split-K clusters of
     single CTAs at both tile widths (few tiles), persistent single CTAs, and

@@ -138,6 +138,14 @@ def test_w4a16_qwen3_8b_full(shape, m):
     check_gemm(synthetic.activations(m, k, 40 + m), q, s)
 
 
+@pytest.mark.parametrize("m,n", [(1, 24), (8, 40)])
+def test_w4a16_longest_k(m, n):
+    """The largest K (a multiple of 128) the boundary accepts."""
+    k = 133120
+    q, s = check_quant(_adversarial(n, k, n + 5))
+    check_gemm(synthetic.activations(m, k, m + 6), q, s)
+
+
 def test_w4a16_empty_tokens():
     q = torch.zeros((16, 64), dtype=torch.uint8, device="cuda")
     s = torch.ones((16, 1), dtype=torch.bfloat16, device="cuda")
