@@ -444,7 +444,8 @@ class Workload:
                 "moe_mlp", lambda x=x, lg=logits, w=weights, o=out: capi.moe_expert_mlp_w8a16(
                     x, lg, synthetic.DSMOE_TOPK, synthetic.DSMOE_SHARED, w[0], w[1], w[2], w[3], out=o),
                 bytes_moe(counts, tokens, hidden, inter, synthetic.DSMOE_ROUTED),
-                2 * rows * (inter2 * hidden + hidden * inter), f"moe_mlp T={tokens}", gpu_kernels=4))
+                2 * rows * (inter2 * hidden + hidden * inter), f"moe_mlp T={tokens}",
+                gpu_kernels=4 if tokens <= 32 else 5))  # routing is one launch up to 32 tokens
             self._pin_out(out)
 
     def run(self, events=None):

@@ -54,6 +54,14 @@ enum {
  * floor((2^31 - 1) / 127^2) = 133,144. */
 #define I8QL_MAX_K 133144
 
+/* W8A8 with at most this many tokens runs on the decode kernel (int8
+ * mma.sync, weight streaming); larger M runs on the tcgen05 tensor-core
+ * kernel.  Measured crossover on GB300: at M = 48 and 64 the tensor-core
+ * kernel takes half the time (Qwen3-8B gate_up at M = 64: 60 against
+ * 123 us); at M <= 32 the decode kernel is as fast or faster on most
+ * shapes. */
+#define I8QL_W8A8_DECODE_MAX_M 32
+
 /*
  * Per-output-channel symmetric int8 weight quantization.
  *
@@ -101,7 +109,7 @@ i8ql_status quantize_act_per_token_int8(const i8ql_bf16* x, int64_t M, int64_t K
  * sw fp32 [N], bias bf16 [N] or NULL.  Outputs: y bf16 [M, N]; acc_debug
  * int32 [M, N] or NULL (when given, receives the exact accumulator).
  * The epilogue may fuse multiply-adds: y is within one bf16 ulp of the
- * value above.  For M > 64 the call takes a temporary stream-ordered
+ * value above.  For M > I8QL_W8A8_DECODE_MAX_M (32) the call takes a temporary stream-ordered
  * workspace (cudaMallocAsync / cudaFreeAsync on `stream`): the fp16 codes of
  * the tokens, 2*M*K bytes, plus, when the plan runs stream-K (see
  * i8ql_w8a8_plan), one int32 partial tile of 128 x 256 per CTA pair half
@@ -130,7 +138,7 @@ i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const
  *
  * Computes exactly what quantize_act_per_token_int8(x) followed by w8a8_gemm
  * computes (same codes, scales, accumulators and outputs), in fewer passes
- * over memory: for M > 64 the quantization pass writes the codes in the form
+ * over memory: for M > 32 the quantization pass writes the codes in the form
  * the tensor-core GEMM reads, so the GEMM needs no separate conversion pass;
  * for M <= 8 with a weight whose decode GEMM is one wave without split-K
  * (large N, up to about 600 row blocks of 32) it is w8a8_linear_fused (one
@@ -382,7 +390,8 @@ i8ql_status moe_combine(const i8ql_bf16* yd, const int32_t* token_row, const flo
  * Inputs: x bf16 [T, H], logits fp32 [T, E_routed]; experts E = E_routed +
  * n_shared (routed first): qw_gate_up int8 [E, 2I, H] with sw_gate_up fp32
  * [E, 2I], qw_down int8 [E, H, I] with sw_down fp32 [E, H].  Output out bf16
- * [T, H].  Four kernels; the intermediates (routing arrays, h [T*S, I] and
+ * [T, H].  Four kernels (five beyond 32 tokens, where the routing's token
+ * selection is its own launch); the intermediates (routing arrays, h [T*S, I] and
  * the down outputs [T*S, H], bf16) live in a temporary stream-ordered
  * workspace (cudaMallocAsync / cudaFreeAsync on `stream`).  Limits as
  * moe_route_topk; H and I multiples of 16.
@@ -401,16 +410,16 @@ i8ql_status moe_expert_mlp_w8a16(const i8ql_bf16* x, const float* logits, int64_
  * allocator calls on the hot path, hosts that own every buffer).  It computes
  * exactly what w8a8_gemm computes, with the same arguments, layouts and
  * errors, but where w8a8_gemm takes a temporary workspace from the
- * stream-ordered allocator (for M > 64: the fp16 codes of the tokens,
+ * stream-ordered allocator (for M > 32: the fp16 codes of the tokens,
  * 2 * M * K bytes, and a stream-K workspace when its plan uses one), this
  * one never runs stream-K (i8ql_w8a8_noalloc_plan) and uses a fixed array
  * compiled into the
  * library: I8QL_NOALLOC_MAX_ELEMENTS 16-bit elements (32 MiB), held by every
  * GPU that loads the library until the process exits.
  *
- *  - For M > 64, M * K must not exceed I8QL_NOALLOC_MAX_ELEMENTS, else
+ *  - For M > 32, M * K must not exceed I8QL_NOALLOC_MAX_ELEMENTS, else
  *    the call returns I8QL_ERR_WORKSPACE_LIMIT and launches nothing.  For
- *    M <= 64 the computation needs no workspace and any size is accepted.
+ *    M <= 32 the computation needs no workspace and any size is accepted.
  *  - The first call on a device looks up the array's device address (once
  *    per device, with that device current); make that first call before any
  *    stream capture.
@@ -442,7 +451,7 @@ i8ql_status i8ql_fp8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int3
  * device, without launching anything.
  *
  * No counterpart on the pages: a query for tests and profiling.  For
- * M <= 64 (the decode kernel) all outputs are 0.  Otherwise *tile_n is the
+ * M <= I8QL_W8A8_DECODE_MAX_M (the decode kernel) all outputs are 0.  Otherwise *tile_n is the
  * width (N side) of the output tiles of the tensor-core kernel (128, 160,
  * 192, 224 or 256; for M <= 128 the operands are swapped and the tokens fill
  * a 128-wide side), *split_k the number of CTAs of a thread-block cluster
@@ -496,7 +505,7 @@ void i8ql_debug_stream_k_timeout(int32_t on);
  * the pages).  Every kernel of this library waits for the kernel launched
  * before it on the same stream (programmatic dependent launch) before it
  * reads anything.  With `on` nonzero (process-wide; default off) the
- * decode-size GEMMs -- w8a16_gemm, w8a8_gemm and w8a8_linear with M <= 64,
+ * decode-size GEMMs -- w8a16_gemm, w8a8_gemm and w8a8_linear with M <= 32,
  * w8a8_linear_fused; not the grouped ones, whose weight addresses depend on
  * device offsets -- instead load the first few k-steps of their weights
  * before that wait, so the weight stream starts while the previous kernel

@@ -202,7 +202,7 @@ def w8a8_gemm_noalloc(qx, sx, qw, sw, y, bias=None, acc_debug=None, stream=None)
     For callers that cannot allocate while they run (graph replay with fixed
     memory, allocator-free serving loops): the output ``y`` must be passed in,
     and the large-M workspace comes from a fixed array inside the library, so
-    ``M * K`` may not exceed ``I8QL_NOALLOC_MAX_ELEMENTS`` when M > 64.
+    ``M * K`` may not exceed ``I8QL_NOALLOC_MAX_ELEMENTS`` when M > 32.
     Calls that could overlap on the GPU must not be issued (they share it).
     """
     m, k = qx.shape
@@ -266,7 +266,7 @@ def _plan(fn_name: str, m: int, n: int, k: int) -> tuple[int, int, int]:
 def i8ql_w8a8_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
     """(tile width, split-K factor, CTA-pair mode: 0 single CTAs, 1 pairs,
     2 pairs with stream-K) w8a8_gemm uses for an M x N x K problem on the
-    current device; (0, 0, 0) in the decode range (M <= 64)."""
+    current device; (0, 0, 0) in the decode range (M <= 32)."""
     return _plan("i8ql_w8a8_plan", m, n, k)
 
 

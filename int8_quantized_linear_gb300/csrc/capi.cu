@@ -495,7 +495,7 @@ const char* i8ql_status_string(i8ql_status status) {
         case I8QL_ERR_BAD_OFFSETS: return "grouped offsets are not 0..T_total and non-decreasing";
         case I8QL_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
         case I8QL_ERR_WORKSPACE_LIMIT:
-            return "problem too large for the fixed workspace of w8a8_gemm_noalloc (M * K > 16 Mi for M > 64)";
+            return "problem too large for the fixed workspace of w8a8_gemm_noalloc (M * K > 16 Mi for M > 32)";
         default: return "unknown status";
     }
 }

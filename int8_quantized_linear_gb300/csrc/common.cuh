@@ -103,7 +103,7 @@ bool early_weight_loads();
 // Kernel launchers.  They assume validated arguments.
 // W8A8 up to this many tokens runs on the decode kernel (int8 mma.sync,
 // weight streaming); larger M runs on the tcgen05 kernel.
-constexpr int64_t kW8A8DecodeMaxM = 64;
+constexpr int64_t kW8A8DecodeMaxM = I8QL_W8A8_DECODE_MAX_M;
 // Per-row quantization; the codes go to q (int8) and/or qh (fp16), either
 // nullable.  The kernel also sets the `nzero` words at `zero` to 0 (the
 // stream-K flags of the GEMM launched after it; nullable).
@@ -160,7 +160,7 @@ cudaError_t w8a8_sk_workspace(int64_t M, int64_t N, int64_t K, int sms, size_t* 
 cudaError_t launch_w8a8_ws(const int8_t* qx, const float* sx, const int8_t* qw, const float* sw,
                            const uint16_t* bias, uint16_t* y, int32_t* acc, int64_t M, int64_t N, int64_t K,
                            uint16_t* ws, void* sk_ws, size_t sk_bytes, const LaunchEnv& env);
-// tcgen05 W8A8 for M > 64: the token codes as fp16 (x16, [M, K]), the weight
+// tcgen05 W8A8 for M > kW8A8DecodeMaxM: the token codes as fp16 (x16, [M, K]), the weight
 // codes as int8 (converted inside the kernel).  Stream-K runs when the plan
 // wants it and sk_ws holds sk_bytes >= what w8a8_sk_workspace reports, its
 // flags zeroed by an earlier kernel of the stream.

@@ -1,4 +1,4 @@
-// W8A8 GEMM entry: routes a problem to the decode kernel (M <= 64, int8
+// W8A8 GEMM entry: routes a problem to the decode kernel (M <= 32, int8
 // mma.sync weight streaming, decode_gemm.cu) or, for larger M, to the
 // tcgen05 tensor-core kernel (w8a8_fused.cu) after one small pass that turns
 // the token codes into fp16 codes.  The fused linear layer (w8a8_linear)

@@ -1,4 +1,4 @@
-// W8A8 GEMM for M > 64: int8 weight tiles are converted to fp16 codes inside
+// W8A8 GEMM for M > 32: int8 weight tiles are converted to fp16 codes inside
 // the GEMM, between their TMA loads and the tensor core.
 //
 // Sources: "feat(quantization): support compressed-tensors W8A8 and mixed

@@ -326,7 +326,8 @@ def test_w8a8_plans_cover_tile_widths_and_split_k():
     for m, n, k in PLAN_SHAPES:
         if m <= 128:
             assert capi.i8ql_w8a8_plan(m, n, k) == capi.i8ql_w8a8_noalloc_plan(m, n, k)
-    assert capi.i8ql_w8a8_plan(64, 4096, 4096) == (0, 0, 0)
+    assert capi.i8ql_w8a8_plan(32, 4096, 4096) == (0, 0, 0)
+    assert capi.i8ql_w8a8_plan(33, 4096, 4096)[0] > 0
 
 
 @pytest.mark.parametrize("entry", ["gemm", "noalloc"])

@@ -53,7 +53,7 @@ def _both(qx, sx, qw, sw, bias):
 
 
 @pytest.mark.parametrize("shapes", [
-    [(300, 513, 1040), (200, 1024, 2064)],   # both take the workspace path (M > 64)
+    [(300, 513, 1040), (200, 1024, 2064)],   # both take the workspace path (M > 32)
     [(129, 6144, 1024), (8, 2560, 2560)],     # workspace path, then the decode path
 ])
 def test_noalloc_matches_w8a8_gemm_on_consecutive_calls(shapes):
