@@ -648,8 +648,11 @@ def _experts(e_count, n, k, seed):
 
 
 @pytest.mark.parametrize("counts", [[3, 0, 4, 2, 0], [0, 0, 0, 0, 9], [1, 1, 1, 1, 1], [70, 0, 0, 0, 5],
-                                    [0, 17, 0, 33, 0]])
+                                    [0, 17, 0, 33, 0], [200, 1, 0, 3, 100], [8, 9, 16, 17, 0, 64],
+                                    [64] * 3 + [1] * 9])
 def test_grouped_small(counts):
+    """Uneven groups, including experts with many token chunks (more rows
+    than experts: their later chunks run on extra slots of their own)."""
     n, k = 40, 80
     q, s = _experts(len(counts), n, k, 50)
     off = np.zeros(len(counts) + 1, np.int32)
