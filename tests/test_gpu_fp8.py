@@ -131,7 +131,7 @@ def check_gemm(qx, sx, qw, sw, bias_bits=None, pm=None, pn=None):
         pn = np.concatenate([g.integers(0, n, 4000), [0, n - 1, 0, n - 1]])
     _, ref = oracle.w8a8_fp8_points(qx, sx, qw, sw, bias_bits, pm, pn)
     got = y[pm, pn]
-    assert util.rel_frobenius(got, ref) <= FROB
+    assert util.rel_frobenius(got, ref) <= util.frob_bar(ref, FROB)
     bound = _bound(qx, sx, qw, sw, pm, pn, k) + np.abs(ref) * 2.0 ** -8 + 1e-30
     worst = np.argmax(np.abs(got - ref) - bound)
     assert np.all(np.abs(got - ref) <= bound), (pm[worst], pn[worst], got[worst], ref[worst], bound[worst])

@@ -109,7 +109,7 @@ def check_gemm(x_bf16, q, s):
     xb = util.bits(x_bf16)
     ref = oracle.w4a16(xb, q, s)
     if ref.size >= FROB_MIN_ELEMENTS:
-        assert util.rel_frobenius(y, ref) <= FROB
+        assert util.rel_frobenius(y, ref) <= util.frob_bar(ref, FROB)
     # magnitudes: the oracle on |x| and |codes| (packed again as nibbles)
     k = x_bf16.shape[1]
     codes = np.abs(oracle.w4_unpack(q, k).astype(np.int16))

@@ -32,6 +32,16 @@ def rel_frobenius(y: np.ndarray, ref: np.ndarray) -> float:
     return float(np.linalg.norm(y - ref) / den) if den > 0 else float(np.linalg.norm(y))
 
 
+def frob_bar(ref: np.ndarray, bar: float) -> float:
+    """The relative-Frobenius bar a bf16 output of `ref` can be held to: `bar`,
+    or, where even the correctly rounded result misses it, that rounding
+    floor with 5 % room (outputs whose energy sits in a few elements driven
+    by outlier channels, each rounded with up to 2^-8 relative error).  The
+    floor comes from the oracle's result alone."""
+    rounded = torch.from_numpy(np.ascontiguousarray(ref, dtype=np.float64)).to(torch.bfloat16).double().numpy()
+    return max(bar, 1.05 * rel_frobenius(rounded, ref))
+
+
 def guarded(shape, dtype, device, fill, guard=256):
     """A tensor view followed by a guard band of sentinel values."""
     n = int(np.prod(shape)) if len(shape) else 1
