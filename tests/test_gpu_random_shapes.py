@@ -116,3 +116,73 @@ def test_grouped_random(case):
         assert util.rel_frobenius(y, ref) <= util.frob_bar(ref, 2e-3), (e_count, n, k, counts.tolist())
     ax, aq = _abs_inputs(xb, q)
     check_elementwise(y, ref, oracle.grouped_w8a16(ax, off, aq, s), k)
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_w8a8_linear_random(case):
+    """The linear layer (its quantization inside the call: one launch, two,
+    or the tensor-core path's fp16 codes, by shape) equals the two calls bit
+    for bit and the oracle's codes and scales."""
+    m, n, k = _shape(6000 + case, 300, 600, 16, 160)
+    if case % 4 == 0:
+        m = 1 + case % 8  # the one-launch range
+    x = synthetic.activations(m, k, 130 + case)
+    qw, sw = oracle.quant_rows(util.bits(synthetic.weight(n, k, 140 + case)))
+    qw_d, sw_d = torch.from_numpy(qw).cuda(), torch.from_numpy(sw).cuda()
+    qx = torch.empty((m, k), dtype=torch.int8, device="cuda")
+    sx = torch.empty((m,), dtype=torch.float32, device="cuda")
+    y = capi.w8a8_linear(x.cuda(), qw_d, sw_d, qx=qx, sx=sx)
+    q2, s2 = capi.quantize_act_per_token_int8(x.cuda())
+    y2 = capi.w8a8_gemm(q2, s2, qw_d, sw_d)
+    torch.cuda.synchronize()
+    qx_ref, sx_ref = oracle.quant_rows(util.bits(x))
+    assert np.array_equal(qx.cpu().numpy(), qx_ref) and np.array_equal(sx.cpu().numpy(), sx_ref)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), (m, n, k)
+
+
+@pytest.mark.parametrize("case", range(CASES // 2))
+def test_moe_layer_random(case):
+    """Random MoE layers (experts, top-k, shared experts, tokens, widths):
+    the routing is bit-exact, the layer equals its four stages called one by
+    one, and the whole chain is within the three stages' bars of the fp64
+    oracle chain."""
+    g = np.random.default_rng(7000 + case)
+    e_r = int(g.integers(1, 65))
+    topk = int(g.integers(1, min(8, e_r) + 1))
+    shared = int(g.integers(0, 3))
+    tokens = int(g.integers(1, 101))
+    hid = 16 * int(g.integers(1, 33))
+    inter = 16 * int(g.integers(1, 33))
+    e_all = e_r + shared
+    qgu = np.empty((e_all, 2 * inter, hid), np.int8)
+    sgu = np.empty((e_all, 2 * inter), np.float32)
+    qd = np.empty((e_all, hid, inter), np.int8)
+    sd = np.empty((e_all, hid), np.float32)
+    for e in range(e_all):
+        qgu[e], sgu[e] = oracle.quant_rows(util.bits(synthetic.weight(2 * inter, hid, 300 + 70 * case + e)))
+        qd[e], sd[e] = oracle.quant_rows(util.bits(synthetic.weight(hid, inter, 900 + 70 * case + e)))
+    x = synthetic.activations(tokens, hid, 150 + case)
+    logits = synthetic.gate_logits(tokens, e_r, 160 + case).numpy()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    off, row_token, token_row, w = capi.moe_route_topk(dev(logits), topk, shared)
+    ref = oracle.moe_route(logits, topk, shared)
+    torch.cuda.synchronize()
+    assert np.array_equal(off.cpu().numpy(), ref.offsets)
+    assert np.array_equal(row_token.cpu().numpy(), ref.row_token)
+    assert np.array_equal(token_row.cpu().numpy(), ref.token_row)
+    h = capi.grouped_w8a16_silu_mul(x.cuda(), row_token, off, dev(qgu), dev(sgu))
+    yd = capi.grouped_w8a16_gemm(h, off, dev(qd), dev(sd))
+    staged = capi.moe_combine(yd, token_row, w)
+    out = capi.moe_expert_mlp_w8a16(x.cuda(), dev(logits), topk, shared, dev(qgu), dev(sgu), dev(qd), dev(sd))
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), staged.view(torch.int16))
+    xg = util.bits(x)[ref.row_token]
+    h64 = oracle.silu_mul(oracle.grouped_w8a16(xg, ref.offsets, qgu, sgu))
+    yd64 = np.zeros((h64.shape[0], hid))
+    for e in range(e_all):
+        a, b = ref.offsets[e], ref.offsets[e + 1]
+        if b > a:
+            yd64[a:b] = h64[a:b] @ (qd[e].astype(np.float64) * sd[e][:, None].astype(np.float64)).T
+    out64 = oracle.moe_combine(yd64, ref.token_row, ref.slot_weight)
+    got = util.from_bits(util.bits(out.cpu())).double().numpy()
+    assert util.rel_frobenius(got, out64) <= util.frob_bar(out64, 6e-3), (e_r, topk, shared, tokens, hid, inter)
