@@ -88,7 +88,6 @@ MOE_TOKENS = (1, 8, 64)
 SWEEP_W8A16_MS = (1, 2, 4, 8, 16, 32, 64)
 W4_MS = (1, 4, 8)
 SWEEP_W8A8_MS = (1, 2, 4, 8, 16, 32, 64, 128, 512, 2048, 8192)
-W8A8_DECODE_MAX_M = 64  # above it a W8A8 call runs on the tensor-core kernel
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Kernel classes of each part, in launch order; "tensor" classes are
 # contractions on the tensor-core kernel (TOPS against the bf16-pipe peak),
@@ -280,7 +279,7 @@ class Workload:
         self.launches.append(Launch(
             kernel, lambda x=x, q=q, s=s, b=bias, y=y: capi.w8a8_linear(x, q, s, bias=b, y=y),
             bytes_quant(m, k) + bytes_w8a8(m, n, k, bias is not None), 2 * m * n * k, f"{label} M={m}",
-            gpu_kernels=2))
+            gpu_kernels=capi.i8ql_w8a8_linear_launches(m, n, k)))
         self._pin_out(y)
 
     def _w8a16(self, kernel, x, q, s, label):
@@ -349,7 +348,7 @@ class Workload:
                 self._linear("w8a8", x, qs[mi], s, bias, f"w8a8_linear {name}")
 
     def _sweep8b(self, seed):
-        from int8_quantized_linear_gb300 import synthetic
+        from int8_quantized_linear_gb300 import capi, synthetic
         seed += 40
         for si, (name, (n, k)) in enumerate(synthetic.QWEN3_8B_SHAPES.items()):
             w, qs, s = self._weight_copies(n, k, seed + si, len(SWEEP_W8A16_MS) + len(SWEEP_W8A8_MS))
@@ -363,7 +362,8 @@ class Workload:
             for m in SWEEP_W8A8_MS:
                 x = synthetic.activations(m, k, 100 * seed + 10 * si + m + 1, device=self.device)
                 self._pin_in(x)
-                kind = "w8a8_decode" if m <= W8A8_DECODE_MAX_M else "w8a8_prefill"
+                # above the decode range a W8A8 call runs on the tensor-core kernel
+                kind = "w8a8_decode" if m <= capi.I8QL_W8A8_DECODE_MAX_M else "w8a8_prefill"
                 self._linear(kind, x, qs[c], s, None, f"w8a8_linear {name}")
                 c += 1
 
@@ -1084,6 +1084,24 @@ def run_single(args, local):
         counts = np.diff(synthetic.moe_routing(tokens, seed=3).offsets)
         nbytes = bytes_moe(counts, tokens, hidden, inter, synthetic.DSMOE_ROUTED)
         flops = 2 * int(counts.sum()) * (inter2 * hidden + hidden * inter)
+    elif kind == "grouped":
+        tokens, proj = dims[0], ("gate_up", "down")[dims[1]]
+        n, k = synthetic.DSMOE_SHAPES[proj]
+        route = synthetic.moe_routing(tokens, seed=3)
+        counts = np.diff(route.offsets)
+        off = torch.from_numpy(route.offsets).to(dev)
+        e_count = route.experts
+        qs = []
+        for c in range(2):  # two weight sets of more than L2 each
+            q = torch.empty((e_count, n, k), dtype=torch.int8, device=dev)
+            sc = torch.empty((e_count, n), dtype=torch.float32, device=dev)
+            for e in range(e_count):
+                capi.quantize_weight_per_channel_int8(synthetic.weight(n, k, 1000 + e, device=dev), q=q[e], scale=sc[e])
+            qs.append((q, sc))
+        x = synthetic.activations(route.total_rows, k, 7, device=dev)
+        y = torch.empty((route.total_rows, n), dtype=torch.bfloat16, device=dev)
+        fns = [lambda q=q, sc=sc: capi.grouped_w8a16_gemm(x, off, q, sc, y=y) for q, sc in qs]
+        nbytes, flops = bytes_grouped(counts, n, k), 2 * int(counts.sum()) * n * k
     elif kind == "quant":
         r, k = dims
         copies = max(1, -(-l2 // (2 * r * k)))
@@ -1113,6 +1131,186 @@ def run_single(args, local):
     return 0
 
 
+SHAPE_GROUPS = ("decode", "prefill", "fp8", "w4", "grouped", "moe", "fused")
+
+
+def _graph_us(calls, reps=3):
+    """Median over three replays of a graph of `reps` passes over `calls`:
+    microseconds per call."""
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            for c in calls:
+                c()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e3 / reps / len(calls))
+    del g
+    return statistics.median(times)
+
+
+def _copies(nbytes):
+    """Weight copies a graph pass rotates through: more than L2 in total."""
+    return max(2, min(24, int(600e6 // max(1, nbytes)) + 1))
+
+
+def run_shapes(args, local):
+    """Per-shape timings of every path (the tables of the measured results):
+    each row is one call, replayed back to back in a CUDA graph over weight
+    copies that together exceed L2, so every call streams its weights from
+    HBM.  Rates are algorithmic bytes or 2*M*N*K per call time; fractions are
+    of the measured copy bandwidth and bf16 peak (FP8 against twice it)."""
+    from int8_quantized_linear_gb300 import capi, synthetic
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, _ = load_peaks()
+    hbm, bf16 = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    groups = SHAPE_GROUPS if args.shapes == "all" else tuple(args.shapes.split(","))
+    for g in groups:
+        if g not in SHAPE_GROUPS:
+            raise SystemExit(f"unknown shape group {g}")
+
+    def row(group, call, shape, m, n, k, us, nbytes=None, flops=None, peak_scale=1.0, **extra):
+        out = {"group": group, "call": call, "shape": shape, "M": m, "N": n, "K": k, "us": round(us, 3)}
+        if nbytes is not None:
+            out["GB/s"] = round(nbytes / us / 1e3, 1)
+            out["hbm_frac"] = round(nbytes / us / 1e3 / hbm, 4)
+        if flops is not None:
+            out["TOPS"] = round(flops / us / 1e6, 1)
+            out["tensor_frac"] = round(flops / us / 1e6 / (bf16 * peak_scale), 4)
+        out.update(extra)
+        print(json.dumps(out), flush=True)
+
+    i8 = {}  # int8 per-channel weights of the Qwen3-4B shapes, shared by the groups that use them
+
+    def int8_weights(name, n, k):
+        if name not in i8:
+            q, s = capi.quantize_weight_per_channel_int8(synthetic.weight(n, k, 1, device=dev))
+            i8[name] = ([q] + [q.clone() for _ in range(_copies(n * k) - 1)], s)
+        return i8[name]
+
+    if "decode" in groups:
+        for name, (n, k) in synthetic.QWEN3_4B_SHAPES.items():
+            ws = [synthetic.weight(n, k, 1 + c, device=dev) for c in range(_copies(2 * n * k))]
+            q = torch.empty((n, k), dtype=torch.int8, device=dev)
+            s = torch.empty((n,), dtype=torch.float32, device=dev)
+            us = _graph_us([lambda w=w: capi.quantize_weight_per_channel_int8(w, q=q, scale=s) for w in ws])
+            row("decode", "quantize_weight_per_channel_int8", name, 0, n, k, us, nbytes=bytes_quant(n, k))
+            del ws
+            qs, s = int8_weights(name, n, k)
+            for m in DECODE_MS:
+                x = synthetic.activations(m, k, 3, device=dev)
+                qx, sx = capi.quantize_act_per_token_int8(x)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                us = _graph_us([lambda q=q: capi.w8a16_gemm(x, q, s, y=y) for q in qs])
+                row("decode", "w8a16_gemm", name, m, n, k, us, nbytes=bytes_w8a16(m, n, k), flops=2 * m * n * k)
+                us = _graph_us([lambda q=q: capi.w8a8_gemm(qx, sx, q, s, y=y) for q in qs])
+                row("decode", "w8a8_gemm", name, m, n, k, us, nbytes=bytes_w8a8(m, n, k, False),
+                    flops=2 * m * n * k)
+    if "fused" in groups:
+        for name, (n, k) in synthetic.QWEN3_4B_SHAPES.items():
+            qs, s = int8_weights(name, n, k)
+            for m in DECODE_MS:
+                x = synthetic.activations(m, k, 3, device=dev)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                us1 = _graph_us([lambda q=q: capi.w8a8_linear(x, q, s, y=y, fused=True) for q in qs])
+                us2 = _graph_us([lambda q=q: capi.w8a8_linear(x, q, s, y=y) for q in qs])
+                row("fused", "w8a8_linear_fused", name, m, n, k, us1, nbytes=bytes_linear_fused(m, n, k, False),
+                    w8a8_linear_us=round(us2, 3), w8a8_linear_launches=capi.i8ql_w8a8_linear_launches(m, n, k))
+    if "prefill" in groups:
+        for name, (n, k) in synthetic.QWEN3_4B_SHAPES.items():
+            qs, s = int8_weights(name, n, k)
+            bias = synthetic.bias(n, 2, device=dev)
+            for m in PREFILL_MS:
+                x = synthetic.activations(m, k, 3, device=dev)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                us = _graph_us([lambda q=q: capi.w8a8_linear(x, q, s, bias=bias, y=y) for q in qs])
+                row("prefill", "w8a8_linear", name, m, n, k, us, flops=2 * m * n * k,
+                    plan=list(capi.i8ql_w8a8_plan(m, n, k)))
+    i8.clear()
+    if "fp8" in groups:
+        for name, (n, k) in synthetic.QWEN3_4B_SHAPES.items():
+            q, s = capi.quantize_weight_per_channel_fp8(synthetic.weight(n, k, 1, device=dev))
+            qs = [q] + [q.clone() for _ in range(_copies(n * k) - 1)]
+            bias = synthetic.bias(n, 2, device=dev)
+            for m in PREFILL_MS:
+                x = synthetic.activations(m, k, 3, device=dev)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                us = _graph_us([lambda q=q: capi.w8a8_fp8_linear(x, q, s, bias=bias, y=y) for q in qs])
+                qx, sx = capi.quantize_act_per_token_fp8(x)
+                us_g = _graph_us([lambda q=q: capi.w8a8_fp8_gemm(qx, sx, q, s, bias=bias, y=y) for q in qs])
+                f = 2 * m * n * k
+                row("fp8", "w8a8_fp8_linear", name, m, n, k, us, flops=f, peak_scale=2.0,
+                    gemm_us=round(us_g, 3), gemm_TOPS=round(f / us_g / 1e6, 1),
+                    plan=list(capi.i8ql_fp8_plan(m, n, k)))
+            del qs
+    if "w4" in groups:
+        for name, (n, k) in synthetic.QWEN3_8B_SHAPES.items():
+            ws = [synthetic.weight(n, k, 4 + c, device=dev) for c in range(_copies(2 * n * k))]
+            q4 = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+            s4 = torch.empty((n, k // 128), dtype=torch.bfloat16, device=dev)
+            us = _graph_us([lambda w=w: capi.quantize_weight_w4_g128(w, q=q4, scale=s4) for w in ws])
+            row("w4", "quantize_weight_w4_g128", name, 0, n, k, us, nbytes=bytes_quant_w4(n, k))
+            del ws
+            qs = [q4] + [q4.clone() for _ in range(_copies(n * k // 2) - 1)]
+            for m in W4_MS:
+                x = synthetic.activations(m, k, 5, device=dev)
+                y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+                us = _graph_us([lambda q=q: capi.w4a16_gemm(x, q, s4, y=y) for q in qs])
+                row("w4", "w4a16_gemm", name, m, n, k, us, nbytes=bytes_w4a16(m, n, k), flops=2 * m * n * k)
+            del qs
+    if "grouped" in groups or "moe" in groups:
+        e_count = synthetic.DSMOE_ROUTED + synthetic.DSMOE_SHARED
+        (inter2, hid), (_, inter) = synthetic.DSMOE_SHAPES["gate_up"], synthetic.DSMOE_SHAPES["down"]
+        sets = {}
+        for pname, (n, k) in synthetic.DSMOE_SHAPES.items():
+            sets[pname] = []
+            for c in range(3):  # three weight sets, each larger than L2
+                q = torch.empty((e_count, n, k), dtype=torch.int8, device=dev)
+                s = torch.empty((e_count, n), dtype=torch.float32, device=dev)
+                for e in range(e_count):
+                    capi.quantize_weight_per_channel_int8(synthetic.weight(n, k, 1000 + e, device=dev),
+                                                          q=q[e], scale=s[e])
+                sets[pname].append((q, s))
+        for tokens in MOE_TOKENS:
+            route = synthetic.moe_routing(tokens, seed=3)
+            counts = np.diff(route.offsets)
+            if "grouped" in groups:
+                off = torch.from_numpy(route.offsets).to(dev)
+                for pname, (n, k) in synthetic.DSMOE_SHAPES.items():
+                    x = synthetic.activations(route.total_rows, k, 7, device=dev)
+                    y = torch.empty((route.total_rows, n), dtype=torch.bfloat16, device=dev)
+                    us = _graph_us([lambda q=q, s=s: capi.grouped_w8a16_gemm(x, off, q, s, y=y)
+                                    for q, s in sets[pname]])
+                    row("grouped", "grouped_w8a16_gemm", pname, tokens, n, k, us,
+                        nbytes=bytes_grouped(counts, n, k), flops=2 * int(counts.sum()) * n * k,
+                        rows=int(counts.sum()), experts_with_rows=int((counts > 0).sum()))
+            if "moe" in groups:
+                x = synthetic.activations(tokens, hid, 8, device=dev)
+                lg = synthetic.gate_logits(tokens, synthetic.DSMOE_ROUTED, 3).to(dev)
+                o = torch.empty((tokens, hid), dtype=torch.bfloat16, device=dev)
+                us = _graph_us([lambda a=a, b=b: capi.moe_expert_mlp_w8a16(
+                    x, lg, synthetic.DSMOE_TOPK, synthetic.DSMOE_SHARED, a[0], a[1], b[0], b[1], out=o)
+                    for a, b in zip(sets["gate_up"], sets["down"])])
+                rows = int(counts.sum())
+                row("moe", "moe_expert_mlp_w8a16", "layer", tokens, hid, inter, us,
+                    nbytes=bytes_moe(counts, tokens, hid, inter, synthetic.DSMOE_ROUTED),
+                    flops=2 * rows * (inter2 * hid + hid * inter))
+    if capi.i8ql_get_device_error() != capi.I8QL_OK:
+        raise SystemExit("device error recorded during the shape table")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1130,17 +1328,22 @@ def main(argv=None):
     ap.add_argument("--ref-row-frac", type=float, default=1 / 8)
     ap.add_argument("--single", default=None,
                     help="time one call: w8a8:M:N:K, linear:M:N:K, w8a16:M:N:K, quant:R:K, "
-                         "w4a16:M:N:K, quant_w4:N:K, fp8:M:N:K (the FP8 linear layer) or moe:T "
-                         "(the DeepSeek-MoE expert MLP) (eager, for profiling)")
+                         "w4a16:M:N:K, quant_w4:N:K, fp8:M:N:K (the FP8 linear layer), moe:T "
+                         "(the DeepSeek-MoE expert MLP) or grouped:T:P (its grouped GEMM, P = 0 "
+                         "gate_up, 1 down) (eager, for profiling)")
+    ap.add_argument("--shapes", default=None,
+                    help="per-shape table instead of the step: comma-separated groups out of "
+                         + ",".join(SHAPE_GROUPS) + " (or all); CUDA-graph replays of back-to-back "
+                         "calls over weight copies larger than L2, one JSON line per shape")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
     world, rank, local = dist_env()
-    if args.single:
+    if args.single or args.shapes:
         from int8_quantized_linear_gb300 import build
         build.build()
-        return run_single(args, local)
+        return run_single(args, local) if args.single else run_shapes(args, local)
     if world > 1:
         import torch.distributed as dist
         if args.impl == "reference":

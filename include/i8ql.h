@@ -475,6 +475,19 @@ i8ql_status i8ql_w8a8_noalloc_plan(int64_t M, int64_t N, int64_t K, int32_t* til
                                    int32_t* cta_pair);
 
 /*
+ * Reports how many kernels one w8a8_linear call of this size launches on
+ * the current device, without launching anything: 0 for M == 0; 1 when the
+ * per-token quantization runs inside the decode GEMM (M <= 8 and a weight
+ * whose decode GEMM is one wave without split-K); 2 otherwise (the
+ * quantization launch, then the GEMM).
+ *
+ * No counterpart on the pages: a query for tests and profiling.  Same
+ * argument rules as w8a8_linear for M, N and K; *launches is a HOST pointer
+ * (null: I8QL_ERR_INVALID_ARG).
+ */
+i8ql_status i8ql_w8a8_linear_launches(int64_t M, int64_t N, int64_t K, int32_t* launches);
+
+/*
  * Waits for `stream`, then reads and clears the current device's sticky
  * kernel-error word.  Returns I8QL_OK, I8QL_ERR_TIMEOUT or
  * I8QL_ERR_BAD_OFFSETS (the first fault recorded since the last read), or

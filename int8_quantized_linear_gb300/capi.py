@@ -28,6 +28,7 @@ I8QL_ERR_NO_DEVICE = 6
 I8QL_ERR_WORKSPACE_LIMIT = 7
 I8QL_MAX_K = 133144
 I8QL_NOALLOC_MAX_ELEMENTS = 16 * 1024 * 1024
+I8QL_W8A8_DECODE_MAX_M = 32  # w8a8_gemm runs the decode kernel up to this M
 
 # Every symbol the C header declares, with its ctypes signature.
 _P, _I64, _S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
@@ -42,6 +43,7 @@ SIGNATURES = {
     "i8ql_w8a8_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
     "i8ql_fp8_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
     "i8ql_w8a8_noalloc_plan": (_S, [_I64, _I64, _I64, _P, _P, _P]),
+    "i8ql_w8a8_linear_launches": (_S, [_I64, _I64, _I64, _P]),
     "i8ql_get_device_error": (_S, [_P]),
     "i8ql_status_string": (ctypes.c_char_p, [_S]),
     "i8ql_version": (_S, []),
@@ -266,7 +268,7 @@ def _plan(fn_name: str, m: int, n: int, k: int) -> tuple[int, int, int]:
 def i8ql_w8a8_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
     """(tile width, split-K factor, CTA-pair mode: 0 single CTAs, 1 pairs,
     2 pairs with stream-K) w8a8_gemm uses for an M x N x K problem on the
-    current device; (0, 0, 0) in the decode range (M <= 32)."""
+    current device; (0, 0, 0) in the decode range (M <= I8QL_W8A8_DECODE_MAX_M)."""
     return _plan("i8ql_w8a8_plan", m, n, k)
 
 
@@ -279,6 +281,15 @@ def i8ql_fp8_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
 def i8ql_w8a8_noalloc_plan(m: int, n: int, k: int) -> tuple[int, int, int]:
     """The same for w8a8_gemm_noalloc (never stream-K)."""
     return _plan("i8ql_w8a8_noalloc_plan", m, n, k)
+
+
+def i8ql_w8a8_linear_launches(m: int, n: int, k: int) -> int:
+    """Kernels one w8a8_linear call of this size launches on the current
+    device: 1 with the quantization inside the decode GEMM, else 2 (0 for
+    m == 0)."""
+    launches = ctypes.c_int32(-1)
+    _check(lib().i8ql_w8a8_linear_launches(m, n, k, ctypes.byref(launches)), "i8ql_w8a8_linear_launches")
+    return launches.value
 
 
 def i8ql_get_device_error(stream=None) -> int:

@@ -468,6 +468,23 @@ i8ql_status i8ql_w8a8_noalloc_plan(int64_t M, int64_t N, int64_t K, int32_t* til
     return plan_query(M, N, K, false, tile_n, split_k, cta_pair);
 }
 
+i8ql_status i8ql_w8a8_linear_launches(int64_t M, int64_t N, int64_t K, int32_t* launches) {
+    I8QL_TRY(check_rows(M));
+    I8QL_TRY(check_k(K));
+    if (N <= 0) return I8QL_ERR_INVALID_ARG;
+    I8QL_TRY(check_rows(N));
+    if (launches == nullptr) return I8QL_ERR_INVALID_ARG;
+    if (M == 0) {
+        *launches = 0;
+        return I8QL_OK;
+    }
+    LaunchEnv env;
+    i8ql_status s;
+    if (!launch_env(nullptr, &env, &s)) return s;
+    *launches = w8a8_linear_one_launch(M, N, K, env.sm_count) ? 1 : 2;
+    return I8QL_OK;
+}
+
 i8ql_status i8ql_fp8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k, int32_t* cta_pair) {
     I8QL_TRY(check_rows(M));
     I8QL_TRY(check_k(K));

@@ -140,6 +140,10 @@ constexpr int64_t kW8A8FusedMaxM = 8;
 // Whether the one-launch kernel runs an N x K weight as one unsplit wave
 // (where it measured faster than a quantization launch plus the GEMM).
 bool w8a8_decode_fused_preferred(int64_t N, int64_t K, int sms);
+// Whether w8a8_linear takes the one-launch form for this problem.
+inline bool w8a8_linear_one_launch(int64_t M, int64_t N, int64_t K, int sms) {
+    return M > 0 && M <= kW8A8FusedMaxM && w8a8_decode_fused_preferred(N, K, sms);
+}
 cudaError_t launch_w8a8_decode_fused(const uint16_t* x, const int8_t* qw, const float* sw, const uint16_t* bias,
                                      uint16_t* y, int8_t* qx, float* sx, int32_t* acc, int64_t M, int64_t N, int64_t K,
                                      const LaunchEnv& env);

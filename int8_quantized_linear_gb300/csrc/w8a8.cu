@@ -128,7 +128,7 @@ cudaError_t launch_w8a8_linear(const uint16_t* x, const int8_t* qw, const float*
     // split-K shapes (qkv 9.1 against 8.3 us) and beyond one wave (Qwen3-8B
     // gate_up); its results are the same bit for bit, and it needs no
     // workspace.
-    if (M <= kW8A8FusedMaxM && w8a8_decode_fused_preferred(N, K, env.sm_count))
+    if (w8a8_linear_one_launch(M, N, K, env.sm_count))
         return launch_w8a8_decode_fused(x, qw, sw, bias, y, qx, sx, acc, M, N, K, env);
     LinearLayout l;
     cudaError_t e = linear_layout(M, N, K, qx != nullptr, sx != nullptr, env.sm_count, &l);

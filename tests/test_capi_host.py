@@ -270,3 +270,25 @@ def test_early_weight_loads_setting(lib):
     finally:
         lib.i8ql_set_early_weight_loads(0)
     assert lib.i8ql_early_weight_loads() == 0
+
+
+def test_w8a8_linear_launches_argument_errors(lib):
+    import ctypes
+    n = ctypes.c_int32(-1)
+    f = lib.i8ql_w8a8_linear_launches
+    assert f(8, 16, 40, ctypes.byref(n)) == capi.I8QL_ERR_UNSUPPORTED   # K % 16
+    assert f(8, 0, 64, ctypes.byref(n)) == capi.I8QL_ERR_INVALID_ARG    # N = 0
+    assert f(-1, 16, 64, ctypes.byref(n)) == capi.I8QL_ERR_INVALID_ARG
+    assert f(8, 16, 64, None) == capi.I8QL_ERR_INVALID_ARG
+    assert f(0, 16, 64, ctypes.byref(n)) == capi.I8QL_OK and n.value == 0  # nothing to launch
+    if not torch.cuda.is_available():
+        assert f(8, 16, 64, ctypes.byref(n)) == capi.I8QL_ERR_NO_DEVICE
+
+
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    for name in ("I8QL_MAX_K", "I8QL_W8A8_DECODE_MAX_M"):
+        m = re.search(rf"#define {name} (\d+)", text)
+        assert m and int(m.group(1)) == getattr(capi, name), name
+    m = re.search(r"#define I8QL_NOALLOC_MAX_ELEMENTS \((\d+) \* (\d+) \* (\d+)\)", text)
+    assert m and int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == capi.I8QL_NOALLOC_MAX_ELEMENTS

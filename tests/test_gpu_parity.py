@@ -406,6 +406,40 @@ def test_w8a8_stream_k_timeout_is_reported_and_recoverable():
     assert np.array_equal(acc2.astype(np.float64), exact)
 
 
+def _library_kernels(fn) -> int:
+    """Kernels of this library that fn() launches, counted by the profiler
+    (-1 if it records no device activity)."""
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+    if not names:
+        return -1
+    ours = ("decode_gemm_kernel", "quant_rows_kernel", "w8a8_fused_kernel", "i8_to_f16_kernel")
+    return sum(1 for n in names if any(o in n for o in ours))
+
+
+@pytest.mark.parametrize("m,n,k,expect", [(1, 19456, 2560, 1), (8, 12288, 4096, 1), (8, 2560, 2560, 2),
+                                          (9, 19456, 2560, 2), (1, 24576, 4096, 2), (64, 2560, 2560, 2),
+                                          (2048, 2560, 2560, 2)])
+def test_w8a8_linear_launch_count(m, n, k, expect):
+    """i8ql_w8a8_linear_launches names the form w8a8_linear takes: one launch
+    for few tokens on an unsplit one-wave decode GEMM (Qwen3-4B gate_up,
+    12288 x 4096), two otherwise (split-K, more than 8 tokens, more than a
+    wave, the tensor-core path); the profiler sees that many kernels."""
+    assert capi.i8ql_w8a8_linear_launches(m, n, k) == expect
+    assert capi.i8ql_w8a8_linear_launches(0, n, k) == 0
+    x = dev(synthetic.activations(m, k, 5))
+    qw = torch.zeros((n, k), dtype=torch.int8, device="cuda")
+    sw = torch.ones((n,), dtype=torch.float32, device="cuda")
+    y = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    capi.w8a8_linear(x, qw, sw, y=y)  # the stream-ordered workspace pool warms up outside the count
+    seen = _library_kernels(lambda: capi.w8a8_linear(x, qw, sw, y=y))
+    assert seen in (-1, expect), seen
+
+
 @pytest.mark.parametrize("m,n,k", [(1, 256, 1024), (7, 300, 2064), (64, 513, 1040), (65, 640, 2560),
                                    (128, 2560, 2560), (300, 1000, 4160), (2048, 2560, 2560),
                                    (3, 19456, 2560), (8, 12288, 4096)])
