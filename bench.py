@@ -194,6 +194,9 @@ KERNEL_SOURCES = {
     "sweep8b": {"w8a16": ["decode_gemm.cu"], "w8a8_decode": ["decode_gemm.cu", "quant.cu"],
                 "w8a8_prefill": ["w8a8.cu", "w8a8_fused.cu", "tc_common.cuh", "quant.cu"]},
     "w4": {"w4a16": ["w4a16.cu"], "quant_w4": ["w4a16.cu", "quant_math.cuh"]},
+    "fp8": {"fp8": ["fp8_gemm.cu", "tc_common.cuh", "quant.cu", "quant_math.cuh"]},
+    "moe": {"moe_mlp": ["moe.cu", "decode_gemm.cu"]},
+    "fused": {"w8a8_fused": ["decode_gemm.cu", "quant_math.cuh"]},
 }
 
 
@@ -214,7 +217,8 @@ def ncu_traffic(kernel, part):
     with open(path) as fh:
         table = json.load(fh)
     entry = table.get(part, {}).get(kernel)
-    if not entry or entry.get("source_sha256_16") != kernel_source_hash(kernel, part):
+    if not entry or kernel not in KERNEL_SOURCES.get(part, {}) or \
+            entry.get("source_sha256_16") != kernel_source_hash(kernel, part):
         return None
     return entry.get("dram_bytes_per_launch")
 
