@@ -142,7 +142,8 @@ i8ql_status w8a8_gemm(const int8_t* qx, const float* sx, const int8_t* qw, const
  * the tensor-core GEMM reads, so the GEMM needs no separate conversion pass;
  * for M <= 8 with a weight whose decode GEMM is one wave without split-K
  * (large N, up to about 600 row blocks of 32) it is w8a8_linear_fused (one
- * launch).
+ * launch); otherwise a quantization launch and the GEMM
+ * (i8ql_w8a8_linear_launches reports which).
  * Inputs: x bf16 [M, K], qw int8 [N, K], sw fp32 [N], bias bf16 [N] or NULL.
  * Outputs: y bf16 [M, N]; qx int8 [M, K] and sx fp32 [M] receive the token
  * codes and scales when given (each may be NULL); acc_debug int32 [M, N] or

@@ -685,8 +685,9 @@ def _experts(e_count, n, k, seed):
                                     [0, 17, 0, 33, 0], [200, 1, 0, 3, 100], [8, 9, 16, 17, 0, 64],
                                     [64] * 3 + [1] * 9])
 def test_grouped_small(counts):
-    """Uneven groups, including experts with many token chunks (more rows
-    than experts: their later chunks run on extra slots of their own)."""
+    """Uneven groups, including experts with many token chunks (each CTA of
+    such an expert loops over its 8-token chunks) and per-row expert slots
+    (few rows: one slot per row, the empty experts launch nothing)."""
     n, k = 40, 80
     q, s = _experts(len(counts), n, k, 50)
     off = np.zeros(len(counts) + 1, np.int32)
