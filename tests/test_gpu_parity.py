@@ -777,6 +777,27 @@ def test_grouped_few_rows_compact_slots(placement):
     check_elementwise(y, ref, oracle.grouped_w8a16(ax, off, aq, s), k)
 
 
+@pytest.mark.parametrize("e_count,rows", [(256, 128), (257, 3), (1000, 40), (65535, 20)])
+def test_grouped_many_experts(e_count, rows):
+    """Expert counts at and past the per-row slot limit (E <= 256 with at
+    most E/2 rows), up to the largest E the launch grid takes (65,535):
+    rows scattered over the experts, random int8 codes and scales."""
+    n, k = 16, 32
+    g = np.random.default_rng(e_count + rows)
+    q = g.integers(-127, 128, (e_count, n, k)).astype(np.int8)
+    s = g.uniform(1e-3, 2e-3, (e_count, n)).astype(np.float32)
+    counts = np.bincount(g.integers(0, e_count, rows), minlength=e_count)
+    off = np.zeros(e_count + 1, np.int32)
+    off[1:] = np.cumsum(counts)
+    x = synthetic.activations(rows, k, e_count)
+    y = gpu_grouped(x, off, q, s)
+    assert capi.i8ql_get_device_error() == capi.I8QL_OK
+    xb = util.bits(x)
+    ref = oracle.grouped_w8a16(xb, off, q, s)
+    ax, aq = _abs_inputs(xb, q)
+    check_elementwise(y, ref, oracle.grouped_w8a16(ax, off, aq, s), k)
+
+
 def test_grouped_bad_offsets_reported_with_few_rows():
     """The per-row slot launch checks every expert's offsets too."""
     n, k = 16, 32
