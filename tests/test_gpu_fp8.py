@@ -154,12 +154,14 @@ def test_fp8_gemm_small_integers_exact():
     """Codes of +-1 .. +-16 (products are integers up to 256, every partial
     sum an integer below 2^24): the fp32 accumulator is exact, so the output
     is the fp32 epilogue of the exact sum to within one bf16 ulp.  This pins
-    the operand layout, descriptors and tile edges (ragged M, N, K)."""
+    the operand layout, descriptors and tile edges (ragged M, N, K, down to a
+    single output channel)."""
     ints = np.arange(1, 17, dtype=np.float32)
     codes = oracle.fp8_encode(ints)
     assert np.array_equal(oracle.fp8_decode(codes), ints)
     for (m, n, k) in [(1, 16, 16), (7, 40, 48), (129, 300, 1040), (256, 256, 4096), (300, 513, 2064),
-                      (64, 640, 4096), (128, 520, 9728)]:
+                      (64, 640, 4096), (128, 520, 9728), (1, 1, 16), (40, 1, 16), (300, 3, 64),
+                      (2048, 5, 128)]:
         g = np.random.default_rng(m + n + k)
         qx = codes[g.integers(0, 16, (m, k))] | (g.integers(0, 2, (m, k)) * 0x80).astype(np.uint8)
         qw = codes[g.integers(0, 16, (n, k))] | (g.integers(0, 2, (n, k)) * 0x80).astype(np.uint8)
