@@ -188,6 +188,30 @@ def test_fp8_gemm_shapes(m, n, k):
     check_gemm(qx, sx, qw, sw, bias)
 
 
+@pytest.mark.parametrize("m,n,k", [(300, 1000, 2560), (2048, 512, 1024), (64, 24, 512)])
+def test_fp8_gemm_unaligned_scales_and_bias(m, n, k):
+    """Weight scales and bias that start off a 16-byte boundary (4- and
+    2-byte aligned, the least the boundary allows) give, bit for bit, the
+    output of the call with 16-byte-aligned copies, for several launch
+    forms (CTA pairs, single CTAs)."""
+    qx, sx = _fp8_codes(m, k, m + 1)
+    qw, sw = _fp8_codes(n, k, n + 2, 0.02)
+    bias = synthetic.bias(n, n + 3).cuda()
+    qx_d, sx_d, qw_d = (torch.from_numpy(a).cuda() for a in (qx, sx, qw))
+    sw_al = torch.from_numpy(sw).cuda()
+    sw_buf = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
+    sw_buf[1:] = sw_al
+    b_buf = torch.zeros(n + 1, dtype=torch.bfloat16, device="cuda")
+    b_buf[1:] = bias
+    y_al = capi.w8a8_fp8_gemm(qx_d, sx_d, qw_d, sw_al, bias=bias)
+    y_un = capi.w8a8_fp8_gemm(qx_d, sx_d, qw_d, sw_buf[1:], bias=b_buf[1:])
+    y_nb = capi.w8a8_fp8_gemm(qx_d, sx_d, qw_d, sw_buf[1:])
+    y_nb_al = capi.w8a8_fp8_gemm(qx_d, sx_d, qw_d, sw_al)
+    torch.cuda.synchronize()
+    assert torch.equal(y_al.view(torch.int16), y_un.view(torch.int16))
+    assert torch.equal(y_nb.view(torch.int16), y_nb_al.view(torch.int16))
+
+
 @pytest.mark.parametrize("m,n,k", [(3, 40, 131072), (130, 257, 65552)])
 def test_fp8_gemm_longest_k(m, n, k):
     """The longest K the exact oracle covers (2^17 products: its fp64 sum of
