@@ -54,3 +54,34 @@ def test_byte_counts():
     counts = np.array([0, 2, 0, 5])
     # experts without rows read nothing
     assert bench.bytes_grouped(counts, n, k) == 2 * (n * k + 4 * n) + 2 * 7 * (k + n)
+
+
+def _res(per, peaks=None):
+    return {"per": per, "peaks": (peaks or {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0,
+                                             "bf16_tflops_sustained": 1800.0}, "measured")}
+
+
+def test_roofline_hbm_class():
+    """An HBM-bound class: achieved = algorithmic bytes per launch / mean
+    launch time, against the copy peak; the dominant class is the one with
+    the most time."""
+    per = {"w8a16": {"ms": 2.0, "launches": 4, "bytes": 4 * 24e6, "flops": 0.0},
+           "grouped": {"ms": 6.0, "launches": 2, "bytes": 2 * 150e6, "flops": 0.0}}
+    r = bench.roofline("decode", _res(per))
+    assert r["kernel"] == "grouped" and r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - 150e6 / 3e-3 / 1e9) < 1e-9          # 50 GB/s
+    assert abs(r["frac"] - r["achieved"] / 6000.0) < 1e-12
+    assert r["algorithmic_bytes_per_launch"] == 150e6
+    r16 = bench.roofline("decode", _res(per), "w8a16")
+    assert abs(r16["achieved"] - 24e6 / 0.5e-3 / 1e9) < 1e-9
+
+
+def test_roofline_tensor_classes_take_their_pipe_peak():
+    per = {"fp8": {"ms": 1.0, "launches": 10, "bytes": 1e9, "flops": 2e12}}
+    r = bench.roofline("fp8", _res(per))
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 2000.0) < 1e-9                       # 2e12 flop in 1 ms
+    assert r["peak"] == 2 * 2000.0 and abs(r["frac"] - 0.5) < 1e-12  # the 8-bit pipe: twice bf16
+    per = {"w8a8": {"ms": 1.0, "launches": 10, "bytes": 1e9, "flops": 1e12}}
+    r = bench.roofline("prefill", _res(per))
+    assert r["peak"] == 2000.0 and abs(r["frac"] - 0.5) < 1e-12
