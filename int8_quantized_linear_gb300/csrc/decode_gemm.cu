@@ -164,15 +164,17 @@ struct WeightRegs {
 //           weight stream) is loaded one k-step ahead.
 // W8A8 streams without conversion and keeps a deep ring.  W8A16 with one
 // token tile trades ring depth for the token prefetch; its grouped form
-// (many short expert GEMMs) does better with more CTAs per SM instead.
+// (many short expert GEMMs) does better with more CTAs per SM instead, and
+// with 16-row warps (MT = 1, small launches only) with more still.
 // Wider token tiles have no registers to spare for the prefetch.
-template <Op OP, int NT, bool GROUPED>
+template <Op OP, int MT, int NT, bool GROUPED>
 struct Tuning {
     static constexpr bool kW8A16One = OP == Op::kW8A16 && NT == 1;
     static constexpr bool kInt = OP != Op::kW8A16;  // int8 x int8 -> int32
     // (the token quantization of kW8A8Q needs the registers of one stage)
     static constexpr int kStages = OP == Op::kW8A8 ? 4 : (OP == Op::kW8A8Q ? 3 : (NT == 1 ? 2 : 3));
-    static constexpr int kMinCtas = (kW8A16One && GROUPED) ? 6 : (NT <= 2 ? 4 : (NT <= 4 ? 3 : 2));
+    static constexpr int kMinCtas =
+        (kW8A16One && GROUPED) ? (MT == 1 ? 8 : 6) : (NT <= 2 ? 4 : (NT <= 4 ? 3 : 2));
     static constexpr bool kXAhead = kInt ? NT <= 2 : (kW8A16One && !GROUPED);
 };
 
@@ -180,12 +182,12 @@ struct Tuning {
 constexpr int kCompactExperts = 256;  // grouped: largest E for per-row expert slots
 
 template <Op OP, int MT, int NT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
+__global__ void __launch_bounds__(kThreads, (Tuning<OP, MT, NT, GROUPED>::kMinCtas))
     decode_gemm_kernel(const DecodeParams p) {
     using Acc = std::conditional_t<OP != Op::kW8A16, int32_t, float>;
     constexpr int kRows = 16 * MT;
     constexpr int kToks = 8 * NT;
-    constexpr int kStages = Tuning<OP, NT, GROUPED>::kStages;
+    constexpr int kStages = Tuning<OP, MT, NT, GROUPED>::kStages;
     __shared__ Acc part[kWarps][kToks * kRows];
 
     // Before waiting for the previous kernel, start streaming this CTA's
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, (Tuning<OP, NT, GROUPED>::kMinCtas))
         {
             // main loop: full k-steps through a kStages-deep register ring
             // of weights (the token operand one k-step ahead if kXAhead)
-            constexpr bool kXAhead = Tuning<OP, NT, GROUPED>::kXAhead;
+            constexpr bool kXAhead = Tuning<OP, MT, NT, GROUPED>::kXAhead;
             WeightRegs<MT> ring[kStages];
 #pragma unroll
             for (int s = 0; s < kStages; ++s)
@@ -656,6 +658,15 @@ cudaError_t launch_auto(DecodeParams p, int64_t groups_hint, int sms, cudaStream
 
 template <Op OP, bool GROUPED>
 cudaError_t dispatch(const DecodeParams& p, int64_t tokens_hint, int64_t groups_hint, int sms, cudaStream_t stream) {
+    if constexpr (GROUPED && OP == Op::kW8A16) {
+        // A grouped launch small enough that its 16-row CTAs still fit in
+        // one wave spreads over more SMs with them (DeepSeek-MoE down at one
+        // token: 12.3 -> 10.5 us; gate_up, past one wave, stays at 32 rows).
+        // The fused gate/up form pairs 16 gate and 16 up rows: 32 rows.
+        if (tokens_hint <= 8 && !p.glu &&
+            row_blocks_of<1>(p) * expert_slots<GROUPED>(p) <= (int64_t)sms * resident_ctas<OP, 1, 1, GROUPED>())
+            return launch_auto<OP, 1, 1, GROUPED>(p, groups_hint, sms, stream);
+    }
     if (tokens_hint <= 8) return launch_auto<OP, 2, 1, GROUPED>(p, groups_hint, sms, stream);
     if (tokens_hint <= 16) return launch_auto<OP, 2, 2, GROUPED>(p, groups_hint, sms, stream);
     if (tokens_hint <= 32) return launch_auto<OP, 2, 4, GROUPED>(p, groups_hint, sms, stream);
