@@ -470,7 +470,8 @@ i8ql_status i8ql_w8a8_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int
 
 /*
  * The same report for w8a8_gemm_noalloc, which never runs stream-K (its
- * fixed array holds only the token codes): *cta_pair is 0 or 1.
+ * fixed array holds only the token codes): *cta_pair is 0 or 1.  No
+ * counterpart on the pages: a query for tests and profiling.
  */
 i8ql_status i8ql_w8a8_noalloc_plan(int64_t M, int64_t N, int64_t K, int32_t* tile_n, int32_t* split_k,
                                    int32_t* cta_pair);
@@ -492,14 +493,17 @@ i8ql_status i8ql_w8a8_linear_launches(int64_t M, int64_t N, int64_t K, int32_t* 
  * Waits for `stream`, then reads and clears the current device's sticky
  * kernel-error word.  Returns I8QL_OK, I8QL_ERR_TIMEOUT or
  * I8QL_ERR_BAD_OFFSETS (the first fault recorded since the last read), or
- * I8QL_ERR_CUDA if the wait itself failed.
+ * I8QL_ERR_CUDA if the wait itself failed.  No counterpart on the pages:
+ * the failure signal of the kernels' bounded waits and offset checks.
  */
 i8ql_status i8ql_get_device_error(void* stream);
 
-/* Static, NUL-terminated description of a status code. */
+/* Static, NUL-terminated description of a status code (no counterpart on
+ * the pages; never NULL, "unknown status" for codes outside the enum). */
 const char* i8ql_status_string(i8ql_status status);
 
-/* Library version as major * 10000 + minor * 100 + patch. */
+/* Library version as major * 10000 + minor * 100 + patch (no counterpart
+ * on the pages). */
 int32_t i8ql_version(void);
 
 /*

@@ -292,3 +292,19 @@ def test_binding_constants_match_the_header():
         assert m and int(m.group(1)) == getattr(capi, name), name
     m = re.search(r"#define I8QL_NOALLOC_MAX_ELEMENTS \((\d+) \* (\d+) \* (\d+)\)", text)
     assert m and int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == capi.I8QL_NOALLOC_MAX_ELEMENTS
+
+
+def test_every_declaration_cites_its_source():
+    """Each comment that documents header declarations names the passage the
+    operation follows ("Source:"), or says it has none on the pages."""
+    text = open(HEADER).read()
+    blocks = re.findall(r"/\*(.*?)\*/\s*((?:(?:i8ql_status|int32_t|const char\*|void)\s+\w+\s*\([^;]*\);\s*)+)",
+                        text, re.S)
+    documented = set()
+    for comment, decls in blocks:
+        names = re.findall(r"(\w+)\s*\(", decls)
+        flat = " ".join(" ".join(line.strip().lstrip("*").split()) for line in comment.splitlines()).strip()
+        assert "Source:" in flat or "no counterpart on the pages" in flat.lower(), names
+        documented.update(names)
+    missing = set(_declared_functions()) - documented
+    assert not missing, f"declarations without a comment: {sorted(missing)}"
