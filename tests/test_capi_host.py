@@ -298,8 +298,8 @@ def test_every_declaration_cites_its_source():
     """Each comment that documents header declarations names the passage the
     operation follows ("Source:"), or says it has none on the pages."""
     text = open(HEADER).read()
-    blocks = re.findall(r"/\*(.*?)\*/\s*((?:(?:i8ql_status|int32_t|const char\*|void)\s+\w+\s*\([^;]*\);\s*)+)",
-                        text, re.S)
+    blocks = re.findall(r"/\*(.*?)\*/\s*(?:#define[^\n]*\n\s*)*"
+                        r"((?:(?:i8ql_status|int32_t|const char\*|void)\s+\w+\s*\([^;]*\);\s*)+)", text, re.S)
     documented = set()
     for comment, decls in blocks:
         names = re.findall(r"(\w+)\s*\(", decls)
