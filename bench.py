@@ -60,6 +60,11 @@ cpu_baseline times the CPU oracle (the only reference implementation: the
 pages ship no code) on the host cores, with one thread and with every core,
 on a bounded sample of the same workload; --impl reference times it with
 every core.
+
+Other modes: --single KIND:DIMS times one call eagerly (for ncu captures of
+one kernel); --shapes GROUPS prints one JSON line per shape and call of
+every path (CUDA-graph replays over weight copies larger than L2), the
+per-call tables of the measured results.
 """
 
 from __future__ import annotations
