@@ -1057,11 +1057,19 @@ Plan choose_plan(int dev, int64_t M, int64_t N, int64_t K, int sms, bool swap, b
         // the same at any tile width, so the alternative costs its fewest
         // waves of whole tiles times nkb; stream-K costs an even share of
         // all k-blocks plus the fix-up.
+        // Its per-pair ranges spread the tiles running at one time over the
+        // whole problem, so the operand panels they share stop hitting in
+        // L2: with deep K over many waves that costs more DRAM traffic than
+        // the tail it removes (Qwen3-8B down at M = 8,192, K = 12,288, 6.7
+        // waves: 680 against 570 us, DRAM traffic 7x the algorithmic bytes),
+        // while at K = 4,096 and 10 waves stream-K still wins (qkv at
+        // M = 8,192: 300 against 322 us).
         constexpr int bn = 256;
         const int64_t pairs = active_clusters(dev, bn, true, 2);
         const int64_t ta = (M + 2 * kBM - 1) / (2 * kBM);
         const int64_t tiles = ta * ((N + bn - 1) / bn);
-        if (pairs >= 2 && tiles > pairs) {
+        const bool deep_many_waves = K >= 8192 && tiles > 3 * pairs;
+        if (pairs >= 2 && tiles > pairs && !deep_many_waves) {
             int64_t whole = INT64_MAX;
             for (int w : kPairWidths) {
                 const int64_t pw = active_clusters(dev, w, true, 2);
